@@ -1,0 +1,188 @@
+/*
+ * idx.h -- C ABI of libidx.so, the GB300 (sm_103a) sparse-attention indexer.
+ *
+ * Two stages, each one asynchronous launch on the caller's stream:
+ *   1. paged FP8 MQA logits   ("flashinfer.attn_scores", fp8_paged_mqa_logits)
+ *   2. threshold top-k select  ("flashinfer.sdsa.indexer_threshold_select"), reading stage 1's
+ *      logits
+ * plus the persistent work split of stage 1 ("flashinfer.attn_scores", Scheduling and Setup)
+ * and the two integer helpers named there.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked "device" are caller-owned device memory; the library never allocates,
+ *     frees or synchronises, so every call can be captured in a CUDA graph once it has run
+ *     eagerly one time (that first call loads the kernels).  `stream` is a cudaStream_t
+ *     (NULL = the legacy default stream).
+ *   - Return value: IDX_OK, or an error code; idx_last_error() then describes it.  On any
+ *     error other than IDX_CUDA nothing has been launched.
+ *   - Content preconditions (table width, seq_lens <= max_seq_len, page ids inside the pool)
+ *     are the caller's, as on the pages; the kernels never read or write outside the buffers
+ *     the arguments describe, even when they are violated (out-of-pool page ids are skipped
+ *     and flagged, see idx_device_status).  With the environment variable IDX_VALIDATE=1 the
+ *     logits call also copies seq_lens and block_tables to the host and checks them, returning
+ *     IDX_CONTRACT on a violation (skipped while the stream is being captured, where such a
+ *     copy is illegal).
+ */
+#ifndef IDX_H
+#define IDX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define IDX_OK 0
+#define IDX_INVALID_ARG 1 /* null pointer, bad size/stride/alignment, inconsistent shapes */
+#define IDX_UNSUPPORTED 2 /* a shape this build has no kernel for (see idx_logits_fp8) */
+#define IDX_CUDA 3        /* a CUDA runtime/driver call or launch failed */
+#define IDX_CONTRACT 4    /* IDX_VALIDATE=1 found a violated content precondition */
+
+/* Device-side status bits (idx_device_status). */
+#define IDX_DEV_WAIT_TIMEOUT 1 /* a pipeline wait gave up after its time limit */
+#define IDX_DEV_BAD_PAGE 2     /* a needed block-table entry was outside [0, num_blocks) */
+
+/* Description of the most recent error on the calling thread ("" if none). */
+const char *idx_last_error(void);
+
+/*
+ * padded_seq_len ("flashinfer.attn_scores", Scheduling and Setup; Example: 8000 -> 8192): the
+ * minimum column count of a logits output row.  The pages give no granularity; this build
+ * rounds up to a multiple of 256 (see idx_logits_fp8 for why any row stride >= this value
+ * works).  Returns -1 for a negative argument.  Host-only arithmetic.
+ */
+int64_t idx_padded_seq_len(int64_t max_seq_len);
+
+/*
+ * min_block_table_width ("flashinfer.attn_scores", Scheduling and Setup; Parameters:
+ * block_tables; Example: ceil(8000/32) = 250): ceil(seq_len / block_size), the fewest
+ * block-table columns a request of seq_len tokens needs.  Returns -1 on a negative seq_len or
+ * a non-positive block_size.  Host-only arithmetic.
+ */
+int64_t idx_min_block_table_width(int64_t seq_len, int32_t block_size);
+
+/* The SM count of the current device (the default persistent grid).  Needs a GPU. */
+int idx_num_sms(int32_t *num_sms_out);
+
+/*
+ * idx_schedule ("flashinfer.attn_scores", Parameters: schedule_meta; Scheduling and Setup):
+ * the persistent logits kernel's work split, computed on the device from seq_lens' current
+ * contents, so it can be captured and re-derives itself on every replay.
+ *
+ *   seq_lens         device int32, element b at seq_lens[b * seq_lens_stride] (stride >= 1, so
+ *                    a view like seq_lens[::next_n] is taken without a copy)
+ *   batch            number of requests, 0 .. 4096
+ *   next_n           draft depth 1..4 (the split does not depend on it; checked for symmetry
+ *                    with the logits call)
+ *   num_sms          CTAs of the persistent grid, 1 .. 1024; 0 = this device's SM count
+ *   schedule         device int32 [num_sms + 1][2], written: entry c is the (request, tile)
+ *                    at which CTA c starts, where request b owns ceil(seq_lens[b] / 128) tiles
+ *                    of 128 positions and CTA c takes the flat tiles
+ *                    [floor(c*U/num_sms), floor((c+1)*U/num_sms)) of the U in all; the last
+ *                    entry is (batch, 0).  Valid only while seq_lens' contents and num_sms are
+ *                    unchanged; a stale one gives wrong coverage but never a hang.
+ */
+int idx_schedule(const int32_t *seq_lens, int64_t seq_lens_stride, int32_t batch, int32_t next_n,
+                 int32_t num_sms, int32_t *schedule, void *stream);
+
+/*
+ * idx_logits_fp8 ("flashinfer.attn_scores", fp8_paged_mqa_logits: formula block, Note,
+ * Parameters, Returns):
+ *
+ *   out[(b*next_n + t) * out_row_stride + p] =
+ *       scale[p] * sum_h weights[b*next_n + t, h] * relu(q[b, t, h, :] . k[p, :])
+ *
+ * for every request b with seq_lens[b] > 0, slot t < next_n and position p < seq_lens[b].
+ * Only p <= seq_lens[b] - next_n + t is meaningful for slot t (the pages' per-slot extent);
+ * positions in [that + 1, seq_lens[b]) hold the same formula's value, columns >= seq_lens[b]
+ * are not written, and rows of a request with seq_lens[b] == 0 are never written.
+ *
+ *   q               device e4m3 bytes [batch, next_n, num_heads, head_dim], contiguous,
+ *                   16-byte aligned
+ *   kv_fused        device uint8 [num_blocks][block_size*(head_dim+4)], 16-byte aligned: per
+ *                   block, all e4m3 values token-major (token i at i*head_dim), then
+ *                   block_size little-endian float32 scales (token i's at
+ *                   block_size*head_dim + 4*i)
+ *   num_blocks      blocks in the pool (>= 1; num_blocks * (block_size*(head_dim+4)/128) must
+ *                   stay below 2^31)
+ *   block_size      tokens per block
+ *   weights         device float32 [batch*next_n, num_heads], contiguous, 16-byte aligned
+ *   block_tables    device int32; request b's j-th block id at block_tables[b*bt_row_stride+j];
+ *                   only j < ceil(seq_lens[b]/block_size) is ever read
+ *   bt_row_stride   >= bt_width (a row-strided view like block_tables[::next_n] is fine)
+ *   bt_width        columns per row, >= ceil(max(seq_lens)/block_size) (caller's contract)
+ *   seq_lens        device int32, seq_lens[b * seq_lens_stride], each 0 .. max_seq_len
+ *   batch           0 .. 4096
+ *   next_n          1 .. 4 (draft depth; slot t = next_n - 1 is the newest and sees the whole
+ *                   sequence)
+ *   num_heads, head_dim, block_size   this build supports 64, 128, 64 (IDX_UNSUPPORTED else)
+ *   max_seq_len     >= every seq_lens[b]
+ *   schedule        device int32 [num_sms+1][2] from idx_schedule with the same seq_lens and
+ *                   num_sms, or NULL to derive the split inside the kernel (recommended)
+ *   num_sms         CTAs of the persistent grid (0 = this device's SM count)
+ *   out             device float32, rows of out_row_stride floats, 16-byte aligned
+ *   out_row_stride  >= idx_padded_seq_len(max_seq_len) and a multiple of 4
+ *   row_ends_out    NULL, or device int32 [batch*next_n] receiving
+ *                   max(0, seq_lens[b] - next_n + t + 1) for every row (zero-length requests
+ *                   included), ready for idx_threshold_select
+ */
+int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t num_blocks,
+                   int32_t block_size, const float *weights, const int32_t *block_tables,
+                   int64_t bt_row_stride, int32_t bt_width, const int32_t *seq_lens,
+                   int64_t seq_lens_stride, int32_t batch, int32_t next_n, int32_t num_heads,
+                   int32_t head_dim, int32_t max_seq_len, const int32_t *schedule,
+                   int32_t num_sms, float *out, int64_t out_row_stride, int32_t *row_ends_out,
+                   void *stream);
+
+/*
+ * idx_threshold_select ("flashinfer.sdsa.indexer_threshold_select": description; Parameters
+ * row_ends, thresholds, counters, candidates, max_context, top_k, arrivals, ranges), over
+ * logits already written by idx_logits_fp8.  One launch, no host synchronisation.
+ *
+ * For row r, key i < row_ends[r] with score s = logits[r*logits_row_stride + i] and
+ * thr = thresholds[r]: s > thr makes a candidate, "neither above nor below" (s == thr or NaN)
+ * a tie.  The n-th candidate is stored at slot top_k + n when n < capacity, the n-th tie at
+ * slot top_k - 1 - n when n < top_k; a slot holds the pair (key index, raw float32 bits of s).
+ * counters[r] counts both, stored or not; the order of stored items is unspecified.
+ *
+ * With K' = min(row_ends[r], top_k) a row fits when candidates <= capacity and either
+ * candidates >= K' or (ties <= top_k and candidates + ties >= K'): then every item of its
+ * exact top-K' (descending value, ties to the lowest index) is in its slots.
+ *
+ * With arrivals (and ranges), the last CTA of each row to finish repairs a row that does not
+ * fit: it finds the row's K'-th largest score v by radix select over totalOrder keys, stores
+ * the keys above v as candidates and the lowest-index keys equal to v as ties (exactly K'
+ * items), sets counters[r] to those counts, thresholds[r] = v, and resets arrivals[r] to 0.
+ * Every row then holds its exact top-K' and ranges[0*rows + r] .. ranges[1*rows + r] (half
+ * open) is the slot range holding its candidates and ties.
+ *
+ *   logits            device float32, 16-byte aligned, row stride a multiple of 4
+ *   row_ends          device int32 [rows], 0 .. max_context
+ *   rows              1 .. 65535
+ *   thresholds        device float32 [rows], read, and written for repaired rows
+ *   counters          device int32 [rows][2] (candidates, ties), ZEROED BY THE CALLER
+ *   candidates        device int32 [rows][top_k + capacity][2]
+ *   top_k             >= 1 (the number of tie slots)
+ *   capacity          >= 0 candidate slots; >= top_k - 1 when arrivals is given
+ *   max_context       the most keys a row sees; sizes the grid (one CTA per 8192 keys)
+ *   arrivals          NULL (no repair), or device int32 [rows], zeroed once; every call
+ *                     leaves it zeroed
+ *   ranges            device int32 [2][rows]; required when arrivals is given, else ignored
+ */
+int idx_threshold_select(const float *logits, int64_t logits_row_stride, const int32_t *row_ends,
+                         int32_t rows, float *thresholds, int32_t *counters, int32_t *candidates,
+                         int32_t top_k, int32_t capacity, int32_t max_context, int32_t *arrivals,
+                         int32_t *ranges, void *stream);
+
+/*
+ * Reads (and, if clear != 0, resets) the OR of the device-side status bits (IDX_DEV_*) that
+ * every kernel of this library has raised on the current device since the last reset.
+ * Synchronous (it copies from the device); a debugging aid, not for the hot path.
+ */
+int idx_device_status(int32_t *status_out, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IDX_H */

@@ -1,0 +1,225 @@
+"""GB300 (sm_103a) sparse-attention indexer: paged FP8 MQA logits and threshold top-k select.
+
+A thin ctypes binding over ``libidx.so`` (declared in ``include/idx.h``).  It only marshals
+arguments: every step of the indexer runs in the library's CUDA kernels, and there is no CPU
+fallback -- if the library has not been built, every call raises.
+
+Low-level names mirror the C ABI (``idx_logits_fp8``, ``idx_threshold_select``, ``idx_schedule``,
+``idx_padded_seq_len``, ``idx_min_block_table_width``, ...); they take raw pointers and sizes.
+The torch-facing helpers (``logits_fp8``, ``threshold_select``, ``schedule``) take tensors,
+check dtypes/devices, and pass pointers, strides and the current CUDA stream through.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+_HERE = Path(__file__).resolve().parent
+LIB_PATH = _HERE / "libidx.so"
+
+IDX_OK = 0
+IDX_INVALID_ARG = 1
+IDX_UNSUPPORTED = 2
+IDX_CUDA = 3
+IDX_CONTRACT = 4
+IDX_DEV_WAIT_TIMEOUT = 1
+IDX_DEV_BAD_PAGE = 2
+
+TILE_TOKENS = 128  # KV positions per work unit of the persistent logits kernel
+
+_lib = None
+
+
+class IdxError(RuntimeError):
+    """A non-zero status from libidx.so."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"libidx status {status}: {message}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded ``libidx.so``.  Raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not LIB_PATH.exists():
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; "
+            "g.build()' or python -m paged_fp8_mqa_gb300.build); the indexer has no CPU path")
+    L = ctypes.CDLL(str(LIB_PATH))
+    c = ctypes
+    P = c.c_void_p
+    L.idx_last_error.restype = c.c_char_p
+    L.idx_last_error.argtypes = []
+    L.idx_padded_seq_len.restype = c.c_int64
+    L.idx_padded_seq_len.argtypes = [c.c_int64]
+    L.idx_min_block_table_width.restype = c.c_int64
+    L.idx_min_block_table_width.argtypes = [c.c_int64, c.c_int32]
+    L.idx_num_sms.restype = c.c_int
+    L.idx_num_sms.argtypes = [P]
+    L.idx_schedule.restype = c.c_int
+    L.idx_schedule.argtypes = [P, c.c_int64, c.c_int32, c.c_int32, c.c_int32, P, P]
+    L.idx_logits_fp8.restype = c.c_int
+    L.idx_logits_fp8.argtypes = [P, P, c.c_int64, c.c_int32, P, P, c.c_int64, c.c_int32, P,
+                                 c.c_int64, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
+                                 c.c_int32, P, c.c_int32, P, c.c_int64, P, P]
+    L.idx_threshold_select.restype = c.c_int
+    L.idx_threshold_select.argtypes = [P, c.c_int64, P, c.c_int32, P, P, P, c.c_int32,
+                                       c.c_int32, c.c_int32, P, P, P]
+    L.idx_device_status.restype = c.c_int
+    L.idx_device_status.argtypes = [P, c.c_int32]
+    _lib = L
+    return L
+
+
+def _check(status: int) -> None:
+    if status != IDX_OK:
+        raise IdxError(status, lib().idx_last_error().decode())
+
+
+# ---- C-ABI mirrors (raw pointers / ints) -------------------------------------------------------
+
+def idx_last_error() -> str:
+    return lib().idx_last_error().decode()
+
+
+def idx_padded_seq_len(max_seq_len: int) -> int:
+    return int(lib().idx_padded_seq_len(max_seq_len))
+
+
+def idx_min_block_table_width(seq_len: int, block_size: int) -> int:
+    return int(lib().idx_min_block_table_width(seq_len, block_size))
+
+
+def idx_num_sms() -> int:
+    out = ctypes.c_int32(0)
+    _check(lib().idx_num_sms(ctypes.byref(out)))
+    return out.value
+
+
+def idx_schedule(seq_lens, seq_lens_stride, batch, next_n, num_sms, schedule, stream) -> int:
+    return lib().idx_schedule(seq_lens, seq_lens_stride, batch, next_n, num_sms, schedule, stream)
+
+
+def idx_logits_fp8(q, kv_fused, num_blocks, block_size, weights, block_tables, bt_row_stride,
+                   bt_width, seq_lens, seq_lens_stride, batch, next_n, num_heads, head_dim,
+                   max_seq_len, schedule, num_sms, out, out_row_stride, row_ends_out,
+                   stream) -> int:
+    return lib().idx_logits_fp8(q, kv_fused, num_blocks, block_size, weights, block_tables,
+                                bt_row_stride, bt_width, seq_lens, seq_lens_stride, batch, next_n,
+                                num_heads, head_dim, max_seq_len, schedule, num_sms, out,
+                                out_row_stride, row_ends_out, stream)
+
+
+def idx_threshold_select(logits, logits_row_stride, row_ends, rows, thresholds, counters,
+                         candidates, top_k, capacity, max_context, arrivals, ranges,
+                         stream) -> int:
+    return lib().idx_threshold_select(logits, logits_row_stride, row_ends, rows, thresholds,
+                                      counters, candidates, top_k, capacity, max_context,
+                                      arrivals, ranges, stream)
+
+
+def idx_device_status(clear: bool = False) -> int:
+    out = ctypes.c_int32(0)
+    _check(lib().idx_device_status(ctypes.byref(out), int(clear)))
+    return out.value
+
+
+# ---- torch-facing marshalling ------------------------------------------------------------------
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name, dims=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dims, got {t.dim()}")
+
+
+def schedule(seq_lens, next_n: int = 1, num_sms: int = 0, out=None, stream=None):
+    """The persistent logits kernel's work split, int32 [num_sms + 1, 2] on the device."""
+    import torch
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    n = num_sms or idx_num_sms()
+    if out is None:
+        out = torch.empty(n + 1, 2, dtype=torch.int32, device=seq_lens.device)
+    _check(idx_schedule(_ptr(seq_lens), seq_lens.stride(0), seq_lens.shape[0], next_n, n,
+                        _ptr(out), _stream(stream)))
+    return out
+
+
+def logits_fp8(q, kv_fused, weights, block_tables, seq_lens, max_seq_len: int, *, out=None,
+               schedule_meta=None, num_sms: int = 0, row_ends_out=None, stream=None):
+    """Paged FP8 MQA logits.  q: e4m3 (or its uint8 view) [B, next_n, 64, 128]; kv_fused: uint8
+    whose leading dim is the block count and whose per-block bytes are 64*(128+4); weights:
+    float32 [B*next_n, 64]; block_tables: int32 [B, W] with unit column stride; seq_lens: int32
+    [B] (any stride).  Returns the [B*next_n, max_seq_len] view of the padded output."""
+    import torch
+    _need(q, (torch.float8_e4m3fn, torch.uint8), "q", 4)
+    _need(kv_fused, torch.uint8, "kv_fused")
+    _need(weights, torch.float32, "weights", 2)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, n, H, D = q.shape
+    if not q.is_contiguous() or not weights.is_contiguous() or not kv_fused.is_contiguous():
+        raise ValueError("q, weights and kv_fused must be contiguous")
+    if block_tables.stride(1) != 1:
+        raise ValueError("block_tables rows must be contiguous (stride(1) == 1)")
+    num_blocks = kv_fused.shape[0]
+    block_size = kv_fused.numel() // num_blocks // (D + 4) if num_blocks else 0
+    if out is None:
+        out = torch.empty(B * n, idx_padded_seq_len(max_seq_len), dtype=torch.float32,
+                          device=q.device)
+    _need(out, torch.float32, "out", 2)
+    if out.stride(1) != 1:
+        raise ValueError("out rows must be contiguous")
+    _check(idx_logits_fp8(_ptr(q), _ptr(kv_fused), num_blocks, block_size, _ptr(weights),
+                          _ptr(block_tables), block_tables.stride(0), block_tables.shape[1],
+                          _ptr(seq_lens), seq_lens.stride(0), B, n, H, D, max_seq_len,
+                          _ptr(schedule_meta), num_sms, _ptr(out), out.stride(0),
+                          _ptr(row_ends_out), _stream(stream)))
+    return out[:B * n, :max_seq_len]
+
+
+def threshold_select(logits, row_ends, thresholds, counters, candidates, top_k: int,
+                     capacity: int, max_context: int, *, arrivals=None, ranges=None,
+                     stream=None):
+    """Per-row threshold top-k over logits (float32 [rows, >= max_context], unit column stride).
+    counters (int32 [rows, 2]) must be zeroed by the caller; candidates is int32
+    [rows, top_k + capacity, 2]; arrivals/ranges enable the repair."""
+    import torch
+    _need(logits, torch.float32, "logits", 2)
+    _need(row_ends, torch.int32, "row_ends", 1)
+    _need(thresholds, torch.float32, "thresholds", 1)
+    _need(counters, torch.int32, "counters", 2)
+    _need(candidates, torch.int32, "candidates", 3)
+    if logits.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous")
+    rows = row_ends.shape[0]
+    for t, name in ((row_ends, "row_ends"), (thresholds, "thresholds"), (counters, "counters"),
+                    (candidates, "candidates")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if candidates.shape[1] != top_k + capacity or candidates.shape[0] < rows:
+        raise ValueError("candidates must be [rows, top_k + capacity, 2]")
+    _check(idx_threshold_select(_ptr(logits), logits.stride(0), _ptr(row_ends), rows,
+                                _ptr(thresholds), _ptr(counters), _ptr(candidates), top_k,
+                                capacity, max_context, _ptr(arrivals), _ptr(ranges),
+                                _stream(stream)))
+
+
+def device_status(clear: bool = False) -> int:
+    """OR of the IDX_DEV_* bits raised by the kernels since the last clear (synchronous)."""
+    return idx_device_status(clear)

@@ -1,0 +1,59 @@
+// internal.h -- host-side interface between the C ABI layer and the kernel translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace idx {
+
+// Largest batch (requests per call) the kernels accept: the logits kernel keeps every
+// request's length in shared memory.
+constexpr int kMaxBatch = 4096;
+
+// Everything the logits kernel needs besides its two tensor maps.
+struct LogitsArgs {
+  const uint8_t *kv;            // pool base
+  const float *weights;         // [batch*next_n, 64]
+  const int32_t *block_tables;  // row b at block_tables + b * bt_stride
+  int64_t bt_stride;
+  const int32_t *seq_lens;      // element b at seq_lens[b * sl_stride]
+  int64_t sl_stride;
+  const int32_t *schedule;      // nullable: [num_ctas + 1][2]
+  float *out;                   // row r at out + r * out_stride
+  int64_t out_stride;
+  int32_t *row_ends;            // nullable: [batch * next_n]
+  int64_t num_blocks;
+  int32_t batch;
+};
+
+// Launches the logits kernel for draft depth `next_n` (1..4) on `num_ctas` CTAs.
+cudaError_t launch_logits_fp8(int next_n, const CUtensorMap &kv_map, const CUtensorMap &q_map,
+                              const LogitsArgs &args, int num_ctas, cudaStream_t stream);
+
+// Launches the standalone schedule kernel.
+cudaError_t launch_schedule(const int32_t *seq_lens, int64_t stride, int batch, int num_ctas,
+                            int32_t *schedule, cudaStream_t stream);
+
+struct SelectArgs {
+  const float *logits;
+  int64_t row_stride;
+  const int32_t *row_ends;
+  float *thresholds;
+  int32_t *counters;
+  int32_t *candidates;
+  int32_t *arrivals;  // nullable
+  int32_t *ranges;    // nullable unless arrivals
+  int32_t rows;
+  int32_t top_k;
+  int32_t capacity;
+  int32_t max_context;
+};
+
+cudaError_t launch_threshold_select(const SelectArgs &args, cudaStream_t stream);
+
+// Device-side status words of each translation unit (IDX_DEV_* bits).
+cudaError_t logits_status(int32_t *value, bool clear);
+cudaError_t select_status(int32_t *value, bool clear);
+
+}  // namespace idx

@@ -1,0 +1,111 @@
+"""Paged FP8 MQA logits: the CUDA path against the float64 oracle, element by element."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_fp8_mqa_gb300 as idx
+from paged_fp8_mqa_gb300 import synth
+from gpu_cases import check_logits, gpu_logits, oracle_logits_cached, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    idx.device_status(clear=True)
+    yield
+    assert idx.device_status(clear=True) == 0, "a kernel raised a device status bit"
+
+
+def _small(seed, next_n, lens, max_seq_len=None, **kw):
+    m = max_seq_len or max(max(lens), 1)
+    return synth.make_workload("edge", seed, len(lens), next_n, m, "fixed", values=list(lens),
+                               **kw)
+
+
+def _oracle(w):
+    return oracle.paged_logits(w.q, w.kv_fused, w.weights, w.block_tables, w.seq_lens,
+                               w.max_seq_len, block_size=w.block_size)
+
+
+def test_tiny_workload():
+    w, ref, tol = oracle_logits_cached("tiny")
+    got, row_ends = gpu_logits(w)
+    check_logits(w, got, ref, tol)
+    assert (row_ends.cpu() == w.row_ends()).all()
+
+
+EDGE = [
+    (1, [1]), (1, [63]), (1, [64]), (1, [65]), (1, [127, 128, 129]), (1, [255, 256, 257]),
+    (2, [1, 2, 3]), (2, [0, 64, 0, 130]), (3, [2, 3, 4, 200]), (4, [3, 4, 5, 1000]),
+    (4, [0, 0, 0]), (1, [5000, 1, 0, 77]), (3, [129, 64, 63, 1]), (2, [4096, 4095]),
+]
+
+
+@pytest.mark.parametrize("next_n,lens", EDGE, ids=[f"n{n}-{'_'.join(map(str, l))}" for n, l in EDGE])
+def test_edge_lengths(next_n, lens):
+    w = _small(100 + len(lens) + next_n, next_n, lens)
+    ref, tol = _oracle(w)
+    got, row_ends = gpu_logits(w)
+    check_logits(w, got, ref, tol)
+    assert (row_ends.cpu() == w.row_ends()).all()
+
+
+@pytest.mark.parametrize("next_n", [1, 2, 3, 4])
+def test_many_requests_ragged(next_n):
+    g = torch.Generator().manual_seed(next_n)
+    lens = torch.randint(0, 3000, (37,), generator=g).tolist()
+    w = _small(200 + next_n, next_n, lens, max_seq_len=3000, scale_range=(0.25, 4.0),
+               outlier_frac=0.01)
+    ref, tol = _oracle(w)
+    got, _ = gpu_logits(w)
+    check_logits(w, got, ref, tol)
+
+
+@pytest.mark.parametrize("num_sms", [1, 3, 37, 500])
+def test_grid_size_does_not_change_results(num_sms):
+    w = _small(301, 2, [700, 0, 1300, 64, 65, 2000])
+    base, _ = gpu_logits(w)
+    got, _ = gpu_logits(w, num_sms=num_sms)
+    assert torch.equal(got.nan_to_num(-1e30), base.nan_to_num(-1e30))
+
+
+def test_precomputed_schedule_matches_in_kernel_split():
+    w = _small(302, 3, [900, 5, 0, 4000, 128])
+    base, _ = gpu_logits(w)
+    got, _ = gpu_logits(w, schedule=True)
+    assert torch.equal(got.nan_to_num(-1e30), base.nan_to_num(-1e30))
+    for n_sms in (1, 10, 152):
+        got2, _ = gpu_logits(w, schedule=True, num_sms=n_sms)
+        assert torch.equal(got2.nan_to_num(-1e30), base.nan_to_num(-1e30))
+
+
+def test_strided_table_and_lengths():
+    """block_tables[::2] and seq_lens[::2] views are read without a copy."""
+    w = _small(303, 2, [300, 1000, 17])
+    t = to_device(w)
+    B, W = w.block_tables.shape
+    bt2 = torch.full((2 * B, W), 0x7FFFFFFF, dtype=torch.int32, device=t["bt"].device)
+    bt2[::2] = t["bt"]
+    sl2 = torch.full((2 * B,), 999999, dtype=torch.int32, device=t["bt"].device)
+    sl2[::2] = t["seq_lens"]
+    ref, tol = _oracle(w)
+    got, _ = gpu_logits(w, tensors=t, bt=bt2[::2], seq_lens=sl2[::2])
+    check_logits(w, got, ref, tol)
+
+
+def test_unused_table_entries_never_read():
+    w = _small(304, 1, [70, 300, 1], max_seq_len=1024, unused_entries="poison")
+    ref, tol = _oracle(w)
+    got, _ = gpu_logits(w)
+    check_logits(w, got, ref, tol)
+
+
+@pytest.mark.parametrize("name", ["decode", "mtp", "long_select", "serving"])
+def test_full_workload(name):
+    w, ref, tol = oracle_logits_cached(name)
+    got, row_ends = gpu_logits(w)
+    stats = check_logits(w, got, ref, tol)
+    assert stats["checked"] == w.valid_scores()
+    assert (row_ends.cpu() == w.row_ends()).all()
