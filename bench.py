@@ -1,0 +1,398 @@
+"""Benchmark: paged FP8 MQA logits on one GB300 (replicas on N GPUs), one JSON line.
+
+Default workload: the decode batch (64 requests, next_n = 1, 64 heads, head_dim 128, 64-token
+blocks, seq_lens uniform in [1024, 32768]).  One step = one launch of the fused logits kernel
+(in-kernel schedule, logits, row_ends).  Metric: Gscores/s, valid (query row, KV position)
+pairs per second.  Inputs are resident in HBM; three copies of the KV pool (each larger than
+L2) are used in rotation so no step finds its pool in L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|mtp|long_select|serving]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores, same metric
+
+Multi-GPU: the path shards by request with no exchange step; each rank runs an independent
+replica of the workload ("scaling": "weak") and rank 0 reports the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import paged_fp8_mqa_gb300 as idx  # noqa: E402
+from paged_fp8_mqa_gb300 import synth  # noqa: E402
+
+METRIC = "Gscores/s (query row x KV pos) and % of HBM/FP8 roofline, paged MQA logits"
+UNIT = "Gscores/s"
+POOL_COPIES = 3
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained",
+                                                     p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def algorithmic(w: synth.Workload) -> dict:
+    """Per-launch algorithmic work: KV values + scales of every valid position (132 B each),
+    the logits written (4 B per valid score), q and w; MMA flops 2*64*128 per score."""
+    P = int(w.seq_lens.to(torch.int64).sum())
+    scores = w.valid_scores()
+    kv = 132 * P
+    out = 4 * scores
+    qw = w.q.numel() + 4 * w.weights.numel()
+    return {"positions": P, "scores": scores, "kv_bytes": kv, "bytes": kv + out + qw,
+            "flops": 2 * 64 * 128 * w.next_n * P}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.proc = None
+        self.device = device
+        self.t0 = self.t1 = None
+
+    def start(self):
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.device).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *sel, f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which: str):
+        setattr(self, which, time.time())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm, mx, reasons = [], None, set()
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for name, col in (("hw_slowdown", 5), ("hw_thermal_slowdown", 6),
+                                  ("sw_thermal_slowdown", 7), ("sw_power_cap", 8)):
+                    if r[col].strip().lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def device_inputs(w: synth.Workload, dev):
+    pools = [w.kv_fused.to(dev)]
+    for _ in range(POOL_COPIES - 1):
+        pools.append(pools[0].clone())
+    return dict(q=w.q.to(dev), pools=pools, weights=w.weights.to(dev),
+                bt=w.block_tables.to(dev), seq_lens=w.seq_lens.to(dev))
+
+
+def launch(w, t, pool, out, row_ends, stream):
+    idx.logits_fp8(t["q"], pool, t["weights"], t["bt"], t["seq_lens"], w.max_seq_len, out=out,
+                   row_ends_out=row_ends, stream=stream)
+
+
+def time_device(w, t, steps, warmup, stream, sampler=None):
+    """K launches, each bracketed by CUDA events on the launching stream; returns per-launch
+    milliseconds and the wall-clock milliseconds of the whole region (events too)."""
+    dev = t["q"].device
+    out = torch.empty(w.rows, idx.idx_padded_seq_len(w.max_seq_len), device=dev)
+    row_ends = torch.empty(w.rows, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            launch(w, t, t["pools"][i % POOL_COPIES], out, row_ends, stream)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t0")
+    with torch.cuda.stream(stream):
+        region0.record(stream)
+        for i in range(steps):
+            starts[i].record(stream)
+            launch(w, t, t["pools"][i % POOL_COPIES], out, row_ends, stream)
+            ends[i].record(stream)
+        region1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t1")
+    barrier()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return per, region0.elapsed_time(region1), out
+
+
+def time_e2e(w, dev, steps, stream):
+    """Same metric through the public call with host buffers: every step copies its inputs
+    from pinned host memory, runs the kernel and copies the logits back."""
+    host = dict(q=w.q.pin_memory(), kv=w.kv_fused.pin_memory(),
+                weights=w.weights.pin_memory(), bt=w.block_tables.pin_memory(),
+                seq_lens=w.seq_lens.pin_memory())
+    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    pad = idx.idx_padded_seq_len(w.max_seq_len)
+    out = torch.empty(w.rows, pad, device=dev)
+    out_h = torch.empty(w.rows, pad).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out.numel() * out.element_size()
+
+    def step():
+        for k in host:
+            devb[k].copy_(host[k], non_blocking=True)
+        idx.logits_fp8(devb["q"], devb["kv"], devb["weights"], devb["bt"], devb["seq_lens"],
+                       w.max_seq_len, out=out, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+def _first_requests(w: synth.Workload, nreq: int) -> synth.Workload:
+    return synth.Workload(**{**w.__dict__, "batch": nreq, "seq_lens": w.seq_lens[:nreq],
+                             "block_tables": w.block_tables[:nreq],
+                             "q": w.q[:nreq].contiguous(),
+                             "weights": w.weights[:nreq * w.next_n].contiguous()})
+
+
+def cpu_baseline(w: synth.Workload, budget_s: float = 15.0) -> dict:
+    """The float64 oracle, as it stands, on this host's cores, over a bounded sample of the
+    workload: its first requests, as many as a one-request probe says fit the time budget."""
+    import oracle
+    lib = oracle.load()
+    threads = oracle.max_threads(lib)
+
+    def run(sub):
+        t0 = time.perf_counter()
+        oracle.paged_logits(sub.q, sub.kv_fused, sub.weights, sub.block_tables, sub.seq_lens,
+                            sub.max_seq_len, block_size=sub.block_size, with_tol=False, lib=lib)
+        return time.perf_counter() - t0
+
+    probe = _first_requests(w, 1)
+    per_score = run(probe) / max(probe.valid_scores(), 1)
+    re = w.row_ends().to(torch.int64).view(w.batch, w.next_n).sum(1).cumsum(0)
+    nreq = max(1, int((re.to(torch.float64) * per_score <= budget_s).sum()))
+    sub = _first_requests(w, nreq)
+    dt = run(sub)
+    return {"value": sub.valid_scores() / dt / 1e9, "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": f"first {nreq} of {w.batch} requests of the {w.name} workload "
+                      f"({sub.valid_scores()} scores in {dt:.1f} s wall; float64, exact e4m3 "
+                      f"decode, OpenMP over rows and 256-position chunks)"}
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def reduce_max(x: float) -> float:
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+def reduce_sum(x: float) -> float:
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+        return float(t.item())
+    return x
+
+
+def make(name: str) -> synth.Workload:
+    return synth.WORKLOADS[name]()
+
+
+def run_reference(args, rank: int, world: int) -> None:
+    """The oracle on the host cores: each step is a bounded sample of the workload."""
+    if rank != 0:
+        return
+    import oracle
+    w = make(args.workload)
+    lib = oracle.load()
+    threads = oracle.max_threads(lib)
+    nreq = max(1, min(w.batch, 4))
+    sub = _first_requests(w, nreq)
+
+    def step():
+        oracle.paged_logits(sub.q, sub.kv_fused, sub.weights, sub.block_tables, sub.seq_lens,
+                            sub.max_seq_len, block_size=sub.block_size, with_tol=False, lib=lib)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = sub.valid_scores() / dt / 1e9
+    sample = (f"first {nreq} of {w.batch} requests of the {w.name} workload "
+              f"({sub.valid_scores()} scores per step), float64 oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def workload_config(w: synth.Workload) -> dict:
+    return {"workload": f"{w.name}: B={w.batch}, next_n={w.next_n}, heads={w.num_heads}, "
+                        f"head_dim={w.head_dim}, block_size={w.block_size}, "
+                        f"max_seq_len={w.max_seq_len}, seed={w.seed}",
+            "batch": w.batch, "next_n": w.next_n, "max_seq_len": w.max_seq_len,
+            "valid_scores": w.valid_scores(),
+            "l2": f"inputs larger than L2: {POOL_COPIES} KV-pool copies "
+                  f"({w.kv_fused.numel() / 1e6:.0f} MB each) used in rotation",
+            "parallelism": "replicas"}
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(dev)
+    peaks = load_peaks()
+
+    w = make(args.workload)
+    t = device_inputs(w, dev)
+    alg = algorithmic(w)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    per, region_ms, _ = time_device(w, t, args.steps, args.warmup, stream, sampler)
+    clocks = sampler.stop() if sampler else None
+    mean_ms = sum(per) / len(per)
+    step_ms = reduce_max(mean_ms)
+    value = reduce_sum(alg["scores"] / (mean_ms * 1e-3) / 1e9)
+    status = idx.device_status(clear=True)
+
+    e2e_ms, h2d, d2h = time_e2e(w, dev, max(3, min(20, args.steps)), stream)
+    e2e_value = reduce_sum(alg["scores"] / (e2e_ms * 1e-3) / 1e9)
+
+    hbm_ach = alg["bytes"] / (mean_ms * 1e-3) / 1e9
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # fp8 dense = 2x bf16 (nominal 4.5 / 2.25 PFLOP/s)
+    t_hbm = alg["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_mma = alg["flops"] / (fp8_peak * 1e12)
+    bound = "hbm" if t_hbm >= t_mma else "tensor"
+    roof = {"bound": bound, "achieved": hbm_ach if bound == "hbm" else
+            alg["flops"] / (mean_ms * 1e-3) / 1e12,
+            "peak": peaks["hbm_gbs"] if bound == "hbm" else fp8_peak,
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "traffic": None,
+            "peak_source": peaks["source"] + (" (fp8 = 2 x bf16)" if bound == "tensor" else ""),
+            "algorithmic_bytes": alg["bytes"], "kv_bytes": alg["kv_bytes"],
+            "flops": alg["flops"],
+            "roofline_time_ms": max(t_hbm, t_mma) * 1e3,
+            "roofline_frac": max(t_hbm, t_mma) * 1e3 / mean_ms}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+
+    secondary = {}
+    if not args.no_secondary and args.workload == "decode":
+        # The next_n = 4 workload, timed the same way (a context figure, not the headline).
+        w2 = make("mtp")
+        t2 = device_inputs(w2, dev)
+        per2, _, _ = time_device(w2, t2, max(3, min(500, args.steps)), args.warmup, stream)
+        m2 = sum(per2) / len(per2)
+        a2 = algorithmic(w2)
+        r2 = max(a2["bytes"] / (peaks["hbm_gbs"] * 1e9), a2["flops"] / (fp8_peak * 1e12)) * 1e3
+        secondary["mtp"] = {"value": a2["scores"] / (m2 * 1e-3) / 1e9, "unit": UNIT,
+                            "ms_per_launch": m2, "roofline_time_ms": r2,
+                            "roofline_frac": r2 / m2,
+                            "hbm_gbs": a2["bytes"] / (m2 * 1e-3) / 1e9,
+                            "tflops": a2["flops"] / (m2 * 1e-3) / 1e12}
+        del t2
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32",
+            "data": "synthetic", "config": workload_config(w),
+            "region_ms_per_step": region_ms / args.steps,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps, "device_status": status,
+            "clocks": clocks, "roofline": roof, "cpu_baseline": cpu,
+        }
+        if secondary:
+            line["secondary"] = secondary
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
