@@ -3,21 +3,26 @@
 //
 //   out[b*n + t, p] = scale[p] * sum_h w[b*n + t, h] * relu(q[b, t, h, :] . k[p, :])
 //
-// One persistent CTA per SM walks a contiguous run of 128-position KV tiles (split.cuh).
-// Warp roles, all iterating the same tile sequence:
-//   warp 0     producer: reads the block table 32 entries at a time, and for each tile TMA-loads
-//              the two 64-token pages' e4m3 values (8 KiB each, 128-byte swizzled) and bulk-
-//              copies their 256-byte float32 scale regions into one pipeline stage; loads q
-//              and w of each new request into one of two q/w buffers.
-//   warp 1     MMA issuer (one thread): per tile, 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each)
+// One persistent CTA per SM walks a contiguous run of 128-position KV tiles (split.cuh); tile k
+// of the run is the CTA's k-th.  Warp roles, all walking the same tile sequence:
+//   warp 0     producer.  Prologue: computes the CTA's tile range from seq_lens (one warp, no
+//              block-wide synchronisation on the way to the first load).  Per tile: reads the
+//              block table 32 entries at a time, TMA-loads the two 64-token pages' e4m3 values
+//              (8 KiB each, 128-byte swizzled) into a KV stage, and copies their float32 scales
+//              (256 B per page) with one 16-byte cp.async per lane into a separate scale ring.
+//              Per request: TMA-loads q and bulk-copies w into one of two q/w buffers.
+//   warp 1     MMA issuer (one thread): 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each),
 //              D[128 positions, n*64 query rows] += K_tile[128, 32] * q[n*64, 32]^T into a
-//              TMEM accumulator (float32), then commits to the stage's and the accumulator's
-//              barriers.  The KV tile is the MMA's M side, so TMEM lane = KV position.
-//   warps 2-5  epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (one position per thread),
-//              computes scale * sum_h w_h * max(s_h, 0) for each draft slot in float32, and
-//              stores it: 32 consecutive positions per warp, one 128-byte line per row.
-// The per-head reduction is per-thread (heads are TMEM columns of the thread's own lane), so it
-// needs no shuffles.
+//              float32 TMEM accumulator; commits release the KV stage and fill the accumulator.
+//              The KV tile is the MMA's M side, so TMEM lane = KV position.
+//   warps 2-9  epilogue, two groups of four warps taking alternate tiles.  Warp w reads TMEM
+//              lanes 32*(w%4)..+31, one position per thread; for each draft slot it computes
+//              scale * sum_h w_h * max(s_h, 0) in float32 (packed FMAs) and stores 32
+//              consecutive positions per warp (one 128-byte line per output row).
+// The KV stage is released by the MMA alone: the epilogue never touches it (its scales come
+// from the scale ring, which is deep enough that the producer cannot overwrite an entry the
+// epilogue still needs), so slow epilogue work never stalls the HBM stream beyond the
+// accumulator slack.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -35,7 +40,9 @@ __device__ int g_logits_status;
 
 namespace {
 
-constexpr int kThreads = 192;                     // 6 warps
+constexpr int kWarps = 10;
+constexpr int kThreads = kWarps * 32;
+constexpr int kEpiWarpBase = 2;                  // epilogue warps 2..9
 constexpr int kHeads = 64;
 constexpr int kHeadDim = 128;
 constexpr int kBlock = 64;                        // tokens per page
@@ -43,62 +50,90 @@ constexpr int kPageBytes = kBlock * (kHeadDim + 4);  // 8448
 constexpr int kPageRows = kPageBytes / 128;       // 66 rows of 128 bytes per page
 constexpr int kValueBytes = kBlock * kHeadDim;    // 8192
 constexpr uint32_t kStageBytes = kTileTokens * kHeadDim;  // 16384: two pages of values
+constexpr int kScaleRing = 16;                    // tiles of scales in flight
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
 
 template <int NN>
 struct Cfg {
   static constexpr int N = NN * kHeads;  // MMA N: query rows of one request
-  static constexpr int STAGES = NN == 1 ? 10 : (NN == 2 ? 10 : (NN == 3 ? 9 : 8));
-  static constexpr int ACC = NN <= 2 ? 4 : 2;
+  static constexpr int STAGES = NN <= 2 ? 10 : (NN == 3 ? 9 : 8);
+  static constexpr int ACC = NN <= 2 ? 4 : 2;  // even: tile k's accumulator belongs to group k&1
   static constexpr int TMEM_COLS = (ACC * N <= 256) ? 256 : 512;
   static constexpr uint32_t Q_BYTES = N * kHeadDim;
   static constexpr uint32_t W_FLOATS = NN * kHeads;
   static constexpr uint32_t OFF_KV = 0;
   static constexpr uint32_t OFF_Q = OFF_KV + STAGES * kStageBytes;
   static constexpr uint32_t OFF_SCALE = OFF_Q + 2 * Q_BYTES;
-  static constexpr uint32_t OFF_W = OFF_SCALE + STAGES * kTileTokens * 4;
+  static constexpr uint32_t OFF_W = OFF_SCALE + kScaleRing * kTileTokens * 4;
   static constexpr uint32_t OFF_BAR = OFF_W + 2 * W_FLOATS * 4;
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * ACC + 4 + 1;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + kScaleRing + 2 * ACC + 4 + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr uint32_t OFF_LEN = OFF_MISC + 128;
+  static constexpr uint32_t OFF_LEN = OFF_MISC + 64;
   static constexpr uint32_t smem_bytes(int batch) {
     return OFF_LEN + 4u * static_cast<uint32_t>(batch) + 1024u;  // + alignment slack
   }
   static_assert(OFF_Q % 1024 == 0 && Q_BYTES % 1024 == 0, "swizzled tiles 1024-aligned");
-  static_assert(OFF_SCALE % 16 == 0 && OFF_W % 16 == 0, "bulk-copy destinations");
+  static_assert(OFF_SCALE % 16 == 0 && OFF_W % 16 == 0, "copy destinations 16-byte aligned");
   static_assert(smem_bytes(kMaxBatch) <= 232448, "fits the 227 KiB per-CTA limit");
-  static_assert(ACC * N <= TMEM_COLS, "accumulators fit the allocation");
+  static_assert(ACC * N <= TMEM_COLS && ACC % 2 == 0, "accumulators");
+  // The producer writes tile k's scales once it has passed tile k-1's stage wait, i.e. once the
+  // MMA finished tile k-1-STAGES, whose accumulator wait needed the epilogue to finish tile
+  // k-1-STAGES-ACC (and, each group working in order, every tile up to k-2-STAGES-ACC).  The
+  // entry's previous user, tile k - kScaleRing, must be among those.
+  static_assert(kScaleRing >= STAGES + ACC + 2, "scale ring deep enough");
 };
 
 __device__ __forceinline__ void flag_error(int bits) { atomicOr(&g_logits_status, bits); }
 
-// scale-free part of one logit: sum over the 64 heads of w_h * max(s_h, 0), in float32 with
-// eight interleaved partial sums (eight terms each) combined pairwise.
+// The scale-free part of one logit: sum over the 64 heads of w_h * max(s_h, 0) in float32,
+// with eight partial sums of eight terms each (packed two at a time), combined pairwise.
 __device__ __forceinline__ float weighted_relu_sum(const uint32_t (&lo)[32],
                                                    const uint32_t (&hi)[32], const float *w) {
   const float4 *w4 = reinterpret_cast<const float4 *>(w);
-  float acc[8];
+  float2 acc[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 16; ++i) {
     const float4 ww = w4[i];
-    const int base = (i & 1) * 4;
-    acc[base + 0] = fmaf(ww.x, fmaxf(__uint_as_float(lo[4 * i + 0]), 0.0f), acc[base + 0]);
-    acc[base + 1] = fmaf(ww.y, fmaxf(__uint_as_float(lo[4 * i + 1]), 0.0f), acc[base + 1]);
-    acc[base + 2] = fmaf(ww.z, fmaxf(__uint_as_float(lo[4 * i + 2]), 0.0f), acc[base + 2]);
-    acc[base + 3] = fmaf(ww.w, fmaxf(__uint_as_float(lo[4 * i + 3]), 0.0f), acc[base + 3]);
+    const uint32_t *s = i < 8 ? &lo[4 * i] : &hi[4 * (i - 8)];
+    const float2 r01 = make_float2(fmaxf(__uint_as_float(s[0]), 0.0f),
+                                   fmaxf(__uint_as_float(s[1]), 0.0f));
+    const float2 r23 = make_float2(fmaxf(__uint_as_float(s[2]), 0.0f),
+                                   fmaxf(__uint_as_float(s[3]), 0.0f));
+    const int q = (i & 1) * 2;
+    acc[q] = __ffma2_rn(make_float2(ww.x, ww.y), r01, acc[q]);
+    acc[q + 1] = __ffma2_rn(make_float2(ww.z, ww.w), r23, acc[q + 1]);
   }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 ww = w4[8 + i];
-    const int base = (i & 1) * 4;
-    acc[base + 0] = fmaf(ww.x, fmaxf(__uint_as_float(hi[4 * i + 0]), 0.0f), acc[base + 0]);
-    acc[base + 1] = fmaf(ww.y, fmaxf(__uint_as_float(hi[4 * i + 1]), 0.0f), acc[base + 1]);
-    acc[base + 2] = fmaf(ww.z, fmaxf(__uint_as_float(hi[4 * i + 2]), 0.0f), acc[base + 2]);
-    acc[base + 3] = fmaf(ww.w, fmaxf(__uint_as_float(hi[4 * i + 3]), 0.0f), acc[base + 3]);
+  return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+         ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+}
+
+// Finds, in one warp, the (request, tile) of flat tile index `flat` given each lane's segment
+// [seg_lo, seg_hi) of requests, the lane's exclusive tile prefix and its tile count.
+__device__ __forceinline__ int2 warp_locate(long long flat, long long total, int seg_lo,
+                                            int seg_hi, long long excl, long long mine,
+                                            const int *s_len, int batch) {
+  int2 at = make_int2(batch, 0);
+  const bool here = flat < total && flat >= excl && flat < excl + mine;
+  if (here) {
+    long long run = excl;
+    for (int b = seg_lo; b < seg_hi; ++b) {
+      const int t = tiles_of(s_len[b]);
+      if (flat < run + t) {
+        at = make_int2(b, static_cast<int>(flat - run));
+        break;
+      }
+      run += t;
+    }
   }
-  return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  const unsigned who = __ballot_sync(0xffffffffu, here);
+  if (who) {
+    const int src = __ffs(who) - 1;
+    at.x = __shfl_sync(0xffffffffu, at.x, src);
+    at.y = __shfl_sync(0xffffffffu, at.y, src);
+  }
+  return at;
 }
 
 template <int NN>
@@ -115,77 +150,88 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *s_w = reinterpret_cast<float *>(smem + C::OFF_W);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *empty = full + C::STAGES;
-  uint64_t *acc_full = empty + C::STAGES;
+  uint64_t *sfull = empty + C::STAGES;
+  uint64_t *acc_full = sfull + kScaleRing;
   uint64_t *acc_empty = acc_full + C::ACC;
   uint64_t *q_full = acc_empty + C::ACC;
   uint64_t *q_empty = q_full + 2;
   uint64_t *drain = q_empty + 2;
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
-  int *s_split = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);      // 4 ints
-  long long *s_warp = reinterpret_cast<long long *>(smem + C::OFF_MISC + 64);  // 6 int64
+  int *s_split = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);  // 4 ints
   int *s_len = reinterpret_cast<int *>(smem + C::OFF_LEN);
-  // Prologue scratch: the inclusive tile prefix lives in the (still unused) KV stages.
-  long long *s_incl = reinterpret_cast<long long *>(s_kv);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int batch = a.batch;
 
-  // ---- 1. lengths and this CTA's tile range --------------------------------------------------
-  {
-    const long long total = load_lengths<kThreads>(a.seq_lens, a.sl_stride, batch, s_len, s_incl,
-                                                   s_warp);
-    if (tid == 0) {
-      int2 s0, s1;
-      if (a.schedule != nullptr) {
-        s0 = make_int2(__ldg(a.schedule + 2 * blockIdx.x), __ldg(a.schedule + 2 * blockIdx.x + 1));
-        s1 = make_int2(__ldg(a.schedule + 2 * blockIdx.x + 2),
-                       __ldg(a.schedule + 2 * blockIdx.x + 3));
-      } else {
-        const long long g = gridDim.x;
-        s0 = locate_tile(s_incl, s_len, batch, total * blockIdx.x / g);
-        s1 = locate_tile(s_incl, s_len, batch, total * (blockIdx.x + 1) / g);
-      }
+  // ---- 1. set-up: warp 0 finds the CTA's tile range, warp 1 prepares barriers and TMEM ------
+  if (warp == 0) {
+    const int per = (batch + 31) / 32;
+    const int lo = min(lane * per, batch);
+    const int hi = min(lo + per, batch);
+    long long mine = 0;
+    for (int b = lo; b < hi; ++b) {
+      int len = __ldg(a.seq_lens + static_cast<int64_t>(b) * a.sl_stride);
+      len = len < 0 ? 0 : len;
+      s_len[b] = len;
+      mine += tiles_of(len);
+    }
+    long long incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const long long total = __shfl_sync(0xffffffffu, incl, 31);
+    const long long excl = incl - mine;
+    int2 s0, s1;
+    if (a.schedule != nullptr) {
+      s0 = make_int2(__ldg(a.schedule + 2 * blockIdx.x), __ldg(a.schedule + 2 * blockIdx.x + 1));
+      s1 = make_int2(__ldg(a.schedule + 2 * blockIdx.x + 2),
+                     __ldg(a.schedule + 2 * blockIdx.x + 3));
+    } else {
+      const long long g = gridDim.x;
+      s0 = warp_locate(total * blockIdx.x / g, total, lo, hi, excl, mine, s_len, batch);
+      s1 = warp_locate(total * (blockIdx.x + 1) / g, total, lo, hi, excl, mine, s_len, batch);
+    }
+    if (lane == 0) {
       s_split[0] = s0.x;
       s_split[1] = s0.y;
       s_split[2] = s1.x;
       s_split[3] = s1.y;
     }
     if (a.row_ends != nullptr) {
-      for (int b = blockIdx.x * kThreads + tid; b < batch; b += gridDim.x * kThreads) {
+      for (int b = blockIdx.x + lane * gridDim.x; b < batch; b += 32 * gridDim.x) {
         const int len = s_len[b];
 #pragma unroll
         for (int t = 0; t < NN; ++t) a.row_ends[b * NN + t] = max(0, len - NN + t + 1);
       }
     }
-  }
-
-  // ---- 2. barriers, tensor memory -------------------------------------------------------------
-  if (tid == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + 4);  // MMA commit + one arrival per epilogue warp
+  } else if (warp == 1) {
+    if (lane == 0) {
+      prefetch_tensor_map(&kv_map);
+      prefetch_tensor_map(&q_map);
+      for (int s = 0; s < C::STAGES; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], 1);  // released by the MMA's commit alone
+      }
+      for (int s = 0; s < kScaleRing; ++s) mbar_init(&sfull[s], 32);  // one per producer lane
+      for (int c = 0; c < C::ACC; ++c) {
+        mbar_init(&acc_full[c], 1);
+        mbar_init(&acc_empty[c], 4);  // the four warps of the owning epilogue group
+      }
+      for (int c = 0; c < 2; ++c) {
+        mbar_init(&q_full[c], 1);
+        mbar_init(&q_empty[c], 1 + 8);  // MMA commit + every epilogue warp
+      }
+      mbar_init(drain, 1);
+      fence_barrier_init();
     }
-    for (int c = 0; c < C::ACC; ++c) {
-      mbar_init(&acc_full[c], 1);
-      mbar_init(&acc_empty[c], 4);
-    }
-    for (int c = 0; c < 2; ++c) {
-      mbar_init(&q_full[c], 1);
-      mbar_init(&q_empty[c], 1 + 4);
-    }
-    mbar_init(drain, 1);
-    fence_barrier_init();
-    prefetch_tensor_map(&kv_map);
-    prefetch_tensor_map(&q_map);
-  }
-  if (warp == 1) {
+    __syncwarp();
     tmem_alloc(s_tmem, C::TMEM_COLS);
     tmem_relinquish();
   }
-  // The prologue wrote the KV stages with ordinary stores; TMA writes them next.
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -200,9 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int qcount = 0, cur_b = -1;
     int win_b = -1, win_base = 0, win_val = 0;
-    int issued = 0;
+    int k = 0;
     bool ok = true;
-    for (TileIter it = first; it.valid(); it.next()) {
+    for (TileIter it = first; it.valid(); it.next(), ++k) {
       const int b = it.b, j = it.j;
       if (b != cur_b) {
         const int qb = qcount & 1;
@@ -226,62 +272,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         win_b = b;
         win_base = pg0 & ~31;
         const int e = win_base + lane;
-        win_val = e < npages ? __ldg(a.block_tables + static_cast<int64_t>(b) * a.bt_stride + e) : 0;
+        win_val = e < npages ? __ldg(a.block_tables + static_cast<int64_t>(b) * a.bt_stride + e)
+                             : 0;
       }
       const int page0 = __shfl_sync(0xffffffffu, win_val, pg0 - win_base);
       const int page1 = __shfl_sync(0xffffffffu, win_val, pg0 + 1 - win_base);
+      const bool v0 = page0 >= 0 && page0 < a.num_blocks;
+      const bool v1 = has1 && page1 >= 0 && page1 < a.num_blocks;
+      // Scales of this tile into ring entry k % kScaleRing: lanes 0-15 page 0, 16-31 page 1.
+      {
+        const int slot = k % kScaleRing;
+        const bool mine_valid = lane < 16 ? v0 : v1;
+        const int page = lane < 16 ? page0 : page1;
+        if (mine_valid)
+          cp_async_16(s_scale + slot * kTileTokens + lane * 4,
+                      a.kv + static_cast<int64_t>(page) * kPageBytes + kValueBytes +
+                          (lane & 15) * 16,
+                      pol_stream);
+        cp_async_arrive_noinc(&sfull[slot]);
+      }
       if (!mbar_wait(&empty[stage], phase ^ 1, kWaitLimitNs)) {
         ok = false;
         break;
       }
       if (lane == 0) {
-        const bool v0 = page0 >= 0 && page0 < a.num_blocks;
-        const bool v1 = has1 && page1 >= 0 && page1 < a.num_blocks;
         if (!v0 || (has1 && !v1)) flag_error(IDX_DEV_BAD_PAGE);
-        mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(kPageBytes) * (v0 + v1));
+        mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(kValueBytes) * (v0 + v1));
         uint8_t *dst = s_kv + stage * kStageBytes;
-        float *sdst = s_scale + stage * kTileTokens;
-        if (v0) {
-          tma_load_2d(dst, &kv_map, &full[stage], 0, page0 * kPageRows, pol_stream);
-          bulk_load(sdst, a.kv + static_cast<int64_t>(page0) * kPageBytes + kValueBytes,
-                    kBlock * 4, &full[stage], pol_stream);
-        }
-        if (v1) {
+        if (v0) tma_load_2d(dst, &kv_map, &full[stage], 0, page0 * kPageRows, pol_stream);
+        if (v1)
           tma_load_2d(dst + kValueBytes, &kv_map, &full[stage], 0, page1 * kPageRows, pol_stream);
-          bulk_load(sdst + kBlock, a.kv + static_cast<int64_t>(page1) * kPageBytes + kValueBytes,
-                    kBlock * 4, &full[stage], pol_stream);
-        }
       }
       __syncwarp();
-      ++issued;
       if (++stage == C::STAGES) {
         stage = 0;
         phase ^= 1;
       }
     }
     if (!ok) flag_error(IDX_DEV_WAIT_TIMEOUT);
-    // Never leave copies in flight: wait for the last loads issued into each stage.
-    const int tail = issued < C::STAGES ? issued : C::STAGES;
-    for (int k = 1; k <= tail; ++k) {
-      const int s = ((stage - k) % C::STAGES + C::STAGES) % C::STAGES;
-      const uint32_t ph = (stage - k < 0) ? (phase ^ 1) : phase;
+    // Never leave copies in flight: wait for the last loads issued into each stage, the last
+    // q/w load, and this lane's cp.async scale copies.
+    const int tail = k < C::STAGES ? k : C::STAGES;
+    for (int d = 1; d <= tail; ++d) {
+      const int s = ((stage - d) % C::STAGES + C::STAGES) % C::STAGES;
+      const uint32_t ph = (stage - d < 0) ? (phase ^ 1) : phase;
       if (!mbar_wait(&full[s], ph, kWaitLimitNs)) flag_error(IDX_DEV_WAIT_TIMEOUT);
     }
     if (qcount > 0 &&
         !mbar_wait(&q_full[(qcount - 1) & 1], ((qcount - 1) >> 1) & 1, kWaitLimitNs))
       flag_error(IDX_DEV_WAIT_TIMEOUT);
+    cp_async_wait_all();
   } else if (warp == 1) {
     // ================================ MMA issuer ==============================================
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(kTileTokens, C::N);
       int stage = 0;
       uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
       int qcount = 0, cur_b = -1, qb = 0;
       bool ok = true;
-      for (TileIter it = first; it.valid();) {
+      int k = 0;
+      for (TileIter it = first; it.valid(); ++k) {
         const int b = it.b;
+        const int acc = k % C::ACC;
+        const uint32_t acc_phase = (k / C::ACC) & 1;
         if (b != cur_b) {
           qb = qcount & 1;
           if (!mbar_wait(&q_full[qb], (qcount >> 1) & 1, kWaitLimitNs)) {
@@ -301,9 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b_addr = smem_addr(s_q + qb * C::Q_BYTES);
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::N);
 #pragma unroll
-        for (int k = 0; k < kHeadDim / 32; ++k)
-          mma_f8f6f4(d_tmem, smem_desc_sw128(a_addr + 32 * k), smem_desc_sw128(b_addr + 32 * k),
-                     idesc, k > 0 ? 1u : 0u);
+        for (int kk = 0; kk < kHeadDim / 32; ++kk)
+          mma_f8f6f4(d_tmem, smem_desc_sw128(a_addr + 32 * kk),
+                     smem_desc_sw128(b_addr + 32 * kk), idesc, kk > 0 ? 1u : 0u);
         mma_commit(&empty[stage]);
         mma_commit(&acc_full[acc]);
         it.next();
@@ -311,10 +364,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1;
-        }
-        if (++acc == C::ACC) {
-          acc = 0;
-          acc_phase ^= 1;
         }
       }
       if (!ok) flag_error(IDX_DEV_WAIT_TIMEOUT);
@@ -325,16 +374,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ================================ epilogue ================================================
+    const int group = (warp - kEpiWarpBase) >> 2;  // takes tiles k with k % 2 == group
     const int quarter = warp & 3;
     const int pos = quarter * 32 + lane;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
     int qcount = 0, cur_b = -1, qb = 0;
     bool ok = true;
-    for (TileIter it = first; it.valid();) {
+    int k = 0;
+    for (TileIter it = first; it.valid(); ++k) {
       const int b = it.b, j = it.j;
       if (b != cur_b) {
         qb = qcount & 1;
@@ -345,51 +392,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur_b = b;
         ++qcount;
       }
-      // The stage's scales (the MMA has consumed its values already or will shortly).
-      if (!mbar_wait(&full[stage], phase, kWaitLimitNs)) {
-        ok = false;
-        break;
-      }
-      const float scale = s_scale[stage * kTileTokens + pos];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      if (!mbar_wait(&acc_full[acc], acc_phase, kWaitLimitNs)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const float *w = s_w + qb * C::W_FLOATS;
-      const int p = j * kTileTokens + pos;
-      const bool store = p < s_len[b];
-      float *dst = a.out + static_cast<int64_t>(b * NN) * a.out_stride + p;
-      // One draft slot at a time (a rolled loop: unrolled, ptxas hoists the next slot's TMEM
-      // loads above this slot's arithmetic and runs out of registers at next_n >= 3).
+      if ((k & 1) == group) {
+        const int slot = k % kScaleRing;
+        const int acc = k % C::ACC;
+        if (!mbar_wait(&sfull[slot], (k / kScaleRing) & 1, kWaitLimitNs) ||
+            !mbar_wait(&acc_full[acc], (k / C::ACC) & 1, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const float scale = s_scale[slot * kTileTokens + pos];
+        tc_fence_after_sync();
+        const float *w = s_w + qb * C::W_FLOATS;
+        const int p = j * kTileTokens + pos;
+        const bool store = p < s_len[b];
+        float *dst = a.out + static_cast<int64_t>(b * NN) * a.out_stride + p;
+        // One draft slot at a time (a rolled loop: unrolled, ptxas hoists the next slot's TMEM
+        // loads above this slot's arithmetic and runs out of registers at next_n >= 3).
 #pragma unroll 1
-      for (int t = 0; t < NN; ++t) {
-        uint32_t lo[32], hi[32];
-        const uint32_t col = static_cast<uint32_t>(acc * C::N + t * kHeads);
-        tmem_ld_32x32b_x32(lane_base + col, lo);
-        tmem_ld_32x32b_x32(lane_base + col + 32, hi);
-        tmem_ld_wait();
-        reg_fence(lo);
-        reg_fence(hi);
-        const float v = scale * weighted_relu_sum(lo, hi, w + t * kHeads);
-        if (store) dst[static_cast<int64_t>(t) * a.out_stride] = v;
+        for (int t = 0; t < NN; ++t) {
+          uint32_t lo[32], hi[32];
+          const uint32_t col = static_cast<uint32_t>(acc * C::N + t * kHeads);
+          tmem_ld_32x32b_x32(lane_base + col, lo);
+          tmem_ld_32x32b_x32(lane_base + col + 32, hi);
+          tmem_ld_wait();
+          reg_fence(lo);
+          reg_fence(hi);
+          const float v = scale * weighted_relu_sum(lo, hi, w + t * kHeads);
+          if (store) dst[static_cast<int64_t>(t) * a.out_stride] = v;
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
       it.next();
       if (!it.valid() || it.b != b) {
+        __syncwarp();
         if (lane == 0) mbar_arrive(&q_empty[qb]);
-      }
-      if (++stage == C::STAGES) {
-        stage = 0;
-        phase ^= 1;
-      }
-      if (++acc == C::ACC) {
-        acc = 0;
-        acc_phase ^= 1;
       }
     }
     if (!ok) flag_error(IDX_DEV_WAIT_TIMEOUT);

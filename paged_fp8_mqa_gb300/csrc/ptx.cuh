@@ -111,6 +111,24 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L1 (LDGSTS), bypassing L1 allocation.
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "l"(policy)
+               : "memory");
+}
+
+// Arrives on `bar` once every cp.async this thread issued so far has landed; the arrival counts
+// toward the barrier's initial count (.noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------------------------
 // tcgen05: tensor memory and the 5th-generation MMA
 // ---------------------------------------------------------------------------------------------
