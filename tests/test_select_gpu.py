@@ -1,0 +1,162 @@
+"""Threshold top-k select: the CUDA path against the oracle's top-k on the GPU's own logits."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_fp8_mqa_gb300 as idx
+from paged_fp8_mqa_gb300 import synth
+from gpu_cases import (check_selection, gpu_logits, gpu_select, kth_values, oracle_logits_cached,
+                       selected_from_slots)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    idx.device_status(clear=True)
+    yield
+    assert idx.device_status(clear=True) == 0, "a kernel raised a device status bit"
+
+
+def _logits_and_thresholds(name):
+    w, ref, _ = oracle_logits_cached(name)
+    got, row_ends = gpu_logits(w, fill=0.0)
+    re = w.row_ends().numpy()
+    kth = torch.from_numpy(kth_values(ref, re, w.top_k))
+    if name == "long_select":
+        thr = synth.thresholds_below_kth(w, kth)
+    else:
+        thr = synth.thresholds_scaled_kth(w, kth)
+    return w, got, row_ends, thr
+
+
+@pytest.mark.parametrize("name", ["long_select", "serving"])
+def test_full_workload_selection(name):
+    w, logits, row_ends, thr = _logits_and_thresholds(name)
+    res = gpu_select(logits, row_ends, thr.cuda(), w.top_k, w.capacity, w.max_seq_len)
+    lc = logits.cpu().numpy()
+    repaired = check_selection(lc, w.row_ends().numpy(), w.top_k, w.capacity, res, thr.numpy())
+    if name == "long_select":
+        assert repaired >= 10  # the ten rows forced to +inf at least
+
+
+def test_any_threshold_gives_the_same_selection():
+    w, logits, row_ends, thr = _logits_and_thresholds("long_select")
+    lc = logits.cpu().numpy()
+    re = w.row_ends().numpy()
+    sets = []
+    g = torch.Generator().manual_seed(5)
+    variants = [thr, torch.full_like(thr, math.inf), torch.full_like(thr, -math.inf),
+                torch.full_like(thr, math.nan), thr + torch.randn(thr.shape, generator=g)]
+    for t in variants:
+        res = gpu_select(logits, row_ends, t.cuda(), w.top_k, w.capacity, w.max_seq_len)
+        check_selection(lc, re, w.top_k, w.capacity, res, t.numpy())
+        k = np.minimum(re, w.top_k)
+        sets.append([selected_from_slots(lc[r], res["candidates"][r], res["ranges"][0, r],
+                                         res["ranges"][1, r], int(k[r])).tolist()
+                     for r in range(len(re))])
+    for s in sets[1:]:
+        assert s == sets[0]
+
+
+def _synthetic(rows, n, kind, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    if kind == "normal":
+        x = torch.randn(rows, n, generator=g)
+    elif kind == "ties":
+        x = torch.randint(-3, 4, (rows, n), generator=g).to(torch.float32)
+    elif kind == "constant":
+        x = torch.full((rows, n), 0.5)
+    elif kind == "zeros":
+        x = torch.zeros(rows, n)
+        x[:, ::3] = -0.0
+    return x
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties", "constant", "zeros"])
+@pytest.mark.parametrize("top_k,capacity", [(64, 63), (64, 200), (1, 0), (300, 299)])
+def test_small_rows(kind, top_k, capacity):
+    rows, n = 9, 20000
+    x = _synthetic(rows, n, kind, seed=top_k)
+    row_ends = torch.tensor([n, 0, 1, 63, 64, 65, 8191, 8193, 19999], dtype=torch.int32)
+    stride = 20480
+    logits = torch.zeros(rows, stride)
+    logits[:, :n] = x
+    lc = logits.numpy()
+    kth = kth_values(lc.astype(np.float64), row_ends.numpy(), top_k)
+    thr = torch.from_numpy(np.nan_to_num(kth, nan=0.0)).to(torch.float32)
+    for t in (thr, thr - 0.25, torch.full_like(thr, math.inf)):
+        res = gpu_select(logits.cuda(), row_ends.cuda(), t.cuda(), top_k, capacity, n)
+        check_selection(lc, row_ends.numpy(), top_k, capacity, res, t.numpy())
+
+
+def test_nan_and_equal_scores_are_ties():
+    """Classification alone (no repair): s > thr is a candidate, s == thr or NaN a tie."""
+    n = 1000
+    x = torch.randn(2, n, generator=torch.Generator().manual_seed(3))
+    x[0, 10] = math.nan
+    x[0, 20] = 0.25
+    x[0, 30] = 0.25
+    x[1, :] = 0.25
+    thr = torch.tensor([0.25, 0.25])
+    row_ends = torch.tensor([n, n], dtype=torch.int32)
+    res = gpu_select(x.cuda(), row_ends.cuda(), thr.cuda(), 64, 2000, n, repair=False)
+    nc, nt, _ = oracle.select_classify(x, row_ends, thr, 64, 2000)
+    assert (res["counters"][:, 0] == nc).all() and (res["counters"][:, 1] == nt).all()
+    tie_idx = sorted(res["candidates"][0, 64 - nt[0]:64, 0])
+    assert tie_idx == [10, 20, 30]
+
+
+def test_classification_only_slots():
+    """Without arrivals: true counts, and the first capacity candidates / top_k ties stored
+    at the slot positions the select's Parameters give, each holding its key and score bits."""
+    w, logits, row_ends, thr = _logits_and_thresholds("serving")
+    lc = logits.cpu().numpy()
+    re = w.row_ends().numpy()
+    res = gpu_select(logits, row_ends, thr.cuda(), w.top_k, w.capacity, w.max_seq_len,
+                     repair=False)
+    nc, nt, _ = oracle.select_classify(lc, re, thr.numpy(), w.top_k, w.capacity)
+    assert (res["counters"][:, 0] == nc).all() and (res["counters"][:, 1] == nt).all()
+    for r in range(len(re)):
+        tk = w.top_k
+        c = res["candidates"][r]
+        stored_c = c[tk:tk + min(nc[r], w.capacity)]
+        stored_t = c[tk - min(nt[r], tk):tk]
+        for items, is_c in ((stored_c, True), (stored_t, False)):
+            if len(items) == 0:
+                continue
+            i = items[:, 0]
+            assert len(np.unique(i)) == len(i) and (i >= 0).all() and (i < re[r]).all()
+            v = lc[r, i]
+            assert (items[:, 1].astype(np.int32).view(np.float32).view(np.uint32)
+                    == v.view(np.uint32)).all()
+            t = thr.numpy()[r]
+            assert (v > t).all() if is_c else (~(v > t) & ~(v < t)).all()
+
+
+def test_arrivals_stay_zero_across_calls():
+    w, logits, row_ends, thr = _logits_and_thresholds("long_select")
+    d = logits.device
+    rows = row_ends.shape[0]
+    arrivals = torch.zeros(rows, dtype=torch.int32, device=d)
+    ranges = torch.zeros(2, rows, dtype=torch.int32, device=d)
+    cand = torch.zeros(rows, w.top_k + w.capacity, 2, dtype=torch.int32, device=d)
+    first = None
+    for it in range(3):
+        counters = torch.zeros(rows, 2, dtype=torch.int32, device=d)
+        t = thr.cuda()
+        idx.threshold_select(logits, row_ends, t, counters, cand, w.top_k, w.capacity,
+                             w.max_seq_len, arrivals=arrivals, ranges=ranges)
+        torch.cuda.synchronize()
+        assert (arrivals == 0).all()
+        c = cand.cpu().numpy()
+        rg = ranges.cpu().numpy()
+        lc = logits.cpu().numpy()
+        k = np.minimum(w.row_ends().numpy(), w.top_k)
+        sel = [selected_from_slots(lc[r], c[r], rg[0, r], rg[1, r], int(k[r])).tolist()
+               for r in range(rows)]
+        first = first or sel
+        assert sel == first
