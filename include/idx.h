@@ -175,6 +175,34 @@ int idx_threshold_select(const float *logits, int64_t logits_row_stride, const i
                          int32_t *ranges, void *stream);
 
 /*
+ * idx_threshold_select_static -- the paper has no counterpart to this entry point; it exists
+ * for callers that cannot allocate device memory.
+ *
+ * idx_threshold_select with repair needs an `arrivals` workspace of one int32 per row.  Some
+ * callers cannot provide one: a serving runtime that plans all of its device memory up front
+ * and forbids allocation inside a step, or a plugin that has no handle on its host
+ * framework's allocator and may not call cudaMalloc itself.  This entry point takes the same
+ * arguments minus `arrivals` and always repairs (so `ranges` is required and capacity must be
+ * >= top_k - 1); the arrival counters live in a static device array inside the library, of
+ * IDX_STATIC_SELECT_MAX_ROWS int32 (64 KiB), which every GPU that loads the library holds until
+ * the process exits.  It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *
+ *   rows   1 .. IDX_STATIC_SELECT_MAX_ROWS; more returns IDX_INVALID_ARG with nothing launched
+ *
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current) and caches it; make that first call before any stream capture.  Each
+ * call clears the counters it uses (an asynchronous memset on `stream`) before its launch.
+ * Every call, on every stream, shares the one array: calls whose work overlaps on the GPU race
+ * on it and must be serialised by the caller (one stream, or events).
+ */
+#define IDX_STATIC_SELECT_MAX_ROWS 16384
+int idx_threshold_select_static(const float *logits, int64_t logits_row_stride,
+                                const int32_t *row_ends, int32_t rows, float *thresholds,
+                                int32_t *counters, int32_t *candidates, int32_t top_k,
+                                int32_t capacity, int32_t max_context, int32_t *ranges,
+                                void *stream);
+
+/*
  * Reads (and, if clear != 0, resets) the OR of the device-side status bits (IDX_DEV_*) that
  * every kernel of this library has raised on the current device since the last reset.
  * Synchronous (it copies from the device); a debugging aid, not for the hot path.

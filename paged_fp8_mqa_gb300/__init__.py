@@ -120,6 +120,26 @@ def idx_threshold_select(logits, logits_row_stride, row_ends, rows, thresholds, 
                                       arrivals, ranges, stream)
 
 
+def idx_threshold_select_static(logits, logits_row_stride, row_ends, rows, thresholds,
+                                counters, candidates, top_k, capacity, max_context, ranges,
+                                stream) -> int:
+    """Mirror of the allocation-free select: like idx_threshold_select with repair, but the
+    arrival counters live in the library's static device array (at most
+    IDX_STATIC_SELECT_MAX_ROWS rows), for callers that cannot allocate a workspace."""
+    L = lib()
+    f = L.idx_threshold_select_static
+    if f.argtypes is None:
+        c = ctypes
+        f.restype = c.c_int
+        f.argtypes = [c.c_void_p, c.c_int64, c.c_void_p, c.c_int32, c.c_void_p, c.c_void_p,
+                      c.c_void_p, c.c_int32, c.c_int32, c.c_int32, c.c_void_p, c.c_void_p]
+    return f(logits, logits_row_stride, row_ends, rows, thresholds, counters, candidates, top_k,
+             capacity, max_context, ranges, stream)
+
+
+IDX_STATIC_SELECT_MAX_ROWS = 16384
+
+
 def idx_device_status(clear: bool = False) -> int:
     out = ctypes.c_int32(0)
     _check(lib().idx_device_status(ctypes.byref(out), int(clear)))

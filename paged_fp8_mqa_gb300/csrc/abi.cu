@@ -278,6 +278,50 @@ IDX_EXPORT int idx_threshold_select(const float *logits, int64_t logits_row_stri
   return IDX_OK;
 }
 
+IDX_EXPORT int idx_threshold_select_static(const float *logits, int64_t logits_row_stride,
+                                           const int32_t *row_ends, int32_t rows,
+                                           float *thresholds, int32_t *counters,
+                                           int32_t *candidates, int32_t top_k, int32_t capacity,
+                                           int32_t max_context, int32_t *ranges, void *stream) {
+  g_error.clear();
+  if (logits == nullptr || row_ends == nullptr || thresholds == nullptr || counters == nullptr ||
+      candidates == nullptr || ranges == nullptr)
+    return fail(IDX_INVALID_ARG,
+                "logits, row_ends, thresholds, counters, candidates, ranges: NULL");
+  if (rows < 0 || rows > IDX_STATIC_SELECT_MAX_ROWS)
+    return fail(IDX_INVALID_ARG, "rows must be 0.." + std::to_string(IDX_STATIC_SELECT_MAX_ROWS) +
+                                     ": the library's static arrival counters hold " +
+                                     std::to_string(IDX_STATIC_SELECT_MAX_ROWS) + " rows");
+  if (top_k < 1 || capacity < 0 || max_context < 0 ||
+      static_cast<int64_t>(top_k) + capacity > (INT32_MAX / 2))
+    return fail(IDX_INVALID_ARG, "top_k >= 1, capacity >= 0, max_context >= 0 required");
+  if (capacity < top_k - 1) return fail(IDX_INVALID_ARG, "capacity must be >= top_k - 1");
+  if (logits_row_stride < max_context || logits_row_stride % 4 != 0)
+    return fail(IDX_INVALID_ARG, "logits_row_stride must be >= max_context and a multiple of 4");
+  if (!aligned(logits, 16)) return fail(IDX_INVALID_ARG, "logits must be 16-byte aligned");
+  if (!aligned(candidates, 8) || !aligned(counters, 4) || !aligned(thresholds, 4) ||
+      !aligned(row_ends, 4) || !aligned(ranges, 4))
+    return fail(IDX_INVALID_ARG, "candidates must be 8-byte aligned, int32/float32 4-byte");
+  if (rows == 0) return IDX_OK;
+  idx::SelectArgs a;
+  a.logits = logits;
+  a.row_stride = logits_row_stride;
+  a.row_ends = row_ends;
+  a.thresholds = thresholds;
+  a.counters = counters;
+  a.candidates = candidates;
+  a.arrivals = nullptr;  // replaced by the static array
+  a.ranges = ranges;
+  a.rows = rows;
+  a.top_k = top_k;
+  a.capacity = capacity;
+  a.max_context = max_context;
+  const cudaError_t e =
+      idx::launch_threshold_select_static(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "static select launch");
+  return IDX_OK;
+}
+
 IDX_EXPORT int idx_device_status(int32_t *status_out, int32_t clear) {
   g_error.clear();
   if (status_out == nullptr) return fail(IDX_INVALID_ARG, "status_out is NULL");

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/idx.h"
+
 namespace idx {
 
 // Largest batch (requests per call) the kernels accept: the logits kernel keeps every
@@ -51,6 +53,10 @@ struct SelectArgs {
 };
 
 cudaError_t launch_threshold_select(const SelectArgs &args, cudaStream_t stream);
+
+// The same launch with `args.arrivals` replaced by the library's own static device array
+// (at most IDX_STATIC_SELECT_MAX_ROWS rows; the caller checks).
+cudaError_t launch_threshold_select_static(SelectArgs args, cudaStream_t stream);
 
 // Device-side status words of each translation unit (IDX_DEV_* bits).
 cudaError_t logits_status(int32_t *value, bool clear);

@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/idx.h"
 #include "internal.h"
@@ -300,6 +301,41 @@ cudaError_t launch_threshold_select(const SelectArgs &args, cudaStream_t stream)
   const dim3 grid(per_row, args.rows);
   k_threshold_select<<<grid, kThreads, 0, stream>>>(args);
   return cudaGetLastError();
+}
+
+// ---- allocation-free variant ---------------------------------------------------------------
+// Arrival counters used by idx_threshold_select_static instead of a caller-provided workspace:
+// one int32 per logits row, IDX_STATIC_SELECT_MAX_ROWS of them (64 KiB), resident on every GPU
+// that loads this library until the process exits.  All calls share it.
+static __device__ __align__(256) int32_t g_static_arrivals[IDX_STATIC_SELECT_MAX_ROWS];
+
+cudaError_t launch_threshold_select_static(SelectArgs args, cudaStream_t stream) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mutex;
+  static int32_t *device_address[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int32_t *arrivals = nullptr;
+  {
+    // Once per device, with that device current: the array's device address.  In host code the
+    // name g_static_arrivals denotes a host-side stand-in, never usable as a kernel argument.
+    std::lock_guard<std::mutex> lock(mutex);
+    if (device_address[dev] == nullptr) {
+      void *p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_static_arrivals);
+      if (e != cudaSuccess) return e;
+      device_address[dev] = static_cast<int32_t *>(p);
+    }
+    arrivals = device_address[dev];
+  }
+  // The kernel returns every counter it uses to zero, but a call cut short (an error, a
+  // killed context) could leave a stale count behind: start each call from zero.
+  e = cudaMemsetAsync(arrivals, 0, sizeof(int32_t) * static_cast<size_t>(args.rows), stream);
+  if (e != cudaSuccess) return e;
+  args.arrivals = arrivals;
+  return launch_threshold_select(args, stream);
 }
 
 cudaError_t select_status(int32_t *value, bool clear) {
