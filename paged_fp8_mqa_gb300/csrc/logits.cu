@@ -3,26 +3,26 @@
 //
 //   out[b*n + t, p] = scale[p] * sum_h w[b*n + t, h] * relu(q[b, t, h, :] . k[p, :])
 //
-// One persistent CTA per SM walks a contiguous run of 128-position KV tiles (split.cuh); tile k
-// of the run is the CTA's k-th.  Warp roles, all walking the same tile sequence:
-//   warp 0     producer.  Prologue: computes the CTA's tile range from seq_lens (one warp, no
-//              block-wide synchronisation on the way to the first load).  Per tile: reads the
-//              block table 32 entries at a time, TMA-loads the two 64-token pages' e4m3 values
-//              (8 KiB each, 128-byte swizzled) into a KV stage, and copies their float32 scales
-//              (256 B per page) with one 16-byte cp.async per lane into a separate scale ring.
-//              Per request: TMA-loads q and bulk-copies w into one of two q/w buffers.
+// One persistent CTA per SM owns a contiguous run of 128-position KV tiles (split.cuh).  Warp 0
+// first turns the run into a tile list in shared memory, up to kMaxList tiles at a time:
+// {request | first/last-of-request flags, tile, page id of each of its two 64-token pages},
+// issuing the block-table reads of the whole list in parallel.  Every role then walks the list:
+//   warp 0     producer (one thread): per tile, TMA-loads the two pages' e4m3 values (8 KiB
+//              each, 128-byte swizzled) into a KV stage; per request, TMA-loads q and
+//              bulk-copies w into one of two q/w buffers.
 //   warp 1     MMA issuer (one thread): 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each),
 //              D[128 positions, n*64 query rows] += K_tile[128, 32] * q[n*64, 32]^T into a
 //              float32 TMEM accumulator; commits release the KV stage and fill the accumulator.
 //              The KV tile is the MMA's M side, so TMEM lane = KV position.
 //   warps 2-9  epilogue, two groups of four warps taking alternate tiles.  Warp w reads TMEM
-//              lanes 32*(w%4)..+31, one position per thread; for each draft slot it computes
-//              scale * sum_h w_h * max(s_h, 0) in float32 (packed FMAs) and stores 32
-//              consecutive positions per warp (one 128-byte line per output row).
-// The KV stage is released by the MMA alone: the epilogue never touches it (its scales come
-// from the scale ring, which is deep enough that the producer cannot overwrite an entry the
-// epilogue still needs), so slow epilogue work never stalls the HBM stream beyond the
-// accumulator slack.
+//              lanes 32*(w%4)..+31, one position per thread; each thread fetches its position's
+//              float32 scale from the page's scale region itself (prefetched three of its tiles
+//              ahead), and for each draft slot computes scale * sum_h w_h * max(s_h, 0) in
+//              float32 (packed FMAs), storing 32 consecutive positions per warp (one 128-byte
+//              line per output row).
+// The KV stage is released by the MMA alone, so the epilogue only holds back the producer
+// through the accumulator slack.  A run longer than kMaxList tiles is processed list by list,
+// the whole CTA synchronising between lists.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -50,7 +50,9 @@ constexpr int kPageBytes = kBlock * (kHeadDim + 4);  // 8448
 constexpr int kPageRows = kPageBytes / 128;       // 66 rows of 128 bytes per page
 constexpr int kValueBytes = kBlock * kHeadDim;    // 8192
 constexpr uint32_t kStageBytes = kTileTokens * kHeadDim;  // 16384: two pages of values
-constexpr int kScaleRing = 16;                    // tiles of scales in flight
+constexpr int kMaxList = 256;                     // tiles per tile list
+constexpr int kFirstFlag = 1 << 16;               // record.x = request | flags
+constexpr int kLastFlag = 1 << 17;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
 
 template <int NN>
@@ -63,24 +65,19 @@ struct Cfg {
   static constexpr uint32_t W_FLOATS = NN * kHeads;
   static constexpr uint32_t OFF_KV = 0;
   static constexpr uint32_t OFF_Q = OFF_KV + STAGES * kStageBytes;
-  static constexpr uint32_t OFF_SCALE = OFF_Q + 2 * Q_BYTES;
-  static constexpr uint32_t OFF_W = OFF_SCALE + kScaleRing * kTileTokens * 4;
-  static constexpr uint32_t OFF_BAR = OFF_W + 2 * W_FLOATS * 4;
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + kScaleRing + 2 * ACC + 4 + 1;
+  static constexpr uint32_t OFF_W = OFF_Q + 2 * Q_BYTES;
+  static constexpr uint32_t OFF_LIST = OFF_W + 2 * W_FLOATS * 4;
+  static constexpr uint32_t OFF_BAR = OFF_LIST + kMaxList * 16;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * ACC + 4 + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t OFF_LEN = OFF_MISC + 64;
   static constexpr uint32_t smem_bytes(int batch) {
     return OFF_LEN + 4u * static_cast<uint32_t>(batch) + 1024u;  // + alignment slack
   }
   static_assert(OFF_Q % 1024 == 0 && Q_BYTES % 1024 == 0, "swizzled tiles 1024-aligned");
-  static_assert(OFF_SCALE % 16 == 0 && OFF_W % 16 == 0, "copy destinations 16-byte aligned");
+  static_assert(OFF_W % 16 == 0 && OFF_LIST % 16 == 0, "copy destinations 16-byte aligned");
   static_assert(smem_bytes(kMaxBatch) <= 232448, "fits the 227 KiB per-CTA limit");
   static_assert(ACC * N <= TMEM_COLS && ACC % 2 == 0, "accumulators");
-  // The producer writes tile k's scales once it has passed tile k-1's stage wait, i.e. once the
-  // MMA finished tile k-1-STAGES, whose accumulator wait needed the epilogue to finish tile
-  // k-1-STAGES-ACC (and, each group working in order, every tile up to k-2-STAGES-ACC).  The
-  // entry's previous user, tile k - kScaleRing, must be among those.
-  static_assert(kScaleRing >= STAGES + ACC + 2, "scale ring deep enough");
 };
 
 __device__ __forceinline__ void flag_error(int bits) { atomicOr(&g_logits_status, bits); }
@@ -136,6 +133,89 @@ __device__ __forceinline__ int2 warp_locate(long long flat, long long total, int
   return at;
 }
 
+// Where one warp is in the CTA's tile run while it writes tile lists.
+struct ListCursor {
+  int b, j;      // next tile to list
+  int b_end, j_end;
+  int prev_b;    // request of the last tile of the previous list (-1 before the first)
+};
+
+// Writes the next list (at most kMaxList tiles) into s_list and returns its length; called by
+// all 32 lanes of one warp.  Record: x = request | kFirstFlag | kLastFlag, y = tile,
+// z / w = page id of the tile's first / second page (-1: absent, or outside the pool).
+__device__ int build_list(ListCursor &cur, int batch, const int *s_len, int4 *s_list,
+                          const LogitsArgs &a, int lane) {
+  int n = 0;
+  bool mid = false;  // the list ends inside a request whose tiles continue in the next list
+  int b = cur.b, j = cur.j;
+  while (n < kMaxList && b < batch && (b < cur.b_end || (b == cur.b_end && j < cur.j_end))) {
+    // Lane l lists the in-range tiles of request b + l.
+    const int rb = b + lane;
+    int jlo = 0, jhi = 0;
+    if (rb < batch && rb <= cur.b_end) {
+      jlo = lane == 0 ? j : 0;
+      const int live = tiles_of(s_len[rb]);
+      // A stale caller schedule may name tiles past the live length: never list those.
+      jhi = rb == cur.b_end ? min(cur.j_end, live) : live;
+      jhi = max(jhi, jlo);
+    }
+    const int cnt = jhi - jlo;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int excl = incl - cnt;
+    const int room = kMaxList - n;
+    for (int t = 0; t < cnt && excl + t < room; ++t)
+      s_list[n + excl + t] = make_int4(rb, jlo + t, -1, -1);
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total <= room) {
+      n += total;
+      b += 32;
+      j = 0;
+      mid = false;
+    } else {
+      const int L = __ffs(__ballot_sync(0xffffffffu, incl > room)) - 1;
+      const int l_excl = __shfl_sync(0xffffffffu, excl, L);
+      const int l_jlo = __shfl_sync(0xffffffffu, jlo, L);
+      b += L;
+      j = l_jlo + (room - l_excl);
+      mid = room - l_excl > 0;
+      n = kMaxList;
+    }
+  }
+  __syncwarp();
+  // Flags and page ids, all block-table reads in flight together.  (A record's low 16 bits
+  // stay the request while other lanes add flags, so neighbours can be read concurrently.)
+  for (int i = lane; i < n; i += 32) {
+    const int4 r = s_list[i];
+    const int rb = r.x, rj = r.y;
+    const int bprev = i == 0 ? cur.prev_b : (s_list[i - 1].x & 0xFFFF);
+    const int bnext = i == n - 1 ? (mid ? rb : -1) : (s_list[i + 1].x & 0xFFFF);
+    const int len = s_len[rb];
+    const int npages = len / kBlock + (len % kBlock != 0 ? 1 : 0);
+    const int32_t *row = a.block_tables + static_cast<int64_t>(rb) * a.bt_stride;
+    int page0 = __ldg(row + 2 * rj);
+    int page1 = 2 * rj + 1 < npages ? __ldg(row + 2 * rj + 1) : -1;
+    bool bad = page0 < 0 || page0 >= a.num_blocks;
+    if (bad) page0 = -1;
+    if (2 * rj + 1 < npages && (page1 < 0 || page1 >= a.num_blocks)) {
+      bad = true;
+      page1 = -1;
+    }
+    if (bad) flag_error(IDX_DEV_BAD_PAGE);
+    s_list[i] = make_int4(rb | (bprev != rb ? kFirstFlag : 0) | (bnext != rb ? kLastFlag : 0),
+                          rj, page0, page1);
+  }
+  __syncwarp();
+  if (n > 0) cur.prev_b = s_list[n - 1].x & 0xFFFF;
+  cur.b = b;
+  cur.j = j;
+  return n;
+}
+
 template <int NN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_logits_fp8(const __grid_constant__ CUtensorMap kv_map,
@@ -146,26 +226,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~static_cast<uintptr_t>(1023u));
   uint8_t *s_kv = smem + C::OFF_KV;
   uint8_t *s_q = smem + C::OFF_Q;
-  float *s_scale = reinterpret_cast<float *>(smem + C::OFF_SCALE);
   float *s_w = reinterpret_cast<float *>(smem + C::OFF_W);
+  int4 *s_list = reinterpret_cast<int4 *>(smem + C::OFF_LIST);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *empty = full + C::STAGES;
-  uint64_t *sfull = empty + C::STAGES;
-  uint64_t *acc_full = sfull + kScaleRing;
+  uint64_t *acc_full = empty + C::STAGES;
   uint64_t *acc_empty = acc_full + C::ACC;
   uint64_t *q_full = acc_empty + C::ACC;
   uint64_t *q_empty = q_full + 2;
   uint64_t *drain = q_empty + 2;
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
-  int *s_split = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);  // 4 ints
+  int *s_count = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);  // current list length
   int *s_len = reinterpret_cast<int *>(smem + C::OFF_LEN);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int batch = a.batch;
+  ListCursor cursor{};
 
-  // ---- 1. set-up: warp 0 finds the CTA's tile range, warp 1 prepares barriers and TMEM ------
+  // ---- 1. set-up: warp 0 finds the CTA's tile run, warp 1 prepares barriers and TMEM --------
   if (warp == 0) {
     const int per = (batch + 31) / 32;
     const int lo = min(lane * per, batch);
@@ -195,12 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       s0 = warp_locate(total * blockIdx.x / g, total, lo, hi, excl, mine, s_len, batch);
       s1 = warp_locate(total * (blockIdx.x + 1) / g, total, lo, hi, excl, mine, s_len, batch);
     }
-    if (lane == 0) {
-      s_split[0] = s0.x;
-      s_split[1] = s0.y;
-      s_split[2] = s1.x;
-      s_split[3] = s1.y;
-    }
+    __syncwarp();
+    // Start at the first tile that exists (a stale schedule or empty requests may point past it).
+    const TileIter it = make_iter(s0.x, s0.y, s1.x, s1.y, batch, s_len);
+    cursor = ListCursor{it.b, it.j, it.b_end, it.j_end, -1};
     if (a.row_ends != nullptr) {
       for (int b = blockIdx.x + lane * gridDim.x; b < batch; b += 32 * gridDim.x) {
         const int len = s_len[b];
@@ -216,7 +294,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&full[s], 1);
         mbar_init(&empty[s], 1);  // released by the MMA's commit alone
       }
-      for (int s = 0; s < kScaleRing; ++s) mbar_init(&sfull[s], 32);  // one per producer lane
       for (int c = 0; c < C::ACC; ++c) {
         mbar_init(&acc_full[c], 1);
         mbar_init(&acc_empty[c], 4);  // the four warps of the owning epilogue group
@@ -232,87 +309,188 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(s_tmem, C::TMEM_COLS);
     tmem_relinquish();
   }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem_base = *s_tmem;
-  const TileIter first = make_iter(s_split[0], s_split[1], s_split[2], s_split[3], batch, s_len);
 
-  if (warp == 0) {
-    // ================================ producer ================================================
-    const uint64_t pol_stream = l2_policy_evict_first();
-    const uint64_t pol_keep = l2_policy_evict_last();
-    int stage = 0;
-    uint32_t phase = 0;
-    int qcount = 0, cur_b = -1;
-    int win_b = -1, win_base = 0, win_val = 0;
-    int k = 0;
-    bool ok = true;
-    for (TileIter it = first; it.valid(); it.next(), ++k) {
-      const int b = it.b, j = it.j;
-      if (b != cur_b) {
-        const int qb = qcount & 1;
-        if (!mbar_wait(&q_empty[qb], ((qcount >> 1) & 1) ^ 1, kWaitLimitNs)) {
-          ok = false;
-          break;
+  // Per-role pipeline state, kept across lists.
+  int stage = 0;
+  uint32_t phase = 0;
+  int qcount = 0, qb = 0;
+  int kbase = 0;  // CTA-wide index of the current list's first tile
+  bool ok = true;
+  uint32_t tmem_base = 0;
+
+  for (;;) {
+    if (warp == 0) {
+      const int n = build_list(cursor, batch, s_len, s_list, a, lane);
+      if (lane == 0) *s_count = n;
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    tmem_base = *s_tmem;
+    const int n = *s_count;
+    if (n == 0) break;
+
+    if (warp == 0) {
+      // ============================== producer ================================================
+      if (lane == 0 && ok) {
+        const uint64_t pol_stream = l2_policy_evict_first();
+        const uint64_t pol_keep = l2_policy_evict_last();
+        for (int i = 0; i < n; ++i) {
+          const int4 r = s_list[i];
+          if (r.x & kFirstFlag) {
+            const int b = r.x & 0xFFFF;
+            const int buf = qcount & 1;
+            if (!mbar_wait(&q_empty[buf], ((qcount >> 1) & 1) ^ 1, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&q_full[buf], C::Q_BYTES + C::W_FLOATS * 4);
+            tma_load_2d(s_q + buf * C::Q_BYTES, &q_map, &q_full[buf], 0, b * C::N, pol_keep);
+            bulk_load(s_w + buf * C::W_FLOATS,
+                      a.weights + static_cast<int64_t>(b) * C::W_FLOATS, C::W_FLOATS * 4,
+                      &q_full[buf], pol_keep);
+            ++qcount;
+          }
+          if (!mbar_wait(&empty[stage], phase ^ 1, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t pages = (r.z >= 0 ? 1u : 0u) + (r.w >= 0 ? 1u : 0u);
+          mbar_arrive_expect_tx(&full[stage], kValueBytes * pages);
+          uint8_t *dst = s_kv + stage * kStageBytes;
+          if (r.z >= 0) tma_load_2d(dst, &kv_map, &full[stage], 0, r.z * kPageRows, pol_stream);
+          if (r.w >= 0)
+            tma_load_2d(dst + kValueBytes, &kv_map, &full[stage], 0, r.w * kPageRows,
+                        pol_stream);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&q_full[qb], C::Q_BYTES + C::W_FLOATS * 4);
-          tma_load_2d(s_q + qb * C::Q_BYTES, &q_map, &q_full[qb], 0, b * C::N, pol_keep);
-          bulk_load(s_w + qb * C::W_FLOATS, a.weights + static_cast<int64_t>(b) * C::W_FLOATS,
-                    C::W_FLOATS * 4, &q_full[qb], pol_keep);
-        }
-        cur_b = b;
-        ++qcount;
-      }
-      const int npages = s_len[b] / kBlock + (s_len[b] % kBlock != 0 ? 1 : 0);
-      const int pg0 = 2 * j;
-      const bool has1 = pg0 + 1 < npages;
-      if (b != win_b || pg0 < win_base || pg0 >= win_base + 32) {
-        win_b = b;
-        win_base = pg0 & ~31;
-        const int e = win_base + lane;
-        win_val = e < npages ? __ldg(a.block_tables + static_cast<int64_t>(b) * a.bt_stride + e)
-                             : 0;
-      }
-      const int page0 = __shfl_sync(0xffffffffu, win_val, pg0 - win_base);
-      const int page1 = __shfl_sync(0xffffffffu, win_val, pg0 + 1 - win_base);
-      const bool v0 = page0 >= 0 && page0 < a.num_blocks;
-      const bool v1 = has1 && page1 >= 0 && page1 < a.num_blocks;
-      // Scales of this tile into ring entry k % kScaleRing: lanes 0-15 page 0, 16-31 page 1.
-      {
-        const int slot = k % kScaleRing;
-        const bool mine_valid = lane < 16 ? v0 : v1;
-        const int page = lane < 16 ? page0 : page1;
-        if (mine_valid)
-          cp_async_16(s_scale + slot * kTileTokens + lane * 4,
-                      a.kv + static_cast<int64_t>(page) * kPageBytes + kValueBytes +
-                          (lane & 15) * 16,
-                      pol_stream);
-        cp_async_arrive_noinc(&sfull[slot]);
-      }
-      if (!mbar_wait(&empty[stage], phase ^ 1, kWaitLimitNs)) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        if (!v0 || (has1 && !v1)) flag_error(IDX_DEV_BAD_PAGE);
-        mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(kValueBytes) * (v0 + v1));
-        uint8_t *dst = s_kv + stage * kStageBytes;
-        if (v0) tma_load_2d(dst, &kv_map, &full[stage], 0, page0 * kPageRows, pol_stream);
-        if (v1)
-          tma_load_2d(dst + kValueBytes, &kv_map, &full[stage], 0, page1 * kPageRows, pol_stream);
       }
       __syncwarp();
-      if (++stage == C::STAGES) {
-        stage = 0;
-        phase ^= 1;
+    } else if (warp == 1) {
+      // ============================== MMA issuer ==============================================
+      if (lane == 0 && ok) {
+        constexpr uint32_t idesc = idesc_e4m3_f32(kTileTokens, C::N);
+        for (int i = 0; i < n; ++i) {
+          const int4 r = s_list[i];
+          const int k = kbase + i;
+          const int acc = k % C::ACC;
+          if (r.x & kFirstFlag) {
+            qb = qcount & 1;
+            if (!mbar_wait(&q_full[qb], (qcount >> 1) & 1, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            ++qcount;
+          }
+          if (!mbar_wait(&full[stage], phase, kWaitLimitNs) ||
+              !mbar_wait(&acc_empty[acc], ((k / C::ACC) & 1) ^ 1, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_addr = smem_addr(s_kv + stage * kStageBytes);
+          const uint32_t b_addr = smem_addr(s_q + qb * C::Q_BYTES);
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::N);
+#pragma unroll
+          for (int kk = 0; kk < kHeadDim / 32; ++kk)
+            mma_f8f6f4(d_tmem, smem_desc_sw128(a_addr + 32 * kk),
+                       smem_desc_sw128(b_addr + 32 * kk), idesc, kk > 0 ? 1u : 0u);
+          mma_commit(&empty[stage]);
+          mma_commit(&acc_full[acc]);
+          if (r.x & kLastFlag) mma_commit(&q_empty[qb]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      __syncwarp();
+    } else {
+      // ============================== epilogue ================================================
+      const int group = (warp - kEpiWarpBase) >> 2;  // takes tiles k with k % 2 == group
+      const int quarter = warp & 3;
+      const int pos = quarter * 32 + lane;
+      const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+      // This position's scale in tile list[i] (0 past the list or for a missing page).
+      auto scale_of = [&](int i) -> float {
+        if (i >= n) return 0.0f;
+        const int4 r = s_list[i];
+        const int page = pos < kBlock ? r.z : r.w;
+        if (page < 0) return 0.0f;
+        return __ldg(reinterpret_cast<const float *>(
+            a.kv + static_cast<int64_t>(page) * kPageBytes + kValueBytes + (pos & 63) * 4));
+      };
+      const int first_own = (group - kbase) & 1;
+      float sc0 = scale_of(first_own), sc1 = scale_of(first_own + 2),
+            sc2 = scale_of(first_own + 4);
+      if (ok) {
+        for (int i = 0; i < n; ++i) {
+          const int4 r = s_list[i];
+          const int b = r.x & 0xFFFF;
+          const int k = kbase + i;
+          if (r.x & kFirstFlag) {
+            qb = qcount & 1;
+            if (!mbar_wait(&q_full[qb], (qcount >> 1) & 1, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            ++qcount;
+          }
+          if ((k & 1) == group) {
+            const float scale = sc0;
+            sc0 = sc1;
+            sc1 = sc2;
+            sc2 = scale_of(i + 6);
+            const int acc = k % C::ACC;
+            if (!mbar_wait(&acc_full[acc], (k / C::ACC) & 1, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const float *w = s_w + qb * C::W_FLOATS;
+            const int p = r.y * kTileTokens + pos;
+            const bool store = p < s_len[b];
+            float *dst = a.out + static_cast<int64_t>(b * NN) * a.out_stride + p;
+            // One draft slot at a time (a rolled loop: unrolled, ptxas hoists the next slot's
+            // TMEM loads above this slot's arithmetic and runs out of registers at next_n >= 3).
+#pragma unroll 1
+            for (int t = 0; t < NN; ++t) {
+              uint32_t lo[32], hi[32];
+              const uint32_t col = static_cast<uint32_t>(acc * C::N + t * kHeads);
+              tmem_ld_32x32b_x32(lane_base + col, lo);
+              tmem_ld_32x32b_x32(lane_base + col + 32, hi);
+              tmem_ld_wait();
+              reg_fence(lo);
+              reg_fence(hi);
+              const float v = scale * weighted_relu_sum(lo, hi, w + t * kHeads);
+              if (store) dst[static_cast<int64_t>(t) * a.out_stride] = v;
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          }
+          if (r.x & kLastFlag) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_empty[qb]);
+          }
+        }
       }
     }
-    if (!ok) flag_error(IDX_DEV_WAIT_TIMEOUT);
-    // Never leave copies in flight: wait for the last loads issued into each stage, the last
-    // q/w load, and this lane's cp.async scale copies.
-    const int tail = k < C::STAGES ? k : C::STAGES;
+    kbase += n;
+    // Everyone is done with this list before warp 0 overwrites it.
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+  }
+
+  // ---- 3. teardown ----------------------------------------------------------------------------
+  if (!ok) flag_error(IDX_DEV_WAIT_TIMEOUT);
+  if (warp == 0 && lane == 0) {
+    // Never leave copies in flight: the last loads issued into each stage and the last q/w.
+    const int tail = kbase < C::STAGES ? kbase : C::STAGES;
     for (int d = 1; d <= tail; ++d) {
       const int s = ((stage - d) % C::STAGES + C::STAGES) % C::STAGES;
       const uint32_t ph = (stage - d < 0) ? (phase ^ 1) : phase;
@@ -321,119 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (qcount > 0 &&
         !mbar_wait(&q_full[(qcount - 1) & 1], ((qcount - 1) >> 1) & 1, kWaitLimitNs))
       flag_error(IDX_DEV_WAIT_TIMEOUT);
-    cp_async_wait_all();
-  } else if (warp == 1) {
-    // ================================ MMA issuer ==============================================
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(kTileTokens, C::N);
-      int stage = 0;
-      uint32_t phase = 0;
-      int qcount = 0, cur_b = -1, qb = 0;
-      bool ok = true;
-      int k = 0;
-      for (TileIter it = first; it.valid(); ++k) {
-        const int b = it.b;
-        const int acc = k % C::ACC;
-        const uint32_t acc_phase = (k / C::ACC) & 1;
-        if (b != cur_b) {
-          qb = qcount & 1;
-          if (!mbar_wait(&q_full[qb], (qcount >> 1) & 1, kWaitLimitNs)) {
-            ok = false;
-            break;
-          }
-          cur_b = b;
-          ++qcount;
-        }
-        if (!mbar_wait(&full[stage], phase, kWaitLimitNs) ||
-            !mbar_wait(&acc_empty[acc], acc_phase ^ 1, kWaitLimitNs)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t a_addr = smem_addr(s_kv + stage * kStageBytes);
-        const uint32_t b_addr = smem_addr(s_q + qb * C::Q_BYTES);
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::N);
-#pragma unroll
-        for (int kk = 0; kk < kHeadDim / 32; ++kk)
-          mma_f8f6f4(d_tmem, smem_desc_sw128(a_addr + 32 * kk),
-                     smem_desc_sw128(b_addr + 32 * kk), idesc, kk > 0 ? 1u : 0u);
-        mma_commit(&empty[stage]);
-        mma_commit(&acc_full[acc]);
-        it.next();
-        if (!it.valid() || it.b != b) mma_commit(&q_empty[qb]);
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-      if (!ok) flag_error(IDX_DEV_WAIT_TIMEOUT);
-      // Every MMA issued above has completed once this commit arrives.
-      mma_commit(drain);
-      if (!mbar_wait(drain, 0, kWaitLimitNs)) flag_error(IDX_DEV_WAIT_TIMEOUT);
-    }
-    __syncwarp();
-  } else {
-    // ================================ epilogue ================================================
-    const int group = (warp - kEpiWarpBase) >> 2;  // takes tiles k with k % 2 == group
-    const int quarter = warp & 3;
-    const int pos = quarter * 32 + lane;
-    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    int qcount = 0, cur_b = -1, qb = 0;
-    bool ok = true;
-    int k = 0;
-    for (TileIter it = first; it.valid(); ++k) {
-      const int b = it.b, j = it.j;
-      if (b != cur_b) {
-        qb = qcount & 1;
-        if (!mbar_wait(&q_full[qb], (qcount >> 1) & 1, kWaitLimitNs)) {
-          ok = false;
-          break;
-        }
-        cur_b = b;
-        ++qcount;
-      }
-      if ((k & 1) == group) {
-        const int slot = k % kScaleRing;
-        const int acc = k % C::ACC;
-        if (!mbar_wait(&sfull[slot], (k / kScaleRing) & 1, kWaitLimitNs) ||
-            !mbar_wait(&acc_full[acc], (k / C::ACC) & 1, kWaitLimitNs)) {
-          ok = false;
-          break;
-        }
-        const float scale = s_scale[slot * kTileTokens + pos];
-        tc_fence_after_sync();
-        const float *w = s_w + qb * C::W_FLOATS;
-        const int p = j * kTileTokens + pos;
-        const bool store = p < s_len[b];
-        float *dst = a.out + static_cast<int64_t>(b * NN) * a.out_stride + p;
-        // One draft slot at a time (a rolled loop: unrolled, ptxas hoists the next slot's TMEM
-        // loads above this slot's arithmetic and runs out of registers at next_n >= 3).
-#pragma unroll 1
-        for (int t = 0; t < NN; ++t) {
-          uint32_t lo[32], hi[32];
-          const uint32_t col = static_cast<uint32_t>(acc * C::N + t * kHeads);
-          tmem_ld_32x32b_x32(lane_base + col, lo);
-          tmem_ld_32x32b_x32(lane_base + col + 32, hi);
-          tmem_ld_wait();
-          reg_fence(lo);
-          reg_fence(hi);
-          const float v = scale * weighted_relu_sum(lo, hi, w + t * kHeads);
-          if (store) dst[static_cast<int64_t>(t) * a.out_stride] = v;
-        }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      }
-      it.next();
-      if (!it.valid() || it.b != b) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&q_empty[qb]);
-      }
-    }
-    if (!ok) flag_error(IDX_DEV_WAIT_TIMEOUT);
+  } else if (warp == 1 && lane == 0) {
+    // Every MMA issued has completed once this commit arrives.
+    mma_commit(drain);
+    if (!mbar_wait(drain, 0, kWaitLimitNs)) flag_error(IDX_DEV_WAIT_TIMEOUT);
   }
-
-  // ---- 3. teardown ----------------------------------------------------------------------------
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();

@@ -109,3 +109,31 @@ def test_full_workload(name):
     stats = check_logits(w, got, ref, tol)
     assert stats["checked"] == w.valid_scores()
     assert (row_ends.cpu() == w.row_ends()).all()
+
+
+@pytest.mark.parametrize("num_sms", [1, 2])
+def test_runs_longer_than_one_tile_list(num_sms):
+    """With one or two CTAs each CTA's run spans several tile lists (of at most 256 tiles)."""
+    w = _small(305, 2, [40000, 30000, 5, 0, 7000], max_seq_len=40000)
+    ref, tol = _oracle(w)
+    got, _ = gpu_logits(w, num_sms=num_sms)
+    check_logits(w, got, ref, tol)
+
+
+def test_stale_schedule_terminates():
+    """A schedule computed for other lengths gives wrong coverage but no hang, no fault and no
+    read past any request's pages."""
+    w = _small(306, 1, [3000, 100, 9000, 64])
+    t = to_device(w)
+    other = torch.tensor([9000, 9000, 9000, 9000], dtype=torch.int32).cuda()
+    stale = idx.schedule(other, 1, 8)
+    pad = idx.idx_padded_seq_len(w.max_seq_len)
+    out = torch.full((w.rows, pad), float("nan"), device="cuda")
+    idx.logits_fp8(t["q"], t["kv"], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len, out=out,
+                   schedule_meta=stale, num_sms=8)
+    torch.cuda.synchronize()
+    # Whatever was written is a correct logit: compare where the stale split reached.
+    ref, tol = _oracle(w)
+    got = out.cpu().double().numpy()
+    m = ~np.isnan(got) & ~np.isnan(ref)
+    assert (np.abs(got[m] - ref[m]) <= 2e-6 * tol[m] + 1e-7).all()
