@@ -15,9 +15,10 @@
 //              float32 TMEM accumulator; commits release the KV stage and fill the accumulator.
 //              The KV tile is the MMA's M side, so TMEM lane = KV position.
 //   warps 2-9  epilogue, two groups of four warps taking alternate tiles.  Warp w reads TMEM
-//              lanes 32*(w%4)..+31, one position per thread; each thread fetches its position's
-//              float32 scale from the page's scale region itself (prefetched three of its tiles
-//              ahead), and for each draft slot computes scale * sum_h w_h * max(s_h, 0) in
+//              lanes 32*(w%4)..+31, one position per thread; each thread cp.asyncs its
+//              position's float32 scale from the page's scale region into a small shared ring,
+//              three of its tiles ahead, and for each draft slot computes
+//              scale * sum_h w_h * max(s_h, 0) in
 //              float32 (packed FMAs), storing 32 consecutive positions per warp (one 128-byte
 //              line per output row).
 // The KV stage is released by the MMA alone, so the epilogue only holds back the producer
@@ -51,6 +52,8 @@ constexpr int kPageRows = kPageBytes / 128;       // 66 rows of 128 bytes per pa
 constexpr int kValueBytes = kBlock * kHeadDim;    // 8192
 constexpr uint32_t kStageBytes = kTileTokens * kHeadDim;  // 16384: two pages of values
 constexpr int kMaxList = 256;                     // tiles per tile list
+constexpr int kScaleAhead = 3;                    // an epilogue group's scale prefetch distance
+constexpr int kScaleSlots = kScaleAhead + 1;      // ... and its ring of tiles in shared memory
 constexpr int kFirstFlag = 1 << 16;               // record.x = request | flags
 constexpr int kLastFlag = 1 << 17;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
@@ -66,7 +69,8 @@ struct Cfg {
   static constexpr uint32_t OFF_KV = 0;
   static constexpr uint32_t OFF_Q = OFF_KV + STAGES * kStageBytes;
   static constexpr uint32_t OFF_W = OFF_Q + 2 * Q_BYTES;
-  static constexpr uint32_t OFF_LIST = OFF_W + 2 * W_FLOATS * 4;
+  static constexpr uint32_t OFF_SCALE = OFF_W + 2 * W_FLOATS * 4;  // 2 groups x kScaleSlots x 128
+  static constexpr uint32_t OFF_LIST = OFF_SCALE + 2 * kScaleSlots * kTileTokens * 4;
   static constexpr uint32_t OFF_BAR = OFF_LIST + kMaxList * 16;
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * ACC + 4 + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -75,15 +79,28 @@ struct Cfg {
     return OFF_LEN + 4u * static_cast<uint32_t>(batch) + 1024u;  // + alignment slack
   }
   static_assert(OFF_Q % 1024 == 0 && Q_BYTES % 1024 == 0, "swizzled tiles 1024-aligned");
-  static_assert(OFF_W % 16 == 0 && OFF_LIST % 16 == 0, "copy destinations 16-byte aligned");
+  static_assert(OFF_W % 16 == 0 && OFF_LIST % 16 == 0 && OFF_SCALE % 16 == 0,
+                "copy destinations 16-byte aligned");
   static_assert(smem_bytes(kMaxBatch) <= 232448, "fits the 227 KiB per-CTA limit");
   static_assert(ACC * N <= TMEM_COLS && ACC % 2 == 0, "accumulators");
 };
 
 __device__ __forceinline__ void flag_error(int bits) { atomicOr(&g_logits_status, bits); }
 
+// relu(s) * 2^-25 on the FMA pipe: a saturating multiply clamps to [0, 1] (NaN to 0), and
+// every score satisfies |s| <= 128 * 448^2 < 2^25, so the product is exact.
+__device__ __forceinline__ float relu_scaled(float s) {
+  float r;
+  asm("mul.rn.sat.f32 %0, %1, 0f33000000;" : "=f"(r) : "f"(s));  // 0f33000000 = 2^-25
+  return r;
+}
+
 // The scale-free part of one logit: sum over the 64 heads of w_h * max(s_h, 0) in float32,
-// with eight partial sums of eight terms each (packed two at a time), combined pairwise.
+// with eight partial sums of eight terms each (packed two at a time), combined pairwise.  Half
+// the heads take their ReLU as max(s, 0) on the ALU pipe, the other half as relu_scaled on the
+// FMA pipe, which balances the two pipes; the latter's partial sums are 2^-25 times what the
+// former would have produced (scaling by a power of two commutes with every rounding), so the
+// final 2^25 rescale makes the result identical to an all-max(s, 0) evaluation.
 __device__ __forceinline__ float weighted_relu_sum(const uint32_t (&lo)[32],
                                                    const uint32_t (&hi)[32], const float *w) {
   const float4 *w4 = reinterpret_cast<const float4 *>(w);
@@ -96,14 +113,15 @@ __device__ __forceinline__ float weighted_relu_sum(const uint32_t (&lo)[32],
     const uint32_t *s = i < 8 ? &lo[4 * i] : &hi[4 * (i - 8)];
     const float2 r01 = make_float2(fmaxf(__uint_as_float(s[0]), 0.0f),
                                    fmaxf(__uint_as_float(s[1]), 0.0f));
-    const float2 r23 = make_float2(fmaxf(__uint_as_float(s[2]), 0.0f),
-                                   fmaxf(__uint_as_float(s[3]), 0.0f));
+    const float2 r23 = make_float2(relu_scaled(__uint_as_float(s[2])),
+                                   relu_scaled(__uint_as_float(s[3])));
     const int q = (i & 1) * 2;
     acc[q] = __ffma2_rn(make_float2(ww.x, ww.y), r01, acc[q]);
     acc[q + 1] = __ffma2_rn(make_float2(ww.z, ww.w), r23, acc[q + 1]);
   }
-  return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
-         ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+  constexpr float kUnscale = 33554432.0f;  // 2^25
+  return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) * kUnscale) +
+         ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y) * kUnscale);
 }
 
 // Finds, in one warp, the (request, tile) of flat tile index `flat` given each lane's segment
@@ -227,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *s_kv = smem + C::OFF_KV;
   uint8_t *s_q = smem + C::OFF_Q;
   float *s_w = reinterpret_cast<float *>(smem + C::OFF_W);
+  float *s_scale = reinterpret_cast<float *>(smem + C::OFF_SCALE);
   int4 *s_list = reinterpret_cast<int4 *>(smem + C::OFF_LIST);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *empty = full + C::STAGES;
@@ -414,18 +433,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int quarter = warp & 3;
       const int pos = quarter * 32 + lane;
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-      // This position's scale in tile list[i] (0 past the list or for a missing page).
-      auto scale_of = [&](int i) -> float {
-        if (i >= n) return 0.0f;
-        const int4 r = s_list[i];
-        const int page = pos < kBlock ? r.z : r.w;
-        if (page < 0) return 0.0f;
-        return __ldg(reinterpret_cast<const float *>(
-            a.kv + static_cast<int64_t>(page) * kPageBytes + kValueBytes + (pos & 63) * 4));
-      };
+      // Scales: this thread copies its position's scale for its group's o-th tile of the list
+      // (list index first_own + 2*o) into ring slot o % kScaleSlots, kScaleAhead tiles ahead,
+      // one cp.async group per tile; the value is read back only after wait_group guarantees
+      // that copy landed, so no register ever waits on an in-flight load.
       const int first_own = (group - kbase) & 1;
-      float sc0 = scale_of(first_own), sc1 = scale_of(first_own + 2),
-            sc2 = scale_of(first_own + 4);
+      float *ring = s_scale + group * kScaleSlots * kTileTokens + pos;
+      auto fetch_scale = [&](int o) {
+        const int i = first_own + 2 * o;
+        if (i < n) {
+          const int4 r = s_list[i];
+          const int page = pos < kBlock ? r.z : r.w;
+          if (page >= 0)
+            cp_async_4(ring + (o % kScaleSlots) * kTileTokens,
+                       a.kv + static_cast<int64_t>(page) * kPageBytes + kValueBytes +
+                           (pos & 63) * 4);
+        }
+        cp_async_commit();
+      };
+#pragma unroll
+      for (int o = 0; o < kScaleAhead; ++o) fetch_scale(o);
+      int own = 0;
       if (ok) {
         for (int i = 0; i < n; ++i) {
           const int4 r = s_list[i];
@@ -440,10 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++qcount;
           }
           if ((k & 1) == group) {
-            const float scale = sc0;
-            sc0 = sc1;
-            sc1 = sc2;
-            sc2 = scale_of(i + 6);
+            fetch_scale(own + kScaleAhead);
+            cp_async_wait_group<kScaleAhead>();
+            const int4 rr = s_list[i];
+            const bool have = (pos < kBlock ? rr.z : rr.w) >= 0;
+            const float scale = have ? ring[(own % kScaleSlots) * kTileTokens] : 0.0f;
+            ++own;
             const int acc = k % C::ACC;
             if (!mbar_wait(&acc_full[acc], (k / C::ACC) & 1, kWaitLimitNs)) {
               ok = false;
@@ -479,6 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (warp >= kEpiWarpBase) cp_async_wait_all();
     kbase += n;
     // Everyone is done with this list before warp 0 overwrites it.
     tc_fence_before_sync();
