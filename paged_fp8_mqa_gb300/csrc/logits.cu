@@ -12,7 +12,7 @@
 //              bulk-copies w into one of two q/w buffers.
 //   warp 1     MMA issuer (one thread): 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each),
 //              D[128 positions, n*64 query rows] += K_tile[128, 32] * q[n*64, 32]^T into a
-//              float32 TMEM accumulator; commits release the KV stage and fill the accumulator.
+//              float32 TMEM accumulator, then one commit that marks the tile done.
 //              The KV tile is the MMA's M side, so TMEM lane = KV position.
 //   warps 2-9  epilogue, two groups of four warps taking alternate tiles.  Warp w reads TMEM
 //              lanes 32*(w%4)..+31, one position per thread; each thread cp.asyncs its
@@ -21,9 +21,18 @@
 //              scale * sum_h w_h * max(s_h, 0) in
 //              float32 (packed FMAs), storing 32 consecutive positions per warp (one 128-byte
 //              line per output row).
-// The KV stage is released by the MMA alone, so the epilogue only holds back the producer
-// through the accumulator slack.  A run longer than kMaxList tiles is processed list by list,
-// the whole CTA synchronising between lists.
+// Barriers.  The issuing thread is the serial point of the pipeline, so it waits on one barrier
+// and commits to one barrier per tile:
+//   full[s]   tile k may be multiplied: its TMA bytes landed (producer's expect_tx), and the
+//             accumulator it overwrites is free (the four epilogue warps that read tile k - ACC,
+//             or the producer for the first ACC tiles).
+//   done[s]   tile k's MMAs completed (one commit): the producer may reuse stage s, and the
+//             epilogue may read tile k's accumulator.
+// Tile k uses stage k % STAGES and accumulator k % ACC.  With ACC even and ACC <= STAGES the
+// parities never alias: the MMA cannot pass tile k + ACC before tile k's epilogue arrived, so
+// done[s] cannot complete tile k + STAGES's phase before tile k's epilogue has waited on it.
+// A run longer than kMaxList tiles is processed list by list, the whole CTA synchronising between
+// lists.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -54,6 +63,7 @@ constexpr uint32_t kStageBytes = kTileTokens * kHeadDim;  // 16384: two pages of
 constexpr int kMaxList = 256;                     // tiles per tile list
 constexpr int kScaleAhead = 3;                    // an epilogue group's scale prefetch distance
 constexpr int kScaleSlots = kScaleAhead + 1;      // ... and its ring of tiles in shared memory
+constexpr int kEpiGroupWarps = 4;                 // warps reading one tile
 constexpr int kFirstFlag = 1 << 16;               // record.x = request | flags
 constexpr int kLastFlag = 1 << 17;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
@@ -72,7 +82,7 @@ struct Cfg {
   static constexpr uint32_t OFF_SCALE = OFF_W + 2 * W_FLOATS * 4;  // 2 groups x kScaleSlots x 128
   static constexpr uint32_t OFF_LIST = OFF_SCALE + 2 * kScaleSlots * kTileTokens * 4;
   static constexpr uint32_t OFF_BAR = OFF_LIST + kMaxList * 16;
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * ACC + 4 + 1;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t OFF_LEN = OFF_MISC + 64;
   static constexpr uint32_t smem_bytes(int batch) {
@@ -82,7 +92,7 @@ struct Cfg {
   static_assert(OFF_W % 16 == 0 && OFF_LIST % 16 == 0 && OFF_SCALE % 16 == 0,
                 "copy destinations 16-byte aligned");
   static_assert(smem_bytes(kMaxBatch) <= 232448, "fits the 227 KiB per-CTA limit");
-  static_assert(ACC * N <= TMEM_COLS && ACC % 2 == 0, "accumulators");
+  static_assert(ACC * N <= TMEM_COLS && ACC % 2 == 0 && ACC <= STAGES, "accumulators");
 };
 
 __device__ __forceinline__ void flag_error(int bits) { atomicOr(&g_logits_status, bits); }
@@ -248,10 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *s_scale = reinterpret_cast<float *>(smem + C::OFF_SCALE);
   int4 *s_list = reinterpret_cast<int4 *>(smem + C::OFF_LIST);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-  uint64_t *empty = full + C::STAGES;
-  uint64_t *acc_full = empty + C::STAGES;
-  uint64_t *acc_empty = acc_full + C::ACC;
-  uint64_t *q_full = acc_empty + C::ACC;
+  uint64_t *done = full + C::STAGES;
+  uint64_t *q_full = done + C::STAGES;
   uint64_t *q_empty = q_full + 2;
   uint64_t *drain = q_empty + 2;
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
@@ -310,12 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensor_map(&kv_map);
       prefetch_tensor_map(&q_map);
       for (int s = 0; s < C::STAGES; ++s) {
-        mbar_init(&full[s], 1);
-        mbar_init(&empty[s], 1);  // released by the MMA's commit alone
-      }
-      for (int c = 0; c < C::ACC; ++c) {
-        mbar_init(&acc_full[c], 1);
-        mbar_init(&acc_empty[c], 4);  // the four warps of the owning epilogue group
+        mbar_init(&full[s], 1 + kEpiGroupWarps);  // producer + the accumulator's last readers
+        mbar_init(&done[s], 1);                   // the MMA's commit
       }
       for (int c = 0; c < 2; ++c) {
         mbar_init(&q_full[c], 1);
@@ -370,12 +374,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                       &q_full[buf], pol_keep);
             ++qcount;
           }
-          if (!mbar_wait(&empty[stage], phase ^ 1, kWaitLimitNs)) {
+          if (!mbar_wait(&done[stage], phase ^ 1, kWaitLimitNs)) {
             ok = false;
             break;
           }
           const uint32_t pages = (r.z >= 0 ? 1u : 0u) + (r.w >= 0 ? 1u : 0u);
           mbar_arrive_expect_tx(&full[stage], kValueBytes * pages);
+          // The first ACC tiles' accumulators were never read: stand in for their readers.
+          if (kbase + i < C::ACC) mbar_arrive_count(&full[stage], kEpiGroupWarps);
           uint8_t *dst = s_kv + stage * kStageBytes;
           if (r.z >= 0) tma_load_2d(dst, &kv_map, &full[stage], 0, r.z * kPageRows, pol_stream);
           if (r.w >= 0)
@@ -404,8 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++qcount;
           }
-          if (!mbar_wait(&full[stage], phase, kWaitLimitNs) ||
-              !mbar_wait(&acc_empty[acc], ((k / C::ACC) & 1) ^ 1, kWaitLimitNs)) {
+          if (!mbar_wait(&full[stage], phase, kWaitLimitNs)) {
             ok = false;
             break;
           }
@@ -417,8 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kHeadDim / 32; ++kk)
             mma_f8f6f4(d_tmem, smem_desc_sw128(a_addr + 32 * kk),
                        smem_desc_sw128(b_addr + 32 * kk), idesc, kk > 0 ? 1u : 0u);
-          mma_commit(&empty[stage]);
-          mma_commit(&acc_full[acc]);
+          mma_commit(&done[stage]);
           if (r.x & kLastFlag) mma_commit(&q_empty[qb]);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -475,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float scale = have ? ring[(own % kScaleSlots) * kTileTokens] : 0.0f;
             ++own;
             const int acc = k % C::ACC;
-            if (!mbar_wait(&acc_full[acc], (k / C::ACC) & 1, kWaitLimitNs)) {
+            if (!mbar_wait(&done[k % C::STAGES], (k / C::STAGES) & 1, kWaitLimitNs)) {
               ok = false;
               break;
             }
@@ -495,12 +499,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_ld_wait();
               reg_fence(lo);
               reg_fence(hi);
+              if (t == NN - 1) {
+                // The accumulator is in registers: free it for tile k + ACC before the arithmetic.
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[(k + C::ACC) % C::STAGES]);
+              }
               const float v = scale * weighted_relu_sum(lo, hi, w + t * kHeads);
               if (store) dst[static_cast<int64_t>(t) * a.out_stride] = v;
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
           }
           if (r.x & kLastFlag) {
             __syncwarp();
