@@ -8,19 +8,21 @@
 // {request | first/last-of-request flags, tile, page id of each of its two 64-token pages},
 // issuing the block-table reads of the whole list in parallel.  Every role then walks the list:
 //   warp 0     producer (one thread): per tile, TMA-loads the two pages' e4m3 values (8 KiB
-//              each, 128-byte swizzled) into a KV stage; per request, TMA-loads q and
-//              bulk-copies w into one of two q/w buffers.
+//              each, 128-byte swizzled) into a KV stage and bulk-copies their float32 scales
+//              (256 B each) into a scale slot; per request, TMA-loads q and bulk-copies w into
+//              one of two q/w buffers.
 //   warp 1     MMA issuer (one thread): 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each),
 //              D[128 positions, n*64 query rows] += K_tile[128, 32] * q[n*64, 32]^T into a
 //              float32 TMEM accumulator, then one commit that marks the tile done.
 //              The KV tile is the MMA's M side, so TMEM lane = KV position.
-//   warps 2-9  epilogue, two groups of four warps taking alternate tiles.  Warp w reads TMEM
-//              lanes 32*(w%4)..+31, one position per thread; each thread cp.asyncs its
-//              position's float32 scale from the page's scale region into a small shared ring,
-//              three of its tiles ahead, and for each draft slot computes
-//              scale * sum_h w_h * max(s_h, 0) in
-//              float32 (packed FMAs), storing 32 consecutive positions per warp (one 128-byte
-//              line per output row).
+//   warps 2-9  epilogue, two groups of four warps taking alternate tiles.  Warp w owns TMEM
+//              lanes 32*(w%4)..+31 and reads them with the 16x256b shape, so that a thread
+//              holds four positions for 16 of the 64 heads: it needs only those heads' weights,
+//              which stay in registers for the whole request.  Per draft slot a thread forms
+//              its four partial sums of w_h * max(s_h, 0) in float32 (packed FMAs), the four
+//              threads of a quad exchange them (reduce-scatter) so that each ends with one
+//              position's complete sum, and the warp stores 32 consecutive positions (one
+//              128-byte line per output row) after multiplying by the position's scale.
 // Barriers.  The issuing thread is the serial point of the pipeline, so it waits on one barrier
 // and commits to one barrier per tile:
 //   full[s]   tile k may be multiplied: its TMA bytes landed (producer's expect_tx), and the
@@ -61,8 +63,7 @@ constexpr int kPageRows = kPageBytes / 128;       // 66 rows of 128 bytes per pa
 constexpr int kValueBytes = kBlock * kHeadDim;    // 8192
 constexpr uint32_t kStageBytes = kTileTokens * kHeadDim;  // 16384: two pages of values
 constexpr int kMaxList = 256;                     // tiles per tile list
-constexpr int kScaleAhead = 3;                    // an epilogue group's scale prefetch distance
-constexpr int kScaleSlots = kScaleAhead + 1;      // ... and its ring of tiles in shared memory
+constexpr int kScaleBytes = kBlock * 4;          // 256: a page's float32 scales
 constexpr int kEpiGroupWarps = 4;                 // warps reading one tile
 constexpr int kFirstFlag = 1 << 16;               // record.x = request | flags
 constexpr int kLastFlag = 1 << 17;
@@ -79,8 +80,12 @@ struct Cfg {
   static constexpr uint32_t OFF_KV = 0;
   static constexpr uint32_t OFF_Q = OFF_KV + STAGES * kStageBytes;
   static constexpr uint32_t OFF_W = OFF_Q + 2 * Q_BYTES;
-  static constexpr uint32_t OFF_SCALE = OFF_W + 2 * W_FLOATS * 4;  // 2 groups x kScaleSlots x 128
-  static constexpr uint32_t OFF_LIST = OFF_SCALE + 2 * kScaleSlots * kTileTokens * 4;
+  // Tile k's scales live in slot k % SCALE_SLOTS.  The producer refills a slot only after tile
+  // k + ACC's MMAs started, which needs tile k's epilogue to have released its accumulator, and
+  // the epilogue reads its scale before that release.
+  static constexpr int SCALE_SLOTS = STAGES + ACC;
+  static constexpr uint32_t OFF_SCALE = OFF_W + 2 * W_FLOATS * 4;
+  static constexpr uint32_t OFF_LIST = OFF_SCALE + SCALE_SLOTS * kTileTokens * 4;
   static constexpr uint32_t OFF_BAR = OFF_LIST + kMaxList * 16;
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -105,33 +110,44 @@ __device__ __forceinline__ float relu_scaled(float s) {
   return r;
 }
 
-// The scale-free part of one logit: sum over the 64 heads of w_h * max(s_h, 0) in float32,
-// with eight partial sums of eight terms each (packed two at a time), combined pairwise.  Half
-// the heads take their ReLU as max(s, 0) on the ALU pipe, the other half as relu_scaled on the
-// FMA pipe, which balances the two pipes; the latter's partial sums are 2^-25 times what the
-// former would have produced (scaling by a power of two commutes with every rounding), so the
-// final 2^25 rescale makes the result identical to an all-max(s, 0) evaluation.
-__device__ __forceinline__ float weighted_relu_sum(const uint32_t (&lo)[32],
-                                                   const uint32_t (&hi)[32], const float *w) {
-  const float4 *w4 = reinterpret_cast<const float4 *>(w);
-  float2 acc[4];
+// Partial logits of the two positions one 16x256b.x8 load covers (lanes g and g + 8 of its
+// window): sums over this thread's 16 heads {8r + 2c, 8r + 2c + 1 : r < 8} of w_h * max(s_h, 0)
+// in float32, the head pair of each r in one packed FMA.  Even r take the ReLU as max(s, 0) on
+// the ALU pipe, odd r as relu_scaled on the FMA pipe, which balances the two pipes; the latter's
+// sums are 2^-25 times what max(s, 0) would have produced (a power-of-two scaling commutes with
+// every rounding), so the final 2^25 rescale makes the result identical to an all-max(s, 0)
+// evaluation of the same summation order.
+__device__ __forceinline__ float2 quad_partials(const uint32_t (&v)[32], const float2 (&w)[8]) {
+  float2 u0 = make_float2(0.0f, 0.0f), u1 = u0, s0 = u0, s1 = u0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float4 ww = w4[i];
-    const uint32_t *s = i < 8 ? &lo[4 * i] : &hi[4 * (i - 8)];
-    const float2 r01 = make_float2(fmaxf(__uint_as_float(s[0]), 0.0f),
-                                   fmaxf(__uint_as_float(s[1]), 0.0f));
-    const float2 r23 = make_float2(relu_scaled(__uint_as_float(s[2])),
-                                   relu_scaled(__uint_as_float(s[3])));
-    const int q = (i & 1) * 2;
-    acc[q] = __ffma2_rn(make_float2(ww.x, ww.y), r01, acc[q]);
-    acc[q + 1] = __ffma2_rn(make_float2(ww.z, ww.w), r23, acc[q + 1]);
+  for (int r = 0; r < 8; ++r) {
+    const float a0 = __uint_as_float(v[4 * r]), a1 = __uint_as_float(v[4 * r + 1]);
+    const float b0 = __uint_as_float(v[4 * r + 2]), b1 = __uint_as_float(v[4 * r + 3]);
+    if (r & 1) {
+      s0 = __ffma2_rn(w[r], make_float2(relu_scaled(a0), relu_scaled(a1)), s0);
+      s1 = __ffma2_rn(w[r], make_float2(relu_scaled(b0), relu_scaled(b1)), s1);
+    } else {
+      u0 = __ffma2_rn(w[r], make_float2(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f)), u0);
+      u1 = __ffma2_rn(w[r], make_float2(fmaxf(b0, 0.0f), fmaxf(b1, 0.0f)), u1);
+    }
   }
   constexpr float kUnscale = 33554432.0f;  // 2^25
-  return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) * kUnscale) +
-         ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y) * kUnscale);
+  return make_float2((u0.x + u0.y) + (s0.x + s0.y) * kUnscale,
+                     (u1.x + u1.y) + (s1.x + s1.y) * kUnscale);
+}
+
+// The four threads of a quad (same g, c = 0..3) hold partial sums of positions g, g + 8, g + 16,
+// g + 24 over disjoint head sets.  Two exchange steps leave thread c with the complete sum of
+// position g + 8c.
+__device__ __forceinline__ float quad_reduce_scatter(float p0, float p1, float p2, float p3, int c) {
+  const bool upper = (c & 2) != 0;  // keeps positions 2, 3
+  float keep0 = upper ? p2 : p0, keep1 = upper ? p3 : p1;
+  const float give0 = upper ? p0 : p2, give1 = upper ? p1 : p3;
+  keep0 += __shfl_xor_sync(0xffffffffu, give0, 2);
+  keep1 += __shfl_xor_sync(0xffffffffu, give1, 2);
+  const bool odd = (c & 1) != 0;  // keeps the second of the two
+  const float mine = odd ? keep1 : keep0, give = odd ? keep0 : keep1;
+  return mine + __shfl_xor_sync(0xffffffffu, give, 1);
 }
 
 // Finds, in one warp, the (request, tile) of flat tile index `flat` given each lane's segment
@@ -379,14 +395,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t pages = (r.z >= 0 ? 1u : 0u) + (r.w >= 0 ? 1u : 0u);
-          mbar_arrive_expect_tx(&full[stage], kValueBytes * pages);
+          mbar_arrive_expect_tx(&full[stage], (kValueBytes + kScaleBytes) * pages);
           // The first ACC tiles' accumulators were never read: stand in for their readers.
           if (kbase + i < C::ACC) mbar_arrive_count(&full[stage], kEpiGroupWarps);
           uint8_t *dst = s_kv + stage * kStageBytes;
-          if (r.z >= 0) tma_load_2d(dst, &kv_map, &full[stage], 0, r.z * kPageRows, pol_stream);
-          if (r.w >= 0)
+          float *sdst = s_scale + ((kbase + i) % C::SCALE_SLOTS) * kTileTokens;
+          if (r.z >= 0) {
+            tma_load_2d(dst, &kv_map, &full[stage], 0, r.z * kPageRows, pol_stream);
+            bulk_load(sdst, a.kv + static_cast<int64_t>(r.z) * kPageBytes + kValueBytes,
+                      kScaleBytes, &full[stage], pol_stream);
+          }
+          if (r.w >= 0) {
             tma_load_2d(dst + kValueBytes, &kv_map, &full[stage], 0, r.w * kPageRows,
                         pol_stream);
+            bulk_load(sdst + kBlock, a.kv + static_cast<int64_t>(r.w) * kPageBytes + kValueBytes,
+                      kScaleBytes, &full[stage], pol_stream);
+          }
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
@@ -435,29 +459,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ============================== epilogue ================================================
       const int group = (warp - kEpiWarpBase) >> 2;  // takes tiles k with k % 2 == group
       const int quarter = warp & 3;
-      const int pos = quarter * 32 + lane;
+      const int c = lane & 3;
+      const int pos = quarter * 32 + (lane >> 2) + 8 * c;  // the position this thread stores
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-      // Scales: this thread copies its position's scale for its group's o-th tile of the list
-      // (list index first_own + 2*o) into ring slot o % kScaleSlots, kScaleAhead tiles ahead,
-      // one cp.async group per tile; the value is read back only after wait_group guarantees
-      // that copy landed, so no register ever waits on an in-flight load.
-      const int first_own = (group - kbase) & 1;
-      float *ring = s_scale + group * kScaleSlots * kTileTokens + pos;
-      auto fetch_scale = [&](int o) {
-        const int i = first_own + 2 * o;
-        if (i < n) {
-          const int4 r = s_list[i];
-          const int page = pos < kBlock ? r.z : r.w;
-          if (page >= 0)
-            cp_async_4(ring + (o % kScaleSlots) * kTileTokens,
-                       a.kv + static_cast<int64_t>(page) * kPageBytes + kValueBytes +
-                           (pos & 63) * 4);
-        }
-        cp_async_commit();
-      };
-#pragma unroll
-      for (int o = 0; o < kScaleAhead; ++o) fetch_scale(o);
-      int own = 0;
+      float2 wreg[NN][8];  // weights of this thread's heads {8r + 2c, 8r + 2c + 1}, per slot
+      int wseq = -1;       // the request (by q/w buffer sequence number) wreg belongs to
       if (ok) {
         for (int i = 0; i < n; ++i) {
           const int4 r = s_list[i];
@@ -472,40 +478,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++qcount;
           }
           if ((k & 1) == group) {
-            fetch_scale(own + kScaleAhead);
-            cp_async_wait_group<kScaleAhead>();
-            const int4 rr = s_list[i];
-            const bool have = (pos < kBlock ? rr.z : rr.w) >= 0;
-            const float scale = have ? ring[(own % kScaleSlots) * kTileTokens] : 0.0f;
-            ++own;
-            const int acc = k % C::ACC;
-            if (!mbar_wait(&done[k % C::STAGES], (k / C::STAGES) & 1, kWaitLimitNs)) {
+            if (wseq != qcount) {
+              const float2 *w2 = reinterpret_cast<const float2 *>(s_w + qb * C::W_FLOATS);
+#pragma unroll
+              for (int t = 0; t < NN; ++t)
+#pragma unroll
+                for (int q = 0; q < 8; ++q) wreg[t][q] = w2[t * (kHeads / 2) + 4 * q + c];
+              wseq = qcount;
+            }
+            const int stage = k % C::STAGES;
+            const uint32_t par = (k / C::STAGES) & 1;
+            // done: tile k's MMAs (so its accumulator) completed.  full: makes the tile's
+            // TMA-written scales visible to this thread (the phase is complete by then).
+            if (!mbar_wait(&done[stage], par, kWaitLimitNs) ||
+                !mbar_wait(&full[stage], par, kWaitLimitNs)) {
               ok = false;
               break;
             }
             tc_fence_after_sync();
-            const float *w = s_w + qb * C::W_FLOATS;
+            const bool have = (pos < kBlock ? r.z : r.w) >= 0;
+            const float scale = have ? s_scale[(k % C::SCALE_SLOTS) * kTileTokens + pos] : 0.0f;
             const int p = r.y * kTileTokens + pos;
             const bool store = p < s_len[b];
             float *dst = a.out + static_cast<int64_t>(b * NN) * a.out_stride + p;
-            // One draft slot at a time (a rolled loop: unrolled, ptxas hoists the next slot's
-            // TMEM loads above this slot's arithmetic and runs out of registers at next_n >= 3).
-#pragma unroll 1
+            const uint32_t col0 = static_cast<uint32_t>((k % C::ACC) * C::N);
+#pragma unroll
             for (int t = 0; t < NN; ++t) {
-              uint32_t lo[32], hi[32];
-              const uint32_t col = static_cast<uint32_t>(acc * C::N + t * kHeads);
-              tmem_ld_32x32b_x32(lane_base + col, lo);
-              tmem_ld_32x32b_x32(lane_base + col + 32, hi);
+              uint32_t va[32], vb[32];  // positions (g, g + 8) and (g + 16, g + 24)
+              const uint32_t col = col0 + static_cast<uint32_t>(t * kHeads);
+              tmem_ld_16x256b_x8(lane_base + col, va);
+              tmem_ld_16x256b_x8(lane_base + (16u << 16) + col, vb);
               tmem_ld_wait();
-              reg_fence(lo);
-              reg_fence(hi);
+              reg_fence(va);
+              reg_fence(vb);
               if (t == NN - 1) {
                 // The accumulator is in registers: free it for tile k + ACC before the arithmetic.
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[(k + C::ACC) % C::STAGES]);
               }
-              const float v = scale * weighted_relu_sum(lo, hi, w + t * kHeads);
+              const float2 p01 = quad_partials(va, wreg[t]);
+              const float2 p23 = quad_partials(vb, wreg[t]);
+              float v = scale * quad_reduce_scatter(p01.x, p01.y, p23.x, p23.y, c);
+              // Orders this slot's arithmetic before the next slot's TMEM loads (volatile asm
+              // keeps its order), so that only one slot's values are live at a time.
+              asm volatile("" : "+f"(v));
               if (store) dst[static_cast<int64_t>(t) * a.out_stride] = v;
             }
           }
@@ -516,7 +533,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (warp >= kEpiWarpBase) cp_async_wait_all();
     kbase += n;
     // Everyone is done with this list before warp 0 overwrites it.
     tc_fence_before_sync();
