@@ -15,7 +15,9 @@
 //              D[128 positions, n*64 query rows] += K_tile[128, 32] * q[n*64, 32]^T into a
 //              float32 TMEM accumulator, then one commit that marks the tile done.
 //              The KV tile is the MMA's M side, so TMEM lane = KV position.
-//   warps 2-9  epilogue, two groups of four warps taking alternate tiles.  Warp w owns TMEM
+//   warps 2-   epilogue, two teams taking alternate tiles: 8 warps, or 16 for next_n >= 3,
+//              where the two warps of a lane quadrant share a tile's draft slots (four epilogue
+//              warps per scheduler hide the arithmetic's latency).  Warp w owns TMEM
 //              lanes 32*(w%4)..+31 and reads them with the 16x256b shape, so that a thread
 //              holds four positions for 16 of the 64 heads: it needs only those heads' weights,
 //              which stay in registers for the whole request.  Per draft slot a thread forms
@@ -52,9 +54,7 @@ __device__ int g_logits_status;
 
 namespace {
 
-constexpr int kWarps = 10;
-constexpr int kThreads = kWarps * 32;
-constexpr int kEpiWarpBase = 2;                  // epilogue warps 2..9
+constexpr int kEpiWarpBase = 2;                  // epilogue warps 2, 3, ...
 constexpr int kHeads = 64;
 constexpr int kHeadDim = 128;
 constexpr int kBlock = 64;                        // tokens per page
@@ -64,16 +64,23 @@ constexpr int kValueBytes = kBlock * kHeadDim;    // 8192
 constexpr uint32_t kStageBytes = kTileTokens * kHeadDim;  // 16384: two pages of values
 constexpr int kMaxList = 256;                     // tiles per tile list
 constexpr int kScaleBytes = kBlock * 4;          // 256: a page's float32 scales
-constexpr int kEpiGroupWarps = 4;                 // warps reading one tile
 constexpr int kFirstFlag = 1 << 16;               // record.x = request | flags
 constexpr int kLastFlag = 1 << 17;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
 
 template <int NN>
 struct Cfg {
+  // Epilogue: two teams take alternate tiles.  A team has SPLIT warps per TMEM lane quadrant;
+  // with next_n >= 3 the two warps of a quadrant share a tile's draft slots, which gives each
+  // scheduler four epilogue warps to hide the arithmetic's latency with.
+  static constexpr int SPLIT = NN <= 2 ? 1 : 2;
+  static constexpr int TEAM_WARPS = 4 * SPLIT;          // warps reading one tile
+  static constexpr int EPI_WARPS = 2 * TEAM_WARPS;
+  static constexpr int THREADS = (kEpiWarpBase + EPI_WARPS) * 32;
+  static constexpr int SLOTS = (NN + SPLIT - 1) / SPLIT;  // draft slots per epilogue warp (max)
   static constexpr int N = NN * kHeads;  // MMA N: query rows of one request
   static constexpr int STAGES = NN <= 2 ? 10 : (NN == 3 ? 9 : 8);
-  static constexpr int ACC = NN <= 2 ? 4 : 2;  // even: tile k's accumulator belongs to group k&1
+  static constexpr int ACC = NN <= 2 ? 4 : 2;  // even: tile k's accumulator belongs to team k&1
   static constexpr int TMEM_COLS = (ACC * N <= 256) ? 256 : 512;
   static constexpr uint32_t Q_BYTES = N * kHeadDim;
   static constexpr uint32_t W_FLOATS = NN * kHeads;
@@ -261,7 +268,7 @@ __device__ int build_list(ListCursor &cur, int batch, const int *s_len, int4 *s_
 }
 
 template <int NN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
     k_logits_fp8(const __grid_constant__ CUtensorMap kv_map,
                  const __grid_constant__ CUtensorMap q_map, const LogitsArgs a) {
   using C = Cfg<NN>;
@@ -334,12 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensor_map(&kv_map);
       prefetch_tensor_map(&q_map);
       for (int s = 0; s < C::STAGES; ++s) {
-        mbar_init(&full[s], 1 + kEpiGroupWarps);  // producer + the accumulator's last readers
+        mbar_init(&full[s], 1 + C::TEAM_WARPS);  // producer + the accumulator's last readers
         mbar_init(&done[s], 1);                   // the MMA's commit
       }
       for (int c = 0; c < 2; ++c) {
         mbar_init(&q_full[c], 1);
-        mbar_init(&q_empty[c], 1 + 8);  // MMA commit + every epilogue warp
+        mbar_init(&q_empty[c], 1 + C::EPI_WARPS);  // MMA commit + every epilogue warp
       }
       mbar_init(drain, 1);
       fence_barrier_init();
@@ -397,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t pages = (r.z >= 0 ? 1u : 0u) + (r.w >= 0 ? 1u : 0u);
           mbar_arrive_expect_tx(&full[stage], (kValueBytes + kScaleBytes) * pages);
           // The first ACC tiles' accumulators were never read: stand in for their readers.
-          if (kbase + i < C::ACC) mbar_arrive_count(&full[stage], kEpiGroupWarps);
+          if (kbase + i < C::ACC) mbar_arrive_count(&full[stage], C::TEAM_WARPS);
           uint8_t *dst = s_kv + stage * kStageBytes;
           float *sdst = s_scale + ((kbase + i) % C::SCALE_SLOTS) * kTileTokens;
           if (r.z >= 0) {
@@ -457,12 +464,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else {
       // ============================== epilogue ================================================
-      const int group = (warp - kEpiWarpBase) >> 2;  // takes tiles k with k % 2 == group
+      const int team = (warp - kEpiWarpBase) / C::TEAM_WARPS;  // takes tiles k with k % 2 == team
+      const int t_first = ((warp - kEpiWarpBase) / 4) % C::SPLIT * C::SLOTS;  // first draft slot
       const int quarter = warp & 3;
       const int c = lane & 3;
       const int pos = quarter * 32 + (lane >> 2) + 8 * c;  // the position this thread stores
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-      float2 wreg[NN][8];  // weights of this thread's heads {8r + 2c, 8r + 2c + 1}, per slot
+      float2 wreg[C::SLOTS][8];  // weights of this thread's heads {8r + 2c, 8r + 2c + 1}, per slot
       int wseq = -1;       // the request (by q/w buffer sequence number) wreg belongs to
       if (ok) {
         for (int i = 0; i < n; ++i) {
@@ -477,13 +485,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++qcount;
           }
-          if ((k & 1) == group) {
+          if ((k & 1) == team) {
             if (wseq != qcount) {
               const float2 *w2 = reinterpret_cast<const float2 *>(s_w + qb * C::W_FLOATS);
 #pragma unroll
-              for (int t = 0; t < NN; ++t)
+              for (int u = 0; u < C::SLOTS; ++u)
 #pragma unroll
-                for (int q = 0; q < 8; ++q) wreg[t][q] = w2[t * (kHeads / 2) + 4 * q + c];
+                for (int q = 0; q < 8; ++q)
+                  wreg[u][q] = t_first + u < NN ? w2[(t_first + u) * (kHeads / 2) + 4 * q + c]
+                                                : make_float2(0.0f, 0.0f);
               wseq = qcount;
             }
             const int stage = k % C::STAGES;
@@ -502,28 +512,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool store = p < s_len[b];
             float *dst = a.out + static_cast<int64_t>(b * NN) * a.out_stride + p;
             const uint32_t col0 = static_cast<uint32_t>((k % C::ACC) * C::N);
+            const int nslots = min(C::SLOTS, NN - t_first);
 #pragma unroll
-            for (int t = 0; t < NN; ++t) {
-              uint32_t va[32], vb[32];  // positions (g, g + 8) and (g + 16, g + 24)
+            for (int u = 0; u < C::SLOTS; ++u) {
+              if (u >= nslots) break;
+              const int t = t_first + u;
+              // The quadrant's two 16-lane windows: positions (g, g + 8) and (g + 16, g + 24).
+              // With the slot split (more warps, fewer registers each) they are read one after
+              // the other, so that only 32 values are live.
               const uint32_t col = col0 + static_cast<uint32_t>(t * kHeads);
+              uint32_t va[32], vb[32];
+              float2 p01;
               tmem_ld_16x256b_x8(lane_base + col, va);
+              if constexpr (C::SPLIT == 2) {
+                tmem_ld_wait();
+                reg_fence(va);
+                p01 = quad_partials(va, wreg[u]);
+                asm volatile("" : "+f"(p01.x), "+f"(p01.y));  // before the next load
+              }
               tmem_ld_16x256b_x8(lane_base + (16u << 16) + col, vb);
               tmem_ld_wait();
-              reg_fence(va);
+              if constexpr (C::SPLIT == 1) reg_fence(va);
               reg_fence(vb);
-              if (t == NN - 1) {
+              if (u == nslots - 1) {
                 // The accumulator is in registers: free it for tile k + ACC before the arithmetic.
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[(k + C::ACC) % C::STAGES]);
               }
-              const float2 p01 = quad_partials(va, wreg[t]);
-              const float2 p23 = quad_partials(vb, wreg[t]);
-              float v = scale * quad_reduce_scatter(p01.x, p01.y, p23.x, p23.y, c);
+              if constexpr (C::SPLIT == 1) p01 = quad_partials(va, wreg[u]);
+              const float2 p23 = quad_partials(vb, wreg[u]);
+              float logit = scale * quad_reduce_scatter(p01.x, p01.y, p23.x, p23.y, c);
               // Orders this slot's arithmetic before the next slot's TMEM loads (volatile asm
               // keeps its order), so that only one slot's values are live at a time.
-              asm volatile("" : "+f"(v));
-              if (store) dst[static_cast<int64_t>(t) * a.out_stride] = v;
+              asm volatile("" : "+f"(logit));
+              if (store) dst[static_cast<int64_t>(t) * a.out_stride] = logit;
             }
           }
           if (r.x & kLastFlag) {
@@ -577,7 +600,7 @@ cudaError_t launch_nn(const CUtensorMap &kv_map, const CUtensorMap &q_map, const
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k_logits_fp8<NN><<<num_ctas, kThreads, smem, stream>>>(kv_map, q_map, args);
+  k_logits_fp8<NN><<<num_ctas, C::THREADS, smem, stream>>>(kv_map, q_map, args);
   return cudaGetLastError();
 }
 
