@@ -194,13 +194,18 @@ struct ListCursor {
 // Writes the next list (at most kMaxList tiles) into s_list and returns its length; called by
 // all 32 lanes of one warp.  Record: x = request | kFirstFlag | kLastFlag, y = tile,
 // z / w = page id of the tile's first / second page (-1: absent, or outside the pool).
-__device__ int build_list(ListCursor &cur, int batch, const int *s_len, int4 *s_list,
-                          const LogitsArgs &a, int lane) {
+//
+// Requests are taken 32 at a time, lane l covering request b + l.  After a scan of their tile
+// counts every record is produced by one lane, 32 * PER records per round (PER per lane), which
+// finds the record's request by a binary search over the scanned counts; each round issues all
+// its block-table reads before writing, so a list of up to 32 * PER tiles costs one memory round
+// trip.  (PER = 1 where the kernel's register budget is tight.)
+template <int PER>
+__device__ __noinline__ int build_list(ListCursor &cur, int batch, const int *s_len, int4 *s_list,
+                                       const LogitsArgs &a, int lane) {
   int n = 0;
-  bool mid = false;  // the list ends inside a request whose tiles continue in the next list
   int b = cur.b, j = cur.j;
   while (n < kMaxList && b < batch && (b < cur.b_end || (b == cur.b_end && j < cur.j_end))) {
-    // Lane l lists the in-range tiles of request b + l.
     const int rb = b + lane;
     int jlo = 0, jhi = 0;
     if (rb < batch && rb <= cur.b_end) {
@@ -218,47 +223,68 @@ __device__ int build_list(ListCursor &cur, int batch, const int *s_len, int4 *s_
       if (lane >= o) incl += y;
     }
     const int excl = incl - cnt;
-    const int room = kMaxList - n;
-    for (int t = 0; t < cnt && excl + t < room; ++t)
-      s_list[n + excl + t] = make_int4(rb, jlo + t, -1, -1);
     const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int room = kMaxList - n;
+    const int take = min(total, room);
+    for (int c0 = 0; c0 < take; c0 += 32 * PER) {
+      int rx[PER], rj[PER], p0[PER], p1[PER];
+      bool has1[PER];
+#pragma unroll
+      for (int h = 0; h < PER; ++h) {
+        const int idx = c0 + 32 * h + lane;
+        // The lane (request) owning record idx: the last lane whose exclusive count <= idx.
+        int src = 0;
+#pragma unroll
+        for (int step = 16; step >= 1; step >>= 1)
+          if (__shfl_sync(0xffffffffu, excl, src + step) <= idx) src += step;
+        const int e_s = __shfl_sync(0xffffffffu, excl, src);
+        const int c_s = __shfl_sync(0xffffffffu, cnt, src);
+        const int j_s = __shfl_sync(0xffffffffu, jlo, src);
+        rx[h] = -1;
+        has1[h] = false;
+        if (idx < take) {
+          const int req = b + src;
+          const int tile = j_s + (idx - e_s);
+          const bool first = n + idx == 0 ? cur.prev_b != req : idx == e_s;
+          const bool last = idx == e_s + c_s - 1;
+          rx[h] = req | (first ? kFirstFlag : 0) | (last ? kLastFlag : 0);
+          rj[h] = tile;
+          const int len = s_len[req];
+          const int npages = len / kBlock + (len % kBlock != 0 ? 1 : 0);
+          const int32_t *row = a.block_tables + static_cast<int64_t>(req) * a.bt_stride;
+          has1[h] = 2 * tile + 1 < npages;
+          p0[h] = __ldg(row + 2 * tile);
+          p1[h] = has1[h] ? __ldg(row + 2 * tile + 1) : -1;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < PER; ++h) {
+        if (rx[h] >= 0) {
+          int q0 = p0[h], q1 = p1[h];
+          bool bad = q0 < 0 || q0 >= a.num_blocks;
+          if (bad) q0 = -1;
+          if (has1[h] && (q1 < 0 || q1 >= a.num_blocks)) {
+            bad = true;
+            q1 = -1;
+          }
+          if (bad) flag_error(IDX_DEV_BAD_PAGE);
+          s_list[n + c0 + 32 * h + lane] = make_int4(rx[h], rj[h], q0, q1);
+        }
+      }
+    }
     if (total <= room) {
       n += total;
       b += 32;
       j = 0;
-      mid = false;
     } else {
+      // The list ends inside request L, which continues in the next list.
       const int L = __ffs(__ballot_sync(0xffffffffu, incl > room)) - 1;
       const int l_excl = __shfl_sync(0xffffffffu, excl, L);
       const int l_jlo = __shfl_sync(0xffffffffu, jlo, L);
       b += L;
       j = l_jlo + (room - l_excl);
-      mid = room - l_excl > 0;
       n = kMaxList;
     }
-  }
-  __syncwarp();
-  // Flags and page ids, all block-table reads in flight together.  (A record's low 16 bits
-  // stay the request while other lanes add flags, so neighbours can be read concurrently.)
-  for (int i = lane; i < n; i += 32) {
-    const int4 r = s_list[i];
-    const int rb = r.x, rj = r.y;
-    const int bprev = i == 0 ? cur.prev_b : (s_list[i - 1].x & 0xFFFF);
-    const int bnext = i == n - 1 ? (mid ? rb : -1) : (s_list[i + 1].x & 0xFFFF);
-    const int len = s_len[rb];
-    const int npages = len / kBlock + (len % kBlock != 0 ? 1 : 0);
-    const int32_t *row = a.block_tables + static_cast<int64_t>(rb) * a.bt_stride;
-    int page0 = __ldg(row + 2 * rj);
-    int page1 = 2 * rj + 1 < npages ? __ldg(row + 2 * rj + 1) : -1;
-    bool bad = page0 < 0 || page0 >= a.num_blocks;
-    if (bad) page0 = -1;
-    if (2 * rj + 1 < npages && (page1 < 0 || page1 >= a.num_blocks)) {
-      bad = true;
-      page1 = -1;
-    }
-    if (bad) flag_error(IDX_DEV_BAD_PAGE);
-    s_list[i] = make_int4(rb | (bprev != rb ? kFirstFlag : 0) | (bnext != rb ? kLastFlag : 0),
-                          rj, page0, page1);
   }
   __syncwarp();
   if (n > 0) cur.prev_b = s_list[n - 1].x & 0xFFFF;
@@ -366,7 +392,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
 
   for (;;) {
     if (warp == 0) {
-      const int n = build_list(cursor, batch, s_len, s_list, a, lane);
+      const int n = build_list<NN <= 2 ? 2 : 1>(cursor, batch, s_len, s_list, a, lane);
       if (lane == 0) *s_count = n;
     }
     tc_fence_before_sync();
