@@ -111,6 +111,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def measured_traffic(workload: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the committed
+    ncu capture, if it was taken on the kernel source as it stands; otherwise None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "paged_fp8_mqa_gb300", "csrc", "logits.cu")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(workload)
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if not rec or rec.get("logits_cu_sha256") != digest:
+        return None
+    return rec["bytes_per_launch"]
+
+
 def device_inputs(w: synth.Workload, dev):
     pools = [w.kv_fused.to(dev)]
     for _ in range(POOL_COPIES - 1):
@@ -125,8 +140,10 @@ def launch(w, t, pool, out, row_ends, stream):
 
 
 def time_device(w, t, steps, warmup, stream, sampler=None):
-    """K launches, each bracketed by CUDA events on the launching stream; returns per-launch
-    milliseconds and the wall-clock milliseconds of the whole region (events too)."""
+    """The timed region: K launches back to back on the launching stream, bracketed by CUDA
+    events (and a barrier plus a device synchronize on both sides).  Returns the milliseconds
+    per launch over the region.  The host enqueues ahead of the device (a short device-side
+    spin opens the region), so the figure is the device's own launch-to-launch time."""
     dev = t["q"].device
     out = torch.empty(w.rows, idx.idx_padded_seq_len(w.max_seq_len), device=dev)
     row_ends = torch.empty(w.rows, dtype=torch.int32, device=dev)
@@ -134,8 +151,6 @@ def time_device(w, t, steps, warmup, stream, sampler=None):
         for i in range(warmup):
             launch(w, t, t["pools"][i % POOL_COPIES], out, row_ends, stream)
     torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     region0 = torch.cuda.Event(enable_timing=True)
     region1 = torch.cuda.Event(enable_timing=True)
     barrier()
@@ -143,18 +158,37 @@ def time_device(w, t, steps, warmup, stream, sampler=None):
     if sampler:
         sampler.mark("t0")
     with torch.cuda.stream(stream):
+        torch.cuda._sleep(2_000_000)  # ~1 ms: the host's enqueueing runs ahead of the device
         region0.record(stream)
+        h0 = time.perf_counter()
         for i in range(steps):
-            starts[i].record(stream)
             launch(w, t, t["pools"][i % POOL_COPIES], out, row_ends, stream)
-            ends[i].record(stream)
+        host_ms = (time.perf_counter() - h0) * 1e3 / steps
         region1.record(stream)
     torch.cuda.synchronize()
     if sampler:
         sampler.mark("t1")
     barrier()
-    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    return per, region0.elapsed_time(region1), out
+    return region0.elapsed_time(region1) / steps, host_ms
+
+
+def time_launch_events(w, t, steps, stream):
+    """Diagnostic: the same launches each bracketed by its own pair of events (which keeps the
+    device from overlapping one launch's start with the previous one's end)."""
+    dev = t["q"].device
+    out = torch.empty(w.rows, idx.idx_padded_seq_len(w.max_seq_len), device=dev)
+    row_ends = torch.empty(w.rows, dtype=torch.int32, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(2_000_000)
+        for i, (a, b) in enumerate(ev):
+            a.record(stream)
+            launch(w, t, t["pools"][i % POOL_COPIES], out, row_ends, stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
 
 def time_e2e(w, dev, steps, stream):
@@ -328,10 +362,10 @@ def main() -> None:
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
-    per, region_ms, _ = time_device(w, t, args.steps, args.warmup, stream, sampler)
+    mean_ms, host_ms = time_device(w, t, args.steps, args.warmup, stream, sampler)
     clocks = sampler.stop() if sampler else None
-    mean_ms = sum(per) / len(per)
     step_ms = reduce_max(mean_ms)
+    event_ms = time_launch_events(w, t, min(args.steps, 200), stream)
     value = reduce_sum(alg["scores"] / (mean_ms * 1e-3) / 1e9)
     status = idx.device_status(clear=True)
 
@@ -347,7 +381,7 @@ def main() -> None:
             alg["flops"] / (mean_ms * 1e-3) / 1e12,
             "peak": peaks["hbm_gbs"] if bound == "hbm" else fp8_peak,
             "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
-            "traffic": None,
+            "traffic": measured_traffic(args.workload),
             "peak_source": peaks["source"] + (" (fp8 = 2 x bf16)" if bound == "tensor" else ""),
             "algorithmic_bytes": alg["bytes"], "kv_bytes": alg["kv_bytes"],
             "flops": alg["flops"],
@@ -360,8 +394,7 @@ def main() -> None:
         # The next_n = 4 workload, timed the same way (a context figure, not the headline).
         w2 = make("mtp")
         t2 = device_inputs(w2, dev)
-        per2, _, _ = time_device(w2, t2, max(3, min(500, args.steps)), args.warmup, stream)
-        m2 = sum(per2) / len(per2)
+        m2, _ = time_device(w2, t2, max(3, min(500, args.steps)), args.warmup, stream)
         a2 = algorithmic(w2)
         r2 = max(a2["bytes"] / (peaks["hbm_gbs"] * 1e9), a2["flops"] / (fp8_peak * 1e12)) * 1e3
         secondary["mtp"] = {"value": a2["scores"] / (m2 * 1e-3) / 1e9, "unit": UNIT,
@@ -381,7 +414,7 @@ def main() -> None:
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32",
             "data": "synthetic", "config": workload_config(w),
-            "region_ms_per_step": region_ms / args.steps,
+            "launch_event_ms": event_ms, "host_enqueue_ms": host_ms,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": args.steps, "device_status": status,
