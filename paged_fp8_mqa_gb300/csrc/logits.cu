@@ -453,12 +453,19 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
       __syncwarp();
     } else if (warp == 1) {
       // ============================== MMA issuer ==============================================
+      // This thread is the pipeline's serial point, so its loop is kept short: the next record
+      // is read one tile ahead, and the shared-memory descriptors are built once and advanced by
+      // adding the stage / buffer offset to their start-address field (addresses stay below
+      // 256 KiB, so the 14-bit field never carries).
       if (lane == 0 && ok) {
         constexpr uint32_t idesc = idesc_e4m3_f32(kTileTokens, C::N);
+        const uint64_t a_desc0 = smem_desc_sw128(smem_addr(s_kv));
+        const uint64_t b_desc0 = smem_desc_sw128(smem_addr(s_q));
+        int acc = kbase % C::ACC;
+        int4 r_next = s_list[0];
         for (int i = 0; i < n; ++i) {
-          const int4 r = s_list[i];
-          const int k = kbase + i;
-          const int acc = k % C::ACC;
+          const int4 r = r_next;
+          if (i + 1 < n) r_next = s_list[i + 1];
           if (r.x & kFirstFlag) {
             qb = qcount & 1;
             if (!mbar_wait(&q_full[qb], (qcount >> 1) & 1, kWaitLimitNs)) {
@@ -472,19 +479,19 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint32_t a_addr = smem_addr(s_kv + stage * kStageBytes);
-          const uint32_t b_addr = smem_addr(s_q + qb * C::Q_BYTES);
+          const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(stage * (kStageBytes >> 4));
+          const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(qb * (C::Q_BYTES >> 4));
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::N);
 #pragma unroll
-          for (int kk = 0; kk < kHeadDim / 32; ++kk)
-            mma_f8f6f4(d_tmem, smem_desc_sw128(a_addr + 32 * kk),
-                       smem_desc_sw128(b_addr + 32 * kk), idesc, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kHeadDim / 32; ++kk)  // K step of 32 bytes = 2 in the field
+            mma_f8f6f4(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, kk > 0 ? 1u : 0u);
           mma_commit(&done[stage]);
           if (r.x & kLastFlag) mma_commit(&q_empty[qb]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
           }
+          if (++acc == C::ACC) acc = 0;
         }
       }
       __syncwarp();
@@ -539,24 +546,29 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
             float *dst = a.out + static_cast<int64_t>(b * NN) * a.out_stride + p;
             const uint32_t col0 = static_cast<uint32_t>((k % C::ACC) * C::N);
             const int nslots = min(C::SLOTS, NN - t_first);
+            // The quadrant's two 16-lane windows hold positions (g, g + 8) and (g + 16, g + 24).
+            // With the slot split (more warps, fewer registers each) they are read one after the
+            // other, so that only 32 values are live.  Without it, the next slot's loads are
+            // issued before this slot's quad reduction, so the shuffles overlap their latency
+            // (with the split that ordering measured slower).
+            uint32_t va[32], vb[32];
 #pragma unroll
             for (int u = 0; u < C::SLOTS; ++u) {
               if (u >= nslots) break;
               const int t = t_first + u;
-              // The quadrant's two 16-lane windows: positions (g, g + 8) and (g + 16, g + 24).
-              // With the slot split (more warps, fewer registers each) they are read one after
-              // the other, so that only 32 values are live.
               const uint32_t col = col0 + static_cast<uint32_t>(t * kHeads);
-              uint32_t va[32], vb[32];
               float2 p01;
-              tmem_ld_16x256b_x8(lane_base + col, va);
+              if (C::SPLIT == 2 || u == 0) {
+                tmem_ld_16x256b_x8(lane_base + col, va);
+                if constexpr (C::SPLIT == 1) tmem_ld_16x256b_x8(lane_base + (16u << 16) + col, vb);
+              }
               if constexpr (C::SPLIT == 2) {
                 tmem_ld_wait();
                 reg_fence(va);
                 p01 = quad_partials(va, wreg[u]);
                 asm volatile("" : "+f"(p01.x), "+f"(p01.y));  // before the next load
+                tmem_ld_16x256b_x8(lane_base + (16u << 16) + col, vb);
               }
-              tmem_ld_16x256b_x8(lane_base + (16u << 16) + col, vb);
               tmem_ld_wait();
               if constexpr (C::SPLIT == 1) reg_fence(va);
               reg_fence(vb);
@@ -567,11 +579,16 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
                 if (lane == 0) mbar_arrive(&full[(k + C::ACC) % C::STAGES]);
               }
               if constexpr (C::SPLIT == 1) p01 = quad_partials(va, wreg[u]);
-              const float2 p23 = quad_partials(vb, wreg[u]);
+              float2 p23 = quad_partials(vb, wreg[u]);
+              // This slot's values are consumed before the next slot's loads reuse the registers
+              // (volatile asm keeps its order).
+              asm volatile("" : "+f"(p01.x), "+f"(p01.y), "+f"(p23.x), "+f"(p23.y));
+              if (C::SPLIT == 1 && u + 1 < nslots) {
+                tmem_ld_16x256b_x8(lane_base + col + kHeads, va);
+                tmem_ld_16x256b_x8(lane_base + (16u << 16) + col + kHeads, vb);
+              }
               float logit = scale * quad_reduce_scatter(p01.x, p01.y, p23.x, p23.y, c);
-              // Orders this slot's arithmetic before the next slot's TMEM loads (volatile asm
-              // keeps its order), so that only one slot's values are live at a time.
-              asm volatile("" : "+f"(logit));
+              if constexpr (C::SPLIT == 2) asm volatile("" : "+f"(logit));  // before the next load
               if (store) dst[static_cast<int64_t>(t) * a.out_stride] = logit;
             }
           }
