@@ -347,9 +347,20 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
       s1 = make_int2(__ldg(a.schedule + 2 * blockIdx.x + 2),
                      __ldg(a.schedule + 2 * blockIdx.x + 3));
     } else {
-      const long long g = gridDim.x;
-      s0 = warp_locate(total * blockIdx.x / g, total, lo, hi, excl, mine, s_len, batch);
-      s1 = warp_locate(total * (blockIdx.x + 1) / g, total, lo, hi, excl, mine, s_len, batch);
+      // The CTA's share [total * c / g, total * (c + 1) / g), in 32-bit arithmetic whenever the
+      // products fit (64-bit division is a long software sequence).
+      const unsigned g = gridDim.x, cb = blockIdx.x;
+      long long f0, f1;
+      if (total <= static_cast<long long>(0xFFFFFFFFu / g)) {
+        const unsigned t32 = static_cast<unsigned>(total);
+        f0 = (t32 * cb) / g;
+        f1 = (t32 * (cb + 1)) / g;
+      } else {
+        f0 = total * cb / g;
+        f1 = total * (cb + 1) / g;
+      }
+      s0 = warp_locate(f0, total, lo, hi, excl, mine, s_len, batch);
+      s1 = warp_locate(f1, total, lo, hi, excl, mine, s_len, batch);
     }
     __syncwarp();
     // Start at the first tile that exists (a stale schedule or empty requests may point past it).
@@ -409,20 +420,6 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
         const uint64_t pol_keep = l2_policy_evict_last();
         for (int i = 0; i < n; ++i) {
           const int4 r = s_list[i];
-          if (r.x & kFirstFlag) {
-            const int b = r.x & 0xFFFF;
-            const int buf = qcount & 1;
-            if (!mbar_wait(&q_empty[buf], ((qcount >> 1) & 1) ^ 1, kWaitLimitNs)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&q_full[buf], C::Q_BYTES + C::W_FLOATS * 4);
-            tma_load_2d(s_q + buf * C::Q_BYTES, &q_map, &q_full[buf], 0, b * C::N, pol_keep);
-            bulk_load(s_w + buf * C::W_FLOATS,
-                      a.weights + static_cast<int64_t>(b) * C::W_FLOATS, C::W_FLOATS * 4,
-                      &q_full[buf], pol_keep);
-            ++qcount;
-          }
           if (!mbar_wait(&done[stage], phase ^ 1, kWaitLimitNs)) {
             ok = false;
             break;
@@ -444,9 +441,24 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
             bulk_load(sdst + kBlock, a.kv + static_cast<int64_t>(r.w) * kPageBytes + kValueBytes,
                       kScaleBytes, &full[stage], pol_stream);
           }
-          if (++stage == C::STAGES) {
+          if (++stage == C::STAGES) {  // (before the q wait, so a timeout there still drains)
             stage = 0;
             phase ^= 1;
+          }
+          // A new request's q and w go out after its first KV tile, whose latency is longer.
+          if (r.x & kFirstFlag) {
+            const int b = r.x & 0xFFFF;
+            const int buf = qcount & 1;
+            if (!mbar_wait(&q_empty[buf], ((qcount >> 1) & 1) ^ 1, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&q_full[buf], C::Q_BYTES + C::W_FLOATS * 4);
+            tma_load_2d(s_q + buf * C::Q_BYTES, &q_map, &q_full[buf], 0, b * C::N, pol_keep);
+            bulk_load(s_w + buf * C::W_FLOATS,
+                      a.weights + static_cast<int64_t>(b) * C::W_FLOATS, C::W_FLOATS * 4,
+                      &q_full[buf], pol_keep);
+            ++qcount;
           }
         }
       }
