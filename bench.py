@@ -2,8 +2,9 @@
 
 Default workload: the decode batch (64 requests, next_n = 1, 64 heads, head_dim 128, 64-token
 blocks, seq_lens uniform in [1024, 32768]).  One step = one launch of the fused logits kernel
-(in-kernel schedule, logits, row_ends).  Metric: Gscores/s, valid (query row, KV position)
-pairs per second.  Inputs are resident in HBM; three copies of the KV pool (each larger than
+(in-kernel schedule, logits, row_ends); for the workloads with a top-k (long_select, serving) the
+step also resets the counters and thresholds and runs the threshold select with its repair.
+Metric: Gscores/s, valid (query row, KV position) pairs per second.  Inputs are resident in HBM; three copies of the KV pool (each larger than
 L2) are used in rotation so no step finds its pool in L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|mtp|long_select|serving]
@@ -135,8 +136,78 @@ def device_inputs(w: synth.Workload, dev):
 
 
 def launch(w, t, pool, out, row_ends, stream):
+    sel = t.get("select")
+    if sel is not None:
+        # The caller's part of the select contract: zeroed counters, this step's thresholds.
+        sel["counters"].zero_()
+        sel["thr"].copy_(sel["thr0"])
     idx.logits_fp8(t["q"], pool, t["weights"], t["bt"], t["seq_lens"], w.max_seq_len, out=out,
                    row_ends_out=row_ends, stream=stream)
+    if sel is not None:
+        idx.threshold_select(out, row_ends, sel["thr"], sel["counters"], sel["cand"], w.top_k,
+                             w.capacity, w.max_seq_len, arrivals=sel["arrivals"],
+                             ranges=sel["ranges"], stream=stream)
+
+
+def selection_inputs(w: synth.Workload, t: dict, dev) -> dict:
+    """Select buffers and this workload's thresholds, derived (outside any timed region) from
+    the logits of one untimed launch: each row's K'-th largest value, perturbed as the workload
+    prescribes (below the K'-th value with forced +inf rows, or x U[0.9, 1.1])."""
+    rows, pad = w.rows, idx.idx_padded_seq_len(w.max_seq_len)
+    out = torch.empty(rows, pad, device=dev)
+    row_ends = torch.empty(rows, dtype=torch.int32, device=dev)
+    idx.logits_fp8(t["q"], t["pools"][0], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len,
+                   out=out, row_ends_out=row_ends)
+    torch.cuda.synchronize()
+    kth = torch.full((rows,), float("nan"), dtype=torch.float64)
+    ends = row_ends.cpu()
+    for r in range(rows):
+        e = int(ends[r])
+        k = min(e, w.top_k)
+        if k:
+            kth[r] = float(torch.topk(out[r, :e], k).values[-1])
+    if w.name == "serving":
+        thr0 = synth.thresholds_scaled_kth(w, kth)
+    else:
+        thr0 = synth.thresholds_below_kth(w, kth)
+    del out
+    return dict(thr0=thr0.to(dev), thr=thr0.to(dev).clone(),
+                counters=torch.zeros(rows, 2, dtype=torch.int32, device=dev),
+                cand=torch.zeros(rows, w.top_k + w.capacity, 2, dtype=torch.int32, device=dev),
+                arrivals=torch.zeros(rows, dtype=torch.int32, device=dev),
+                ranges=torch.zeros(2, rows, dtype=torch.int32, device=dev))
+
+
+def time_select(w, t, stream, launches: int = 200) -> dict:
+    """Diagnostic: the select launch alone, each bracketed by its own events, on logits that
+    stay in L2 between launches (the situation inside a step)."""
+    sel = t["select"]
+    rows, pad = w.rows, idx.idx_padded_seq_len(w.max_seq_len)
+    out = torch.empty(rows, pad, device=t["q"].device)
+    row_ends = torch.empty(rows, dtype=torch.int32, device=t["q"].device)
+    with torch.cuda.stream(stream):
+        idx.logits_fp8(t["q"], t["pools"][0], t["weights"], t["bt"], t["seq_lens"],
+                       w.max_seq_len, out=out, row_ends_out=row_ends, stream=stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(launches)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(2_000_000)
+        for a, b in ev:
+            sel["counters"].zero_()
+            sel["thr"].copy_(sel["thr0"])
+            a.record(stream)
+            idx.threshold_select(out, row_ends, sel["thr"], sel["counters"], sel["cand"],
+                                 w.top_k, w.capacity, w.max_seq_len, arrivals=sel["arrivals"],
+                                 ranges=sel["ranges"], stream=stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    keys = int(w.row_ends().to(torch.int64).sum())
+    return {"ms_per_launch": ms, "keys": keys, "keys_per_s": keys / (ms * 1e-3),
+            "logits_gbs": 4 * keys / (ms * 1e-3) / 1e9,
+            "note": "reads each row's logits (L2-resident after the logits kernel) once; "
+                    "rows that do not fit are re-read by the last CTA's radix repair"}
 
 
 def time_device(w, t, steps, warmup, stream, sampler=None):
@@ -191,25 +262,40 @@ def time_launch_events(w, t, steps, stream):
     return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
 
-def time_e2e(w, dev, steps, stream):
-    """Same metric through the public call with host buffers: every step copies its inputs
-    from pinned host memory, runs the kernel and copies the logits back."""
+def time_e2e(w, dev, steps, stream, sel=None):
+    """Same metric through the public calls with host buffers: every step copies its inputs
+    from pinned host memory, runs the step and copies its result back (the logits, or for a
+    selecting workload the selection: candidates, counters, ranges and thresholds)."""
     host = dict(q=w.q.pin_memory(), kv=w.kv_fused.pin_memory(),
                 weights=w.weights.pin_memory(), bt=w.block_tables.pin_memory(),
                 seq_lens=w.seq_lens.pin_memory())
+    if sel is not None:
+        host["thr"] = sel["thr0"].cpu().pin_memory()
     devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
     pad = idx.idx_padded_seq_len(w.max_seq_len)
     out = torch.empty(w.rows, pad, device=dev)
-    out_h = torch.empty(w.rows, pad).pin_memory()
+    row_ends = torch.empty(w.rows, dtype=torch.int32, device=dev)
+    if sel is None:
+        results = {"out": out}
+    else:
+        results = {"cand": sel["cand"], "counters": sel["counters"], "ranges": sel["ranges"],
+                   "thr": devb["thr"]}
+    back = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in results.items()}
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out.numel() * out.element_size()
+    d2h = sum(v.numel() * v.element_size() for v in back.values())
 
     def step():
         for k in host:
             devb[k].copy_(host[k], non_blocking=True)
         idx.logits_fp8(devb["q"], devb["kv"], devb["weights"], devb["bt"], devb["seq_lens"],
-                       w.max_seq_len, out=out, stream=stream)
-        out_h.copy_(out, non_blocking=True)
+                       w.max_seq_len, out=out, row_ends_out=row_ends, stream=stream)
+        if sel is not None:
+            sel["counters"].zero_()
+            idx.threshold_select(out, row_ends, devb["thr"], sel["counters"], sel["cand"],
+                                 w.top_k, w.capacity, w.max_seq_len, arrivals=sel["arrivals"],
+                                 ranges=sel["ranges"], stream=stream)
+        for k, v in results.items():
+            back[k].copy_(v, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -358,6 +444,8 @@ def main() -> None:
 
     w = make(args.workload)
     t = device_inputs(w, dev)
+    if w.top_k is not None:
+        t["select"] = selection_inputs(w, t, dev)
     alg = algorithmic(w)
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
@@ -366,10 +454,11 @@ def main() -> None:
     clocks = sampler.stop() if sampler else None
     step_ms = reduce_max(mean_ms)
     event_ms = time_launch_events(w, t, min(args.steps, 200), stream)
+    select_diag = time_select(w, t, stream) if "select" in t else None
     value = reduce_sum(alg["scores"] / (mean_ms * 1e-3) / 1e9)
     status = idx.device_status(clear=True)
 
-    e2e_ms, h2d, d2h = time_e2e(w, dev, max(3, min(20, args.steps)), stream)
+    e2e_ms, h2d, d2h = time_e2e(w, dev, max(3, min(20, args.steps)), stream, t.get("select"))
     e2e_value = reduce_sum(alg["scores"] / (e2e_ms * 1e-3) / 1e9)
 
     hbm_ach = alg["bytes"] / (mean_ms * 1e-3) / 1e9
@@ -417,11 +506,13 @@ def main() -> None:
             "launch_event_ms": event_ms, "host_enqueue_ms": host_ms,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps, "device_status": status,
+            "gpu_launches": args.steps * (2 if select_diag else 1), "device_status": status,
             "clocks": clocks, "roofline": roof, "cpu_baseline": cpu,
         }
         if secondary:
             line["secondary"] = secondary
+        if select_diag:
+            line["select"] = select_diag
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -9,11 +9,15 @@
 // (n < top_k), each as (key index, raw float32 bits).
 //
 // With `arrivals`, the last CTA of a row to finish (an atomicAdd ticket, no waiting) decides
-// whether the row fits; if not, it repairs it alone: an MSB-first radix select (4 passes of 8
-// bits over order-preserving uint32 keys, i.e. IEEE totalOrder) finds the row's K'-th largest
-// key v, K' = min(row_end, top_k); a final in-order sweep stores the keys above v as candidates
-// and the lowest-index keys equal to v as ties, K' items in all.  It then rewrites counters,
-// the threshold (v) and ranges, and returns arrivals[r] to zero.
+// whether the row fits; if not, it repairs it alone: an MSB-first radix select over
+// order-preserving uint32 keys (i.e. IEEE totalOrder) finds the row's K'-th largest key v,
+// K' = min(row_end, top_k), and the row's keys above v become candidates and its lowest-index
+// keys equal to v ties, K' items in all.  It then rewrites counters, the threshold (v) and
+// ranges, and returns arrivals[r] to zero.  The repair reads the row twice: an 11-bit histogram
+// of the leading key bits finds the bin holding v; a second sweep stores the keys of higher bins
+// as candidates and gathers the bin's own keys into shared memory, where the remaining 21 bits
+// are resolved.  A bin too large for that buffer falls back to four 8-bit passes over the row
+// and a final in-order sweep.
 
 #include <cuda_runtime.h>
 
@@ -29,10 +33,16 @@ __device__ int g_select_status;
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 8192;       // keys per sweeping CTA (16 per thread)
-constexpr int kRepairSpan = kThreads * 8;
+constexpr int kChunk = 16384;      // keys per sweeping CTA
+constexpr int kSweepLoads = kChunk / (kThreads * 4);  // float4 per thread, all in flight
+constexpr int kBufKeys = 6144;                  // keys of the bin holding v, kept in shared memory
+constexpr int kTieRank = 2048;                  // ties ranked in shared memory (ordered case)
+constexpr uint32_t kSelectSmem = 2048 * 4 + kBufKeys * 8;  // dynamic: histogram + (key, index)
+constexpr int kPassLoads = 8;                   // float4 loads in flight per thread, histogram
+constexpr int kSweepKeys = 16;                  // contiguous keys per thread, final sweep
+constexpr int kRepairSpan = kThreads * kSweepKeys;
 
 // Order-preserving map float -> uint32: a < b in IEEE totalOrder iff key(a) < key(b).
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -100,6 +110,173 @@ __device__ __forceinline__ int block_scan(int v, int *s_warp, int *total) {
   return before + incl - v;
 }
 
+// The bin of the need-th largest key of a histogram of nbins (2048 or 1024) bins, scanning
+// from the top: *s_bin and *s_above (the count of keys in higher bins).  All threads call it.
+__device__ __forceinline__ void find_bin(const unsigned *h, int nbins, unsigned need,
+                                         int *s_bin, unsigned *s_above, int *s_warp) {
+  const int tid = threadIdx.x;
+  const int per = nbins / kThreads;
+  const int hi = nbins - 1 - per * tid;
+  unsigned local = 0;
+  for (int j = 0; j < per; ++j) local += h[hi - j];
+  int total;
+  const unsigned before = static_cast<unsigned>(block_scan(static_cast<int>(local), s_warp, &total));
+  if (before < need && need <= before + local) {
+    unsigned cum = before;
+    for (int j = 0; j < per; ++j) {
+      const unsigned c = h[hi - j];
+      if (cum + c >= need) {
+        *s_bin = hi - j;
+        *s_above = cum;
+        break;
+      }
+      cum += c;
+    }
+  }
+  __syncthreads();
+}
+
+// Two-sweep repair of a row (see the file comment); false if the bin holding v has more keys than
+// the buffer, or more tied keys than can be ranked, in which case nothing it wrote is counted and
+// the caller falls back to repair_row.
+__device__ bool repair_row_fast(const float *row, int row_end, int K, int top_k, int2 *slots,
+                                int *cand_out, int *tie_out, float *thr_out, uint8_t *dyn) {
+  unsigned *s_h = reinterpret_cast<unsigned *>(dyn);                // [2048]
+  uint32_t *s_bkey = reinterpret_cast<uint32_t *>(dyn + 2048 * 4);  // [kBufKeys]
+  int *s_bidx = reinterpret_cast<int *>(s_bkey + kBufKeys);         // [kBufKeys]
+  __shared__ int s_bin, s_nbuf, s_cand, s_ntie;
+  __shared__ unsigned s_above;
+  __shared__ int s_warp[kWarps];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < 2048; i += kThreads) s_h[i] = 0;
+  if (tid == 0) {
+    s_nbuf = 0;
+    s_cand = 0;
+    s_ntie = 0;
+    s_bin = 0;
+    s_above = 0;
+  }
+  __syncthreads();
+  // ---- sweep 1: histogram of the leading 11 key bits
+  for (int base = 0; base < row_end; base += kThreads * 4 * kPassLoads) {
+    float4 v[kPassLoads];
+#pragma unroll
+    for (int u = 0; u < kPassLoads; ++u) {
+      const int i = base + (u * kThreads + tid) * 4;
+      if (i + 3 < row_end) {
+        v[u] = __ldg(reinterpret_cast<const float4 *>(row + i));
+      } else {
+        v[u].x = i < row_end ? __ldg(row + i) : 0.0f;
+        v[u].y = i + 1 < row_end ? __ldg(row + i + 1) : 0.0f;
+        v[u].z = i + 2 < row_end ? __ldg(row + i + 2) : 0.0f;
+        v[u].w = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPassLoads; ++u) {
+      const int i = base + (u * kThreads + tid) * 4;
+      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (i + k < row_end) atomicAdd(&s_h[order_key(e[k]) >> 21], 1u);
+    }
+  }
+  __syncthreads();
+  find_bin(s_h, 2048, static_cast<unsigned>(K), &s_bin, &s_above, s_warp);
+  const uint32_t b1 = static_cast<uint32_t>(s_bin);
+  const unsigned above1 = s_above;
+  const int nb = static_cast<int>(s_h[b1]);
+  if (nb > kBufKeys) return false;
+  // ---- sweep 2: keys of higher bins are candidates; the bin's own keys go to the buffer
+  for (int base = 0; base < row_end; base += kThreads * 4 * kPassLoads) {
+    float4 v[kPassLoads];
+#pragma unroll
+    for (int u = 0; u < kPassLoads; ++u) {
+      const int i = base + (u * kThreads + tid) * 4;
+      if (i + 3 < row_end) {
+        v[u] = __ldg(reinterpret_cast<const float4 *>(row + i));
+      } else {
+        v[u].x = i < row_end ? __ldg(row + i) : 0.0f;
+        v[u].y = i + 1 < row_end ? __ldg(row + i + 1) : 0.0f;
+        v[u].z = i + 2 < row_end ? __ldg(row + i + 2) : 0.0f;
+        v[u].w = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPassLoads; ++u) {
+      const int i = base + (u * kThreads + tid) * 4;
+      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (i + k >= row_end) continue;
+        const uint32_t key = order_key(e[k]);
+        const uint32_t bin = key >> 21;
+        if (bin > b1) {
+          const int n = atomicAdd(&s_cand, 1);
+          slots[top_k + n] = make_int2(i + k, __float_as_int(e[k]));
+        } else if (bin == b1) {
+          const int n = atomicAdd(&s_nbuf, 1);
+          s_bkey[n] = key;
+          s_bidx[n] = i + k;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // ---- the remaining 21 bits among the buffered keys: 11 bits, then 10
+  const unsigned need1 = static_cast<unsigned>(K) - above1;  // 1 <= need1 <= nb
+  for (int i = tid; i < 2048; i += kThreads) s_h[i] = 0;
+  __syncthreads();
+  for (int j = tid; j < nb; j += kThreads) atomicAdd(&s_h[(s_bkey[j] >> 10) & 2047u], 1u);
+  __syncthreads();
+  find_bin(s_h, 2048, need1, &s_bin, &s_above, s_warp);
+  const uint32_t b2 = static_cast<uint32_t>(s_bin);
+  const unsigned need2 = need1 - s_above;
+  for (int i = tid; i < 1024; i += kThreads) s_h[i] = 0;
+  __syncthreads();
+  for (int j = tid; j < nb; j += kThreads)
+    if (((s_bkey[j] >> 10) & 2047u) == b2) atomicAdd(&s_h[s_bkey[j] & 1023u], 1u);
+  __syncthreads();
+  find_bin(s_h, 1024, need2, &s_bin, &s_above, s_warp);
+  const uint32_t vkey = (b1 << 21) | (b2 << 10) | static_cast<uint32_t>(s_bin);
+  const int m = static_cast<int>(need2 - s_above);  // keys equal to v that are kept
+  const int ties = static_cast<int>(s_h[s_bin]);    // keys equal to v in the row
+  const int c = K - m;                              // keys above v
+  if (ties > m && ties > kTieRank) return false;
+  // ---- write the buffered keys above v, and the ties (all, or the m lowest indices)
+  int *s_tidx = reinterpret_cast<int *>(s_h);  // tie indices when they must be ranked
+  __syncthreads();
+  for (int j = tid; j < nb; j += kThreads) {
+    const uint32_t key = s_bkey[j];
+    if (key > vkey) {
+      const int n = atomicAdd(&s_cand, 1);
+      slots[top_k + n] = make_int2(s_bidx[j], __float_as_int(key_value(key)));
+    } else if (key == vkey) {
+      const int n = atomicAdd(&s_ntie, 1);
+      if (ties == m)
+        slots[top_k - 1 - n] = make_int2(s_bidx[j], __float_as_int(key_value(vkey)));
+      else
+        s_tidx[n] = s_bidx[j];
+    }
+  }
+  __syncthreads();
+  if (ties > m) {
+    // Keep the m lowest indices: a tie's rank is the number of ties with a smaller index.
+    for (int j = tid; j < ties; j += kThreads) {
+      const int mine = s_tidx[j];
+      int rank = 0;
+      for (int q = 0; q < ties; ++q) rank += s_tidx[q] < mine ? 1 : 0;
+      if (rank < m) slots[top_k - 1 - rank] = make_int2(mine, __float_as_int(key_value(vkey)));
+    }
+  }
+  if (tid == 0) {
+    *cand_out = c;
+    *tie_out = m;
+    *thr_out = key_value(vkey);
+  }
+  return true;
+}
+
 // Repairs row `r` (called by every thread of the row's last CTA): see the file comment.
 __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2 *slots,
                            int *cand_out, int *tie_out, float *thr_out) {
@@ -119,19 +296,31 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
     for (int i = tid; i < 256; i += kThreads) s_hist[i] = 0;
     __syncthreads();
     const uint32_t prefix = s_prefix, mask = s_mask;
-    for (int i = tid * 4; i < row_end; i += kThreads * 4) {
-      if (i + 3 < row_end) {
-        const float4 v = *reinterpret_cast<const float4 *>(row + i);
-        const float e[4] = {v.x, v.y, v.z, v.w};
+    // kPassLoads float4 per thread in flight before any is used (the row is L2-resident; one
+    // load at a time would leave each pass bound by the L2 latency).
+    for (int base = 0; base < row_end; base += kThreads * 4 * kPassLoads) {
+      float4 v[kPassLoads];
+#pragma unroll
+      for (int u = 0; u < kPassLoads; ++u) {
+        const int i = base + (u * kThreads + tid) * 4;
+        if (i + 3 < row_end) {
+          v[u] = __ldg(reinterpret_cast<const float4 *>(row + i));
+        } else {
+          v[u].x = i < row_end ? __ldg(row + i) : 0.0f;
+          v[u].y = i + 1 < row_end ? __ldg(row + i + 1) : 0.0f;
+          v[u].z = i + 2 < row_end ? __ldg(row + i + 2) : 0.0f;
+          v[u].w = 0.0f;  // i + 3 >= row_end here
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kPassLoads; ++u) {
+        const int i = base + (u * kThreads + tid) * 4;
+        const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t key = order_key(e[k]);
-          if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1u);
-        }
-      } else {
-        for (int k = i; k < row_end; ++k) {
-          const uint32_t key = order_key(row[k]);
-          if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1u);
+          if (i + k < row_end && (key & mask) == prefix)
+            atomicAdd(&s_hist[(key >> shift) & 255u], 1u);
         }
       }
     }
@@ -176,23 +365,30 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
   }
   __syncthreads();
   for (int i0 = 0; i0 < row_end; i0 += kRepairSpan) {
-    const int first = i0 + tid * 8;
-    uint32_t keys[8];
+    // Each thread takes kSweepKeys consecutive keys (four float4 loads in flight), so that one
+    // block scan per span ranks the ties in index order.
+    const int first = i0 + tid * kSweepKeys;
+    uint32_t keys[kSweepKeys];
+    if (first + kSweepKeys - 1 < row_end) {
+      float4 v[kSweepKeys / 4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) keys[k] = 0u;  // key 0 is below every real key's tie/candidate
-    if (first + 7 < row_end) {
-      const float4 a = *reinterpret_cast<const float4 *>(row + first);
-      const float4 b = *reinterpret_cast<const float4 *>(row + first + 4);
-      keys[0] = order_key(a.x); keys[1] = order_key(a.y); keys[2] = order_key(a.z);
-      keys[3] = order_key(a.w); keys[4] = order_key(b.x); keys[5] = order_key(b.y);
-      keys[6] = order_key(b.z); keys[7] = order_key(b.w);
+      for (int u = 0; u < kSweepKeys / 4; ++u)
+        v[u] = __ldg(reinterpret_cast<const float4 *>(row + first) + u);
+#pragma unroll
+      for (int u = 0; u < kSweepKeys / 4; ++u) {
+        keys[4 * u] = order_key(v[u].x);
+        keys[4 * u + 1] = order_key(v[u].y);
+        keys[4 * u + 2] = order_key(v[u].z);
+        keys[4 * u + 3] = order_key(v[u].w);
+      }
     } else {
-      for (int k = 0; k < 8; ++k)
-        if (first + k < row_end) keys[k] = order_key(row[first + k]);
+#pragma unroll
+      for (int k = 0; k < kSweepKeys; ++k)  // key 0 is below every real key's tie/candidate
+        keys[k] = first + k < row_end ? order_key(__ldg(row + first + k)) : 0u;
     }
     int mine = 0;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < kSweepKeys; ++k) {
       const bool valid = first + k < row_end;
       if (valid && keys[k] > vkey) {
         const int n = atomicAdd(&s_cand, 1);
@@ -203,7 +399,7 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
     int total;
     int rank = s_tie_base + block_scan(mine, s_warp, &total);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < kSweepKeys; ++k) {
       if (first + k < row_end && keys[k] == vkey) {
         if (rank < m) slots[top_k - 1 - rank] = make_int2(first + k, __float_as_int(key_value(vkey)));
         ++rank;
@@ -221,6 +417,7 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
 }
 
 __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs a) {
+  extern __shared__ __align__(16) uint8_t select_smem[];
   const int r = blockIdx.y;
   const int tid = threadIdx.x;
   int row_end = a.row_ends[r];
@@ -234,24 +431,32 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
   // ---- sweep: classify this CTA's keys ------------------------------------------------------
   const int begin = blockIdx.x * kChunk;
   const int end = min(begin + kChunk, row_end);
-  for (int i0 = begin; i0 < end; i0 += kThreads * 4) {
-    const int i = i0 + tid * 4;
-    float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    if (i + 3 < end) {
-      const float4 x = __ldcs(reinterpret_cast<const float4 *>(row + i));
-      v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-    } else {
+  if (begin < end) {
+    float4 v[kSweepLoads];  // all of this thread's loads in flight before any is classified
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (i + k < end) v[k] = row[i + k];
+    for (int u = 0; u < kSweepLoads; ++u) {
+      const int i = begin + (u * kThreads + tid) * 4;
+      if (i + 3 < end) {
+        v[u] = __ldcs(reinterpret_cast<const float4 *>(row + i));
+      } else {
+        v[u].x = i < end ? row[i] : 0.0f;
+        v[u].y = i + 1 < end ? row[i + 1] : 0.0f;
+        v[u].z = i + 2 < end ? row[i + 2] : 0.0f;
+        v[u].w = 0.0f;
+      }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const bool valid = i + k < end;
-      const float s = v[k];
-      const bool is_cand = valid && s > thr;
-      const bool is_tie = valid && !(s > thr) && !(s < thr);
-      offer(is_cand, is_tie, i + k, s, counter, slots, a.top_k, a.capacity);
+    for (int u = 0; u < kSweepLoads; ++u) {
+      const int i = begin + (u * kThreads + tid) * 4;
+      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const bool valid = i + k < end;
+        const float s = e[k];
+        const bool is_cand = valid && s > thr;
+        const bool is_tie = valid && !(s > thr) && !(s < thr);
+        offer(is_cand, is_tie, i + k, s, counter, slots, a.top_k, a.capacity);
+      }
     }
   }
   if (a.arrivals == nullptr) return;
@@ -281,7 +486,10 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
   } else {
     __shared__ int s_c, s_m;
     __shared__ float s_v;
-    repair_row(row, row_end, K, a.top_k, slots, &s_c, &s_m, &s_v);
+    if (!repair_row_fast(row, row_end, K, a.top_k, slots, &s_c, &s_m, &s_v, select_smem)) {
+      __syncthreads();
+      repair_row(row, row_end, K, a.top_k, slots, &s_c, &s_m, &s_v);
+    }
     __syncthreads();
     if (tid == 0) {
       counter[0] = s_c;
@@ -299,7 +507,14 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
 cudaError_t launch_threshold_select(const SelectArgs &args, cudaStream_t stream) {
   const int per_row = args.max_context > 0 ? (args.max_context + kChunk - 1) / kChunk : 1;
   const dim3 grid(per_row, args.rows);
-  k_threshold_select<<<grid, kThreads, 0, stream>>>(args);
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        k_threshold_select, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelectSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  k_threshold_select<<<grid, kThreads, kSelectSmem, stream>>>(args);
   return cudaGetLastError();
 }
 
