@@ -399,6 +399,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   int qcount = 0, qb = 0;
   int kbase = 0;  // CTA-wide index of the current list's first tile
   bool ok = true;
+  bool drained = false;  // (MMA issuer) the drain commit is out
   uint32_t tmem_base = 0;
 
   for (;;) {
@@ -504,6 +505,12 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
             phase ^= 1;
           }
           if (++acc == C::ACC) acc = 0;
+        }
+        // A short list is the run's last: commit the drain behind its MMAs now, so that it has
+        // completed by the teardown.
+        if (ok && n < kMaxList) {
+          mma_commit(drain);
+          drained = true;
         }
       }
       __syncwarp();
@@ -612,6 +619,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
       }
     }
     kbase += n;
+    if (n < kMaxList) break;  // the run ended inside this list
     // Everyone is done with this list before warp 0 overwrites it.
     tc_fence_before_sync();
     __syncthreads();
@@ -619,21 +627,26 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   }
 
   // ---- 3. teardown ----------------------------------------------------------------------------
-  if (!ok) flag_error(IDX_DEV_WAIT_TIMEOUT);
-  if (warp == 0 && lane == 0) {
-    // Never leave copies in flight: the last loads issued into each stage and the last q/w.
-    const int tail = kbase < C::STAGES ? kbase : C::STAGES;
-    for (int d = 1; d <= tail; ++d) {
-      const int s = ((stage - d) % C::STAGES + C::STAGES) % C::STAGES;
-      const uint32_t ph = (stage - d < 0) ? (phase ^ 1) : phase;
-      if (!mbar_wait(&full[s], ph, kWaitLimitNs)) flag_error(IDX_DEV_WAIT_TIMEOUT);
+  // When every role finished its lists, every copy issued was consumed (the MMA waited for it)
+  // and every MMA completed (the epilogue waited for it).  Only after a wait gave up can copies
+  // still be in flight; then the producer waits for the last loads of each stage and the last q/w.
+  if (__syncthreads_or(!ok)) {
+    if (!ok) flag_error(IDX_DEV_WAIT_TIMEOUT);
+    if (warp == 0 && lane == 0) {
+      const int tail = kbase < C::STAGES ? kbase : C::STAGES;
+      for (int d = 1; d <= tail; ++d) {
+        const int s = ((stage - d) % C::STAGES + C::STAGES) % C::STAGES;
+        const uint32_t ph = (stage - d < 0) ? (phase ^ 1) : phase;
+        if (!mbar_wait(&full[s], ph, kWaitLimitNs)) flag_error(IDX_DEV_WAIT_TIMEOUT);
+      }
+      if (qcount > 0 &&
+          !mbar_wait(&q_full[(qcount - 1) & 1], ((qcount - 1) >> 1) & 1, kWaitLimitNs))
+        flag_error(IDX_DEV_WAIT_TIMEOUT);
     }
-    if (qcount > 0 &&
-        !mbar_wait(&q_full[(qcount - 1) & 1], ((qcount - 1) >> 1) & 1, kWaitLimitNs))
-      flag_error(IDX_DEV_WAIT_TIMEOUT);
-  } else if (warp == 1 && lane == 0) {
-    // Every MMA issued has completed once this commit arrives.
-    mma_commit(drain);
+  }
+  if (warp == 1 && lane == 0) {
+    // Every MMA issued (and every commit behind one) has completed once the drain arrives.
+    if (!drained) mma_commit(drain);
     if (!mbar_wait(drain, 0, kWaitLimitNs)) flag_error(IDX_DEV_WAIT_TIMEOUT);
   }
   tc_fence_before_sync();
