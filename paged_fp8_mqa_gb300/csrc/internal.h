@@ -9,6 +9,25 @@
 
 namespace idx {
 
+// Launches `kernel` as a programmatic dependent of the previous kernel in `stream`: the launch may
+// be processed while that kernel still runs, so its latency hides behind it.  Every kernel of
+// this library calls griddep_wait() before it touches global memory, which keeps stream order.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Largest batch (requests per call) the kernels accept: the logits kernel keeps every
 // request's length in shared memory.
 constexpr int kMaxBatch = 4096;

@@ -315,6 +315,10 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   int *s_count = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);  // current list length
   int *s_len = reinterpret_cast<int *>(smem + C::OFF_LEN);
 
+  // The previous kernel in the stream may still be running: no global memory before this.
+  griddep_wait();
+  griddep_launch_dependents();
+
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -668,8 +672,8 @@ cudaError_t launch_nn(const CUtensorMap &kv_map, const CUtensorMap &q_map, const
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k_logits_fp8<NN><<<num_ctas, C::THREADS, smem, stream>>>(kv_map, q_map, args);
-  return cudaGetLastError();
+  return launch_dependent(k_logits_fp8<NN>, dim3(num_ctas), dim3(C::THREADS), smem, stream, kv_map,
+                          q_map, args);
 }
 
 }  // namespace

@@ -17,6 +17,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Programmatic dependent launch.  griddep_wait: returns once every grid this one depends on (the
+// previous kernel in the stream, when it was launched as a programmatic dependent) has completed
+// and its memory operations are visible; a no-op otherwise.  griddep_launch_dependents: the
+// kernels that depend on this grid may be scheduled (they wait for its completion likewise).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t lane_id() {
   uint32_t l;
   asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));

@@ -7,6 +7,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 #include "split.cuh"
 
 namespace idx {
@@ -17,6 +18,9 @@ constexpr int kThreads = 256;
 __global__ void __launch_bounds__(kThreads)
     k_schedule(const int32_t *seq_lens, int64_t stride, int batch, int num_ctas,
                int32_t *schedule) {
+  // The previous kernel in the stream may still be running: no global memory before this.
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ long long smem[];  // [kThreads/32] warp totals, [batch] prefix, [batch] lens
   long long *s_warp = smem;
   long long *s_incl = smem + kThreads / 32;
@@ -42,8 +46,8 @@ cudaError_t launch_schedule(const int32_t *seq_lens, int64_t stride, int batch, 
     configured = true;
   }
   const size_t smem = sizeof(long long) * (kThreads / 32 + batch) + 4 * static_cast<size_t>(batch);
-  k_schedule<<<1, kThreads, smem, stream>>>(seq_lens, stride, batch, num_ctas, schedule);
-  return cudaGetLastError();
+  return launch_dependent(k_schedule, dim3(1), dim3(kThreads), smem, stream, seq_lens, stride, batch,
+                          num_ctas, schedule);
 }
 
 }  // namespace idx

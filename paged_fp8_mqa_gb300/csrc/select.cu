@@ -26,6 +26,7 @@
 
 #include "../../include/idx.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace idx {
 
@@ -417,6 +418,9 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
 }
 
 __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs a) {
+  // The previous kernel in the stream may still be running: no global memory before this.
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ __align__(16) uint8_t select_smem[];
   const int r = blockIdx.y;
   const int tid = threadIdx.x;
@@ -514,8 +518,7 @@ cudaError_t launch_threshold_select(const SelectArgs &args, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k_threshold_select<<<grid, kThreads, kSelectSmem, stream>>>(args);
-  return cudaGetLastError();
+  return launch_dependent(k_threshold_select, grid, dim3(kThreads), kSelectSmem, stream, args);
 }
 
 // ---- allocation-free variant ---------------------------------------------------------------
