@@ -112,17 +112,26 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# Sources compiled into the logits kernel: the committed traffic figures hold only for them.
+KERNEL_SOURCES = ("logits.cu", "ptx.cuh", "split.cuh", "internal.h")
+
+
+def kernel_sources_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "paged_fp8_mqa_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()
+
+
 def measured_traffic(workload: str):
     """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the committed
-    ncu capture, if it was taken on the kernel source as it stands; otherwise None."""
-    import hashlib
+    ncu capture, if it was taken on the kernel sources as they stand; otherwise None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "paged_fp8_mqa_gb300", "csrc", "logits.cu")
     if not os.path.exists(path):
         return None
     rec = json.load(open(path)).get(workload)
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    if not rec or rec.get("logits_cu_sha256") != digest:
+    if not rec or rec.get("kernel_sources_sha256") != kernel_sources_digest():
         return None
     return rec["bytes_per_launch"]
 

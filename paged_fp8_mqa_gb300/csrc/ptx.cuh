@@ -77,14 +77,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return done != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended for up to `hint_ns` while the phase is
+// incomplete; it resumes as soon as the phase completes.  (Without the hint a try_wait returns
+// after ~80 ns, so a waiting warp keeps issuing and takes issue slots and shared-memory
+// bandwidth from the warps that work.)
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // Waits for the phase of the given parity to complete, for at most `limit_ns` nanoseconds.
 // Returns false (and the caller must stop using the pipeline) if the limit ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0u && global_timer_ns() - start > limit_ns) return false;
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (global_timer_ns() - start > limit_ns) return false;
   }
 }
 
