@@ -157,31 +157,33 @@ __device__ __forceinline__ float quad_reduce_scatter(float p0, float p1, float p
   return mine + __shfl_xor_sync(0xffffffffu, give, 1);
 }
 
-// Finds, in one warp, the (request, tile) of flat tile index `flat` given each lane's segment
-// [seg_lo, seg_hi) of requests, the lane's exclusive tile prefix and its tile count.
-__device__ __forceinline__ int2 warp_locate(long long flat, long long total, int seg_lo,
-                                            int seg_hi, long long excl, long long mine,
-                                            const int *s_len, int batch) {
-  int2 at = make_int2(batch, 0);
-  const bool here = flat < total && flat >= excl && flat < excl + mine;
-  if (here) {
+// Finds, in one warp, the (request, tile) of the flat tile indices f0 and f1 (< f0 + 2^31) given
+// each lane's segment [seg_lo, seg_hi) of requests, the lane's exclusive tile prefix and its tile
+// count: the lanes holding them walk their segment once.  An index >= total gives (batch, 0).
+__device__ __forceinline__ void warp_locate2(long long f0, long long f1, long long total,
+                                             int seg_lo, int seg_hi, long long excl,
+                                             long long mine, const int *s_len, int batch,
+                                             int2 &at0, int2 &at1) {
+  at0 = make_int2(batch, 0);
+  at1 = make_int2(batch, 0);
+  const bool here0 = f0 < total && f0 >= excl && f0 < excl + mine;
+  const bool here1 = f1 < total && f1 >= excl && f1 < excl + mine;
+  if (here0 || here1) {
     long long run = excl;
     for (int b = seg_lo; b < seg_hi; ++b) {
       const int t = tiles_of(s_len[b]);
-      if (flat < run + t) {
-        at = make_int2(b, static_cast<int>(flat - run));
-        break;
-      }
+      if (here0 && f0 >= run && f0 < run + t) at0 = make_int2(b, static_cast<int>(f0 - run));
+      if (here1 && f1 >= run && f1 < run + t) at1 = make_int2(b, static_cast<int>(f1 - run));
       run += t;
     }
   }
-  const unsigned who = __ballot_sync(0xffffffffu, here);
-  if (who) {
-    const int src = __ffs(who) - 1;
-    at.x = __shfl_sync(0xffffffffu, at.x, src);
-    at.y = __shfl_sync(0xffffffffu, at.y, src);
-  }
-  return at;
+  const unsigned who0 = __ballot_sync(0xffffffffu, here0);
+  const unsigned who1 = __ballot_sync(0xffffffffu, here1);
+  const int src0 = who0 ? __ffs(who0) - 1 : 0, src1 = who1 ? __ffs(who1) - 1 : 0;
+  const int2 r0 = make_int2(__shfl_sync(0xffffffffu, at0.x, src0), __shfl_sync(0xffffffffu, at0.y, src0));
+  const int2 r1 = make_int2(__shfl_sync(0xffffffffu, at1.x, src1), __shfl_sync(0xffffffffu, at1.y, src1));
+  if (who0) at0 = r0;
+  if (who1) at1 = r1;
 }
 
 // Where one warp is in the CTA's tile run while it writes tile lists.
@@ -191,18 +193,26 @@ struct ListCursor {
   int prev_b;    // request of the last tile of the previous list (-1 before the first)
 };
 
-// Writes the next list (at most kMaxList tiles) into s_list and returns its length; called by
-// all 32 lanes of one warp.  Record: x = request | kFirstFlag | kLastFlag, y = tile,
-// z / w = page id of the tile's first / second page (-1: absent, or outside the pool).
+// The list builder's state after a list: where the next list starts, and this list's length.
+struct ListResult {
+  ListCursor cur;
+  int n;
+};
+
+// Writes the next list (at most kMaxList tiles) into s_list; called by all 32 lanes of one warp.
+// Record: x = request | kFirstFlag | kLastFlag, y = tile, z / w = page id of the tile's first /
+// second page (-1: absent, or outside the pool).
 //
 // Requests are taken 32 at a time, lane l covering request b + l.  After a scan of their tile
 // counts every record is produced by one lane, 32 * PER records per round (PER per lane), which
-// finds the record's request by a binary search over the scanned counts; each round issues all
-// its block-table reads before writing, so a list of up to 32 * PER tiles costs one memory round
-// trip.  (PER = 1 where the kernel's register budget is tight.)
+// finds the record's request by a binary search over the scanned counts.  A round first places
+// all its records, then issues all their block-table reads, then writes: a list of up to
+// 32 * PER tiles costs one memory round trip.  (PER = 1 where the kernel's register budget is
+// tight.)  Everything is passed by value, so that nothing of the caller's lives in local memory.
 template <int PER>
-__device__ __noinline__ int build_list(ListCursor &cur, int batch, const int *s_len, int4 *s_list,
-                                       const LogitsArgs &a, int lane) {
+__device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const int *s_len,
+                                              int4 *s_list, const int32_t *block_tables,
+                                              int64_t bt_stride, int64_t num_blocks, int lane) {
   int n = 0;
   int b = cur.b, j = cur.j;
   while (n < kMaxList && b < batch && (b < cur.b_end || (b == cur.b_end && j < cur.j_end))) {
@@ -229,6 +239,7 @@ __device__ __noinline__ int build_list(ListCursor &cur, int batch, const int *s_
     for (int c0 = 0; c0 < take; c0 += 32 * PER) {
       int rx[PER], rj[PER], p0[PER], p1[PER];
       bool has1[PER];
+      const int32_t *row[PER];
 #pragma unroll
       for (int h = 0; h < PER; ++h) {
         const int idx = c0 + 32 * h + lane;
@@ -241,7 +252,9 @@ __device__ __noinline__ int build_list(ListCursor &cur, int batch, const int *s_
         const int c_s = __shfl_sync(0xffffffffu, cnt, src);
         const int j_s = __shfl_sync(0xffffffffu, jlo, src);
         rx[h] = -1;
+        rj[h] = 0;
         has1[h] = false;
+        row[h] = block_tables;
         if (idx < take) {
           const int req = b + src;
           const int tile = j_s + (idx - e_s);
@@ -251,19 +264,22 @@ __device__ __noinline__ int build_list(ListCursor &cur, int batch, const int *s_
           rj[h] = tile;
           const int len = s_len[req];
           const int npages = len / kBlock + (len % kBlock != 0 ? 1 : 0);
-          const int32_t *row = a.block_tables + static_cast<int64_t>(req) * a.bt_stride;
+          row[h] = block_tables + static_cast<int64_t>(req) * bt_stride;
           has1[h] = 2 * tile + 1 < npages;
-          p0[h] = __ldg(row + 2 * tile);
-          p1[h] = has1[h] ? __ldg(row + 2 * tile + 1) : -1;
         }
+      }
+#pragma unroll
+      for (int h = 0; h < PER; ++h) {
+        p0[h] = rx[h] >= 0 ? __ldg(row[h] + 2 * rj[h]) : -1;
+        p1[h] = has1[h] ? __ldg(row[h] + 2 * rj[h] + 1) : -1;
       }
 #pragma unroll
       for (int h = 0; h < PER; ++h) {
         if (rx[h] >= 0) {
           int q0 = p0[h], q1 = p1[h];
-          bool bad = q0 < 0 || q0 >= a.num_blocks;
+          bool bad = q0 < 0 || q0 >= num_blocks;
           if (bad) q0 = -1;
-          if (has1[h] && (q1 < 0 || q1 >= a.num_blocks)) {
+          if (has1[h] && (q1 < 0 || q1 >= num_blocks)) {
             bad = true;
             q1 = -1;
           }
@@ -290,7 +306,7 @@ __device__ __noinline__ int build_list(ListCursor &cur, int batch, const int *s_
   if (n > 0) cur.prev_b = s_list[n - 1].x & 0xFFFF;
   cur.b = b;
   cur.j = j;
-  return n;
+  return ListResult{cur, n};
 }
 
 template <int NN>
@@ -363,8 +379,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
         f0 = total * cb / g;
         f1 = total * (cb + 1) / g;
       }
-      s0 = warp_locate(f0, total, lo, hi, excl, mine, s_len, batch);
-      s1 = warp_locate(f1, total, lo, hi, excl, mine, s_len, batch);
+      warp_locate2(f0, f1, total, lo, hi, excl, mine, s_len, batch, s0, s1);
     }
     __syncwarp();
     // Start at the first tile that exists (a stale schedule or empty requests may point past it).
@@ -408,8 +423,11 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
 
   for (;;) {
     if (warp == 0) {
-      const int n = build_list<NN <= 2 ? 2 : 1>(cursor, batch, s_len, s_list, a, lane);
-      if (lane == 0) *s_count = n;
+      const ListResult lr = build_list<NN <= 2 ? 2 : 1>(cursor, batch, s_len, s_list,
+                                                         a.block_tables, a.bt_stride,
+                                                         a.num_blocks, lane);
+      cursor = lr.cur;
+      if (lane == 0) *s_count = lr.n;
     }
     tc_fence_before_sync();
     __syncthreads();
