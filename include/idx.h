@@ -110,7 +110,9 @@ int idx_schedule(const int32_t *seq_lens, int64_t seq_lens_stride, int32_t batch
  *   block_tables    device int32; request b's j-th block id at block_tables[b*bt_row_stride+j];
  *                   only j < ceil(seq_lens[b]/block_size) is ever read
  *   bt_row_stride   >= bt_width (a row-strided view like block_tables[::next_n] is fine)
- *   bt_width        columns per row, >= ceil(max(seq_lens)/block_size) (caller's contract)
+ *   bt_width        columns per row, >= ceil(max(seq_lens)/block_size) (caller's contract); the
+ *                   first bt_width entries of every row must be mapped memory: the kernel may
+ *                   prefetch them into L2 (it reads only the live ones)
  *   seq_lens        device int32, seq_lens[b * seq_lens_stride], each 0 .. max_seq_len
  *   batch           0 .. 4096
  *   next_n          1 .. 4 (draft depth; slot t = next_n - 1 is the newest and sees the whole

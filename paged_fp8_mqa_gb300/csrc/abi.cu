@@ -222,6 +222,7 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
   a.weights = weights;
   a.block_tables = block_tables;
   a.bt_stride = bt_row_stride;
+  a.bt_width = bt_width;
   a.seq_lens = seq_lens;
   a.sl_stride = seq_lens_stride;
   a.schedule = schedule;

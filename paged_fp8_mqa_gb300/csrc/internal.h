@@ -38,6 +38,7 @@ struct LogitsArgs {
   const float *weights;         // [batch*next_n, 64]
   const int32_t *block_tables;  // row b at block_tables + b * bt_stride
   int64_t bt_stride;
+  int64_t bt_width;             // columns per row the caller provides (only the live ones are read)
   const int32_t *seq_lens;      // element b at seq_lens[b * sl_stride]
   int64_t sl_stride;
   const int32_t *schedule;      // nullable: [num_ctas + 1][2]

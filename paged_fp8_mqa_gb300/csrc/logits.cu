@@ -331,13 +331,33 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   int *s_count = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);  // current list length
   int *s_len = reinterpret_cast<int *>(smem + C::OFF_LEN);
 
-  // The previous kernel in the stream may still be running: no global memory before this.
-  griddep_wait();
-  griddep_launch_dependents();
-
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+
+  // The previous kernel in the stream may still be running: nothing is read before griddep_wait.
+  // L2 prefetches read nothing (L2 is where that kernel's writes land, so later loads still see
+  // them): seq_lens and this CTA's share of the block table start their way from DRAM while the
+  // previous kernel drains.  Block-table lines hold at least one byte of a row's declared width.
+  if (warp == 0) {
+    if (a.sl_stride == 1) {
+      for (int l = lane; l * 32 < a.batch; l += 32) prefetch_l2(a.seq_lens + l * 32);
+    } else {
+      for (int b = lane; b < a.batch; b += 32) prefetch_l2(a.seq_lens + b * a.sl_stride);
+    }
+  } else if (warp == kEpiWarpBase && a.bt_width > 0 &&
+             static_cast<int64_t>(a.batch) * a.bt_width <= (int64_t{1} << 21)) {
+    for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
+      const int32_t *row = a.block_tables + static_cast<int64_t>(b) * a.bt_stride;
+      const uintptr_t first = reinterpret_cast<uintptr_t>(row) & ~uintptr_t{127};
+      const uintptr_t last = reinterpret_cast<uintptr_t>(row + a.bt_width - 1) & ~uintptr_t{127};
+      for (uintptr_t line = first + 128u * lane; line <= last; line += 128u * 32u)
+        prefetch_l2(reinterpret_cast<const void *>(line));
+    }
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+
   const int batch = a.batch;
   ListCursor cursor{};
 
