@@ -13,11 +13,15 @@
 // order-preserving uint32 keys (i.e. IEEE totalOrder) finds the row's K'-th largest key v,
 // K' = min(row_end, top_k), and the row's keys above v become candidates and its lowest-index
 // keys equal to v ties, K' items in all.  It then rewrites counters, the threshold (v) and
-// ranges, and returns arrivals[r] to zero.  The repair reads the row twice: an 11-bit histogram
-// of the leading key bits finds the bin holding v; a second sweep stores the keys of higher bins
-// as candidates and gathers the bin's own keys into shared memory, where the remaining 21 bits
-// are resolved.  A bin too large for that buffer falls back to four 8-bit passes over the row
-// and a final in-order sweep.
+// ranges, and returns arrivals[r] to zero.  The repair first needs a key lo <= v: 0 if the whole
+// row fits a 6144-key shared-memory buffer, else the row's threshold if the classification
+// counted between K' and 6144 keys at or above it, else a bound read off a sample of 2048 of
+// the row's keys with a safety margin.  One sweep gathers every key >= lo into the buffer (one
+// shared atomic per warp and 32 keys), where three histogram passes (11, 11, 10 bits) find v
+// and the output is written.  If fewer than K' or more than 6144 keys are >= lo, it falls back
+// to two sweeps (an 11-bit histogram of the row finds the bin holding v; a second sweep stores
+// the keys of higher bins as candidates and gathers the bin into the buffer), and if that bin is
+// too large, to four 8-bit passes over the row and a final in-order sweep.
 
 #include <cuda_runtime.h>
 
@@ -42,6 +46,7 @@ constexpr int kBufKeys = 6144;                  // keys of the bin holding v, ke
 constexpr int kTieRank = 2048;                  // ties ranked in shared memory (ordered case)
 constexpr uint32_t kSelectSmem = 2048 * 4 + kBufKeys * 8;  // dynamic: histogram + (key, index)
 constexpr int kPassLoads = 8;                   // float4 loads in flight per thread, histogram
+constexpr int kSamples = 2048;                  // keys sampled to bound the K'-th from below
 constexpr int kSweepKeys = 16;                  // contiguous keys per thread, final sweep
 constexpr int kRepairSpan = kThreads * kSweepKeys;
 
@@ -137,6 +142,238 @@ __device__ __forceinline__ void find_bin(const unsigned *h, int nbins, unsigned 
   __syncthreads();
 }
 
+// Finishes a repair from the shared-memory buffer of nb (key, index) pairs.  The buffer holds
+// every key of the row that is >= v (the K-th largest), except the `*s_cand` keys already stored
+// as candidates, which all lie above the buffer's keys.  need = K - *s_cand.  With b1 >= 0 every
+// buffered key has leading 11 bits b1; with b1 < 0 the buffer may span any bins.  Writes the
+// buffered keys above v as candidates and the ties (all of them, or the m lowest indices).
+// Returns false, having written nothing, if more than kTieRank tied keys would need ranking.
+__device__ bool finish_from_buffer(const uint32_t *s_bkey, const int *s_bidx, int nb, int b1_in,
+                                   unsigned need, int K, int top_k, int2 *slots, int *s_cand,
+                                   unsigned *s_h, int *cand_out, int *tie_out, float *thr_out) {
+  __shared__ int s_bin, s_ntie;
+  __shared__ unsigned s_above;
+  __shared__ int s_warp[kWarps];
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_bin = 0;
+    s_above = 0;
+    s_ntie = 0;
+  }
+  uint32_t b1 = static_cast<uint32_t>(b1_in);
+  if (b1_in < 0) {  // the leading 11 bits
+    for (int i = tid; i < 2048; i += kThreads) s_h[i] = 0;
+    __syncthreads();
+    for (int j = tid; j < nb; j += kThreads) atomicAdd(&s_h[s_bkey[j] >> 21], 1u);
+    __syncthreads();
+    find_bin(s_h, 2048, need, &s_bin, &s_above, s_warp);
+    b1 = static_cast<uint32_t>(s_bin);
+    need -= s_above;
+  }
+  // The next 11 bits among the keys of bin b1, then the last 10.
+  for (int i = tid; i < 2048; i += kThreads) s_h[i] = 0;
+  __syncthreads();
+  for (int j = tid; j < nb; j += kThreads)
+    if ((s_bkey[j] >> 21) == b1) atomicAdd(&s_h[(s_bkey[j] >> 10) & 2047u], 1u);
+  __syncthreads();
+  find_bin(s_h, 2048, need, &s_bin, &s_above, s_warp);
+  const uint32_t p2 = (b1 << 11) | static_cast<uint32_t>(s_bin);
+  const unsigned need2 = need - s_above;
+  for (int i = tid; i < 1024; i += kThreads) s_h[i] = 0;
+  __syncthreads();
+  for (int j = tid; j < nb; j += kThreads)
+    if ((s_bkey[j] >> 10) == p2) atomicAdd(&s_h[s_bkey[j] & 1023u], 1u);
+  __syncthreads();
+  find_bin(s_h, 1024, need2, &s_bin, &s_above, s_warp);
+  const uint32_t vkey = (p2 << 10) | static_cast<uint32_t>(s_bin);
+  const int m = static_cast<int>(need2 - s_above);  // keys equal to v that are kept
+  const int ties = static_cast<int>(s_h[s_bin]);    // keys equal to v in the row
+  const int c = K - m;                              // keys above v
+  if (ties > m && ties > kTieRank) return false;
+  // ---- write the buffered keys above v, and the ties (all, or the m lowest indices)
+  int *s_tidx = reinterpret_cast<int *>(s_h);  // tie indices when they must be ranked
+  __syncthreads();
+  const int lane = tid & 31;
+  for (int j0 = 0; j0 < nb; j0 += kThreads) {  // slots reserved with one atomic per warp
+    const int j = j0 + tid;
+    const uint32_t key = j < nb ? s_bkey[j] : 0u;
+    const bool is_c = j < nb && key > vkey;
+    const bool is_t = j < nb && key == vkey;
+    const unsigned mc = __ballot_sync(0xffffffffu, is_c);
+    if (mc) {
+      const int leader = __ffs(mc) - 1;
+      int n = 0;
+      if (lane == leader) n = atomicAdd(s_cand, __popc(mc));
+      n = __shfl_sync(0xffffffffu, n, leader) + __popc(mc & lanemask_lt());
+      if (is_c) slots[top_k + n] = make_int2(s_bidx[j], __float_as_int(key_value(key)));
+    }
+    const unsigned mt = __ballot_sync(0xffffffffu, is_t);
+    if (mt) {
+      const int leader = __ffs(mt) - 1;
+      int n = 0;
+      if (lane == leader) n = atomicAdd(&s_ntie, __popc(mt));
+      n = __shfl_sync(0xffffffffu, n, leader) + __popc(mt & lanemask_lt());
+      if (is_t) {
+        if (ties == m)
+          slots[top_k - 1 - n] = make_int2(s_bidx[j], __float_as_int(key_value(vkey)));
+        else
+          s_tidx[n] = s_bidx[j];
+      }
+    }
+  }
+  __syncthreads();
+  if (ties > m) {
+    // Keep the m lowest indices: a tie's rank is the number of ties with a smaller index.
+    for (int j = tid; j < ties; j += kThreads) {
+      const int mine = s_tidx[j];
+      int rank = 0;
+      for (int q = 0; q < ties; ++q) rank += s_tidx[q] < mine ? 1 : 0;
+      if (rank < m) slots[top_k - 1 - rank] = make_int2(mine, __float_as_int(key_value(vkey)));
+    }
+  }
+  if (tid == 0) {
+    *cand_out = c;
+    *tie_out = m;
+    *thr_out = key_value(vkey);
+  }
+  return true;
+}
+
+// kPassLoads float4 loads of the row per thread, all in flight before any is used (the row is
+// L2-resident; one load at a time would leave a sweep bound by the L2 latency).  Keys past
+// row_end read as 0.0f and must be masked by the caller.
+__device__ __forceinline__ void load_pass(const float *row, int row_end, int base,
+                                          float4 (&v)[kPassLoads]) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int u = 0; u < kPassLoads; ++u) {
+    const int i = base + (u * kThreads + tid) * 4;
+    if (i + 3 < row_end) {
+      v[u] = __ldg(reinterpret_cast<const float4 *>(row + i));
+    } else {
+      v[u].x = i < row_end ? __ldg(row + i) : 0.0f;
+      v[u].y = i + 1 < row_end ? __ldg(row + i + 1) : 0.0f;
+      v[u].z = i + 2 < row_end ? __ldg(row + i + 2) : 0.0f;
+      v[u].w = 0.0f;
+    }
+  }
+}
+
+// One-sweep repair of a row (see the file comment): gathers every key >= lo into the buffer and
+// finishes there.  lo: 0 (every key) when the row fits the buffer; else `lo_hint` when the caller
+// has one (the row's threshold, when the classification counted between K and kBufKeys keys at
+// or above it); else the 22-bit prefix of the key of a sample of kSamples keys that ranks at 1.5
+// times the rank the K-th largest is expected at, plus 16 (found by two histogram passes).
+// Returns false, having written nothing, unless between K and kBufKeys keys are >= lo (and the
+// ties can be ranked).
+__device__ bool repair_row_gather(const float *row, int row_end, int K, int top_k, int2 *slots,
+                                  bool have_hint, uint32_t lo_hint, int *cand_out, int *tie_out,
+                                  float *thr_out, uint8_t *dyn) {
+  unsigned *s_h = reinterpret_cast<unsigned *>(dyn);                // [2048]: samples, histogram
+  uint32_t *s_bkey = reinterpret_cast<uint32_t *>(dyn + 2048 * 4);  // [kBufKeys]
+  int *s_bidx = reinterpret_cast<int *>(s_bkey + kBufKeys);         // [kBufKeys]
+  __shared__ int s_nbuf, s_cand;
+  const int tid = threadIdx.x;
+  if (K > kBufKeys) return false;
+  uint32_t lo = 0;
+  if (row_end > kBufKeys) {
+    if (have_hint) {
+      lo = lo_hint;
+    } else {
+      // kSamples keys evenly spread over the row; two histogram passes (leading 11 bits, then
+      // the next 11 within the bin) find the sample of the wanted rank, whose 22-bit prefix is lo.
+      __shared__ int s_sbin;
+      __shared__ unsigned s_sabove;
+      __shared__ int s_swarp[kWarps];
+      uint32_t smp[kSamples / kThreads];
+#pragma unroll
+      for (int q = 0; q < kSamples / kThreads; ++q)
+        smp[q] = order_key(
+            __ldg(row + static_cast<int64_t>(q * kThreads + tid) * row_end / kSamples));
+      const int64_t want =
+          static_cast<int64_t>(K) * kSamples * 3 / (2 * static_cast<int64_t>(row_end));
+      const unsigned rank = static_cast<unsigned>(min(static_cast<int64_t>(kSamples), want + 17));
+      for (int i = tid; i < 2048; i += kThreads) s_h[i] = 0;
+      if (tid == 0) {
+        s_sbin = 0;
+        s_sabove = 0;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < kSamples / kThreads; ++q) atomicAdd(&s_h[smp[q] >> 21], 1u);
+      __syncthreads();
+      find_bin(s_h, 2048, rank, &s_sbin, &s_sabove, s_swarp);
+      const uint32_t sb1 = static_cast<uint32_t>(s_sbin);
+      const unsigned rank2 = rank - s_sabove;
+      for (int i = tid; i < 2048; i += kThreads) s_h[i] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < kSamples / kThreads; ++q)
+        if ((smp[q] >> 21) == sb1) atomicAdd(&s_h[(smp[q] >> 10) & 2047u], 1u);
+      __syncthreads();
+      find_bin(s_h, 2048, rank2, &s_sbin, &s_sabove, s_swarp);
+      lo = (sb1 << 21) | (static_cast<uint32_t>(s_sbin) << 10);
+      __syncthreads();
+    }
+  }
+  if (tid == 0) {
+    s_nbuf = 0;
+    s_cand = 0;
+  }
+  __syncthreads();
+  const int lane = tid & 31;
+  for (int base = 0; base < row_end; base += kThreads * 4 * kPassLoads) {
+    float4 v[kPassLoads];
+    load_pass(row, row_end, base, v);
+    // This thread's keys >= lo as a bit mask; then one warp scan and one shared atomic per warp
+    // place them in the buffer, each lane storing only its own (few) keys, re-read from L1.
+    uint32_t take = 0;
+    if (base + kThreads * 4 * kPassLoads <= row_end) {
+#pragma unroll
+      for (int u = 0; u < kPassLoads; ++u) {
+        take |= (order_key(v[u].x) >= lo ? 1u : 0u) << (4 * u);
+        take |= (order_key(v[u].y) >= lo ? 1u : 0u) << (4 * u + 1);
+        take |= (order_key(v[u].z) >= lo ? 1u : 0u) << (4 * u + 2);
+        take |= (order_key(v[u].w) >= lo ? 1u : 0u) << (4 * u + 3);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kPassLoads; ++u) {
+        const int i = base + (u * kThreads + tid) * 4;
+        const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (i + k < row_end && order_key(e[k]) >= lo) take |= 1u << (4 * u + k);
+      }
+    }
+    const int cnt = __popc(take);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int n = 0;
+    if (lane == 31 && incl > 0) n = atomicAdd(&s_nbuf, incl);
+    n = __shfl_sync(0xffffffffu, n, 31) + incl - cnt;
+    while (take) {
+      const int bit = __ffs(take) - 1;
+      take &= take - 1;
+      const int i = base + ((bit >> 2) * kThreads + tid) * 4 + (bit & 3);
+      if (n < kBufKeys) {
+        s_bkey[n] = order_key(__ldg(row + i));
+        s_bidx[n] = i;
+      }
+      ++n;
+    }
+  }
+  __syncthreads();
+  const int nb = s_nbuf;
+  if (nb < K || nb > kBufKeys) return false;
+  return finish_from_buffer(s_bkey, s_bidx, nb, -1, static_cast<unsigned>(K), K, top_k, slots,
+                            &s_cand, s_h, cand_out, tie_out, thr_out);
+}
+
 // Two-sweep repair of a row (see the file comment); false if the bin holding v has more keys than
 // the buffer, or more tied keys than can be ranked, in which case nothing it wrote is counted and
 // the caller falls back to repair_row.
@@ -145,7 +382,7 @@ __device__ bool repair_row_fast(const float *row, int row_end, int K, int top_k,
   unsigned *s_h = reinterpret_cast<unsigned *>(dyn);                // [2048]
   uint32_t *s_bkey = reinterpret_cast<uint32_t *>(dyn + 2048 * 4);  // [kBufKeys]
   int *s_bidx = reinterpret_cast<int *>(s_bkey + kBufKeys);         // [kBufKeys]
-  __shared__ int s_bin, s_nbuf, s_cand, s_ntie;
+  __shared__ int s_bin, s_nbuf, s_cand;
   __shared__ unsigned s_above;
   __shared__ int s_warp[kWarps];
   const int tid = threadIdx.x;
@@ -153,7 +390,6 @@ __device__ bool repair_row_fast(const float *row, int row_end, int K, int top_k,
   if (tid == 0) {
     s_nbuf = 0;
     s_cand = 0;
-    s_ntie = 0;
     s_bin = 0;
     s_above = 0;
   }
@@ -161,18 +397,7 @@ __device__ bool repair_row_fast(const float *row, int row_end, int K, int top_k,
   // ---- sweep 1: histogram of the leading 11 key bits
   for (int base = 0; base < row_end; base += kThreads * 4 * kPassLoads) {
     float4 v[kPassLoads];
-#pragma unroll
-    for (int u = 0; u < kPassLoads; ++u) {
-      const int i = base + (u * kThreads + tid) * 4;
-      if (i + 3 < row_end) {
-        v[u] = __ldg(reinterpret_cast<const float4 *>(row + i));
-      } else {
-        v[u].x = i < row_end ? __ldg(row + i) : 0.0f;
-        v[u].y = i + 1 < row_end ? __ldg(row + i + 1) : 0.0f;
-        v[u].z = i + 2 < row_end ? __ldg(row + i + 2) : 0.0f;
-        v[u].w = 0.0f;
-      }
-    }
+    load_pass(row, row_end, base, v);
 #pragma unroll
     for (int u = 0; u < kPassLoads; ++u) {
       const int i = base + (u * kThreads + tid) * 4;
@@ -191,18 +416,7 @@ __device__ bool repair_row_fast(const float *row, int row_end, int K, int top_k,
   // ---- sweep 2: keys of higher bins are candidates; the bin's own keys go to the buffer
   for (int base = 0; base < row_end; base += kThreads * 4 * kPassLoads) {
     float4 v[kPassLoads];
-#pragma unroll
-    for (int u = 0; u < kPassLoads; ++u) {
-      const int i = base + (u * kThreads + tid) * 4;
-      if (i + 3 < row_end) {
-        v[u] = __ldg(reinterpret_cast<const float4 *>(row + i));
-      } else {
-        v[u].x = i < row_end ? __ldg(row + i) : 0.0f;
-        v[u].y = i + 1 < row_end ? __ldg(row + i + 1) : 0.0f;
-        v[u].z = i + 2 < row_end ? __ldg(row + i + 2) : 0.0f;
-        v[u].w = 0.0f;
-      }
-    }
+    load_pass(row, row_end, base, v);
 #pragma unroll
     for (int u = 0; u < kPassLoads; ++u) {
       const int i = base + (u * kThreads + tid) * 4;
@@ -224,58 +438,9 @@ __device__ bool repair_row_fast(const float *row, int row_end, int K, int top_k,
     }
   }
   __syncthreads();
-  // ---- the remaining 21 bits among the buffered keys: 11 bits, then 10
-  const unsigned need1 = static_cast<unsigned>(K) - above1;  // 1 <= need1 <= nb
-  for (int i = tid; i < 2048; i += kThreads) s_h[i] = 0;
-  __syncthreads();
-  for (int j = tid; j < nb; j += kThreads) atomicAdd(&s_h[(s_bkey[j] >> 10) & 2047u], 1u);
-  __syncthreads();
-  find_bin(s_h, 2048, need1, &s_bin, &s_above, s_warp);
-  const uint32_t b2 = static_cast<uint32_t>(s_bin);
-  const unsigned need2 = need1 - s_above;
-  for (int i = tid; i < 1024; i += kThreads) s_h[i] = 0;
-  __syncthreads();
-  for (int j = tid; j < nb; j += kThreads)
-    if (((s_bkey[j] >> 10) & 2047u) == b2) atomicAdd(&s_h[s_bkey[j] & 1023u], 1u);
-  __syncthreads();
-  find_bin(s_h, 1024, need2, &s_bin, &s_above, s_warp);
-  const uint32_t vkey = (b1 << 21) | (b2 << 10) | static_cast<uint32_t>(s_bin);
-  const int m = static_cast<int>(need2 - s_above);  // keys equal to v that are kept
-  const int ties = static_cast<int>(s_h[s_bin]);    // keys equal to v in the row
-  const int c = K - m;                              // keys above v
-  if (ties > m && ties > kTieRank) return false;
-  // ---- write the buffered keys above v, and the ties (all, or the m lowest indices)
-  int *s_tidx = reinterpret_cast<int *>(s_h);  // tie indices when they must be ranked
-  __syncthreads();
-  for (int j = tid; j < nb; j += kThreads) {
-    const uint32_t key = s_bkey[j];
-    if (key > vkey) {
-      const int n = atomicAdd(&s_cand, 1);
-      slots[top_k + n] = make_int2(s_bidx[j], __float_as_int(key_value(key)));
-    } else if (key == vkey) {
-      const int n = atomicAdd(&s_ntie, 1);
-      if (ties == m)
-        slots[top_k - 1 - n] = make_int2(s_bidx[j], __float_as_int(key_value(vkey)));
-      else
-        s_tidx[n] = s_bidx[j];
-    }
-  }
-  __syncthreads();
-  if (ties > m) {
-    // Keep the m lowest indices: a tie's rank is the number of ties with a smaller index.
-    for (int j = tid; j < ties; j += kThreads) {
-      const int mine = s_tidx[j];
-      int rank = 0;
-      for (int q = 0; q < ties; ++q) rank += s_tidx[q] < mine ? 1 : 0;
-      if (rank < m) slots[top_k - 1 - rank] = make_int2(mine, __float_as_int(key_value(vkey)));
-    }
-  }
-  if (tid == 0) {
-    *cand_out = c;
-    *tie_out = m;
-    *thr_out = key_value(vkey);
-  }
-  return true;
+  return finish_from_buffer(s_bkey, s_bidx, nb, static_cast<int>(b1),
+                            static_cast<unsigned>(K) - above1, K, top_k, slots, &s_cand, s_h,
+                            cand_out, tie_out, thr_out);
 }
 
 // Repairs row `r` (called by every thread of the row's last CTA): see the file comment.
@@ -441,7 +606,7 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
     for (int u = 0; u < kSweepLoads; ++u) {
       const int i = begin + (u * kThreads + tid) * 4;
       if (i + 3 < end) {
-        v[u] = __ldcs(reinterpret_cast<const float4 *>(row + i));
+        v[u] = __ldg(reinterpret_cast<const float4 *>(row + i));
       } else {
         v[u].x = i < end ? row[i] : 0.0f;
         v[u].y = i + 1 < end ? row[i + 1] : 0.0f;
@@ -490,9 +655,16 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
   } else {
     __shared__ int s_c, s_m;
     __shared__ float s_v;
-    if (!repair_row_fast(row, row_end, K, a.top_k, slots, &s_c, &s_m, &s_v, select_smem)) {
+    // The threshold bounds the K'-th key from below when at least K' and at most a buffer's worth
+    // of keys were counted at or above it (NaN thresholds excepted).
+    const bool hint = thr == thr && s_nc + s_nt >= K && s_nc + s_nt <= kBufKeys;
+    if (!repair_row_gather(row, row_end, K, a.top_k, slots, hint, order_key(thr), &s_c, &s_m, &s_v,
+                           select_smem)) {
       __syncthreads();
-      repair_row(row, row_end, K, a.top_k, slots, &s_c, &s_m, &s_v);
+      if (!repair_row_fast(row, row_end, K, a.top_k, slots, &s_c, &s_m, &s_v, select_smem)) {
+        __syncthreads();
+        repair_row(row, row_end, K, a.top_k, slots, &s_c, &s_m, &s_v);
+      }
     }
     __syncthreads();
     if (tid == 0) {
