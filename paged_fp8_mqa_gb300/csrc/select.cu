@@ -145,7 +145,8 @@ __device__ __forceinline__ void find_bin(const unsigned *h, int nbins, unsigned 
 // Finishes a repair from the shared-memory buffer of nb (key, index) pairs.  The buffer holds
 // every key of the row that is >= v (the K-th largest), except the `*s_cand` keys already stored
 // as candidates, which all lie above the buffer's keys.  need = K - *s_cand.  With b1 >= 0 every
-// buffered key has leading 11 bits b1; with b1 < 0 the buffer may span any bins.  Writes the
+// buffered key has leading 11 bits b1; with b1 < 0 the buffer may span any bins (b1 == -2: the
+// histogram of their leading 11 bits is already in s_h).  Writes the
 // buffered keys above v as candidates and the ties (all of them, or the m lowest indices).
 // Returns false, having written nothing, if more than kTieRank tied keys would need ranking.
 __device__ bool finish_from_buffer(const uint32_t *s_bkey, const int *s_bidx, int nb, int b1_in,
@@ -161,10 +162,12 @@ __device__ bool finish_from_buffer(const uint32_t *s_bkey, const int *s_bidx, in
     s_ntie = 0;
   }
   uint32_t b1 = static_cast<uint32_t>(b1_in);
-  if (b1_in < 0) {  // the leading 11 bits
-    for (int i = tid; i < 2048; i += kThreads) s_h[i] = 0;
-    __syncthreads();
-    for (int j = tid; j < nb; j += kThreads) atomicAdd(&s_h[s_bkey[j] >> 21], 1u);
+  if (b1_in < 0) {  // the leading 11 bits (b1_in == -2: their histogram is already in s_h)
+    if (b1_in == -1) {
+      for (int i = tid; i < 2048; i += kThreads) s_h[i] = 0;
+      __syncthreads();
+      for (int j = tid; j < nb; j += kThreads) atomicAdd(&s_h[s_bkey[j] >> 21], 1u);
+    }
     __syncthreads();
     find_bin(s_h, 2048, need, &s_bin, &s_above, s_warp);
     b1 = static_cast<uint32_t>(s_bin);
@@ -316,6 +319,7 @@ __device__ bool repair_row_gather(const float *row, int row_end, int K, int top_
       __syncthreads();
     }
   }
+  for (int i = tid; i < 2048; i += kThreads) s_h[i] = 0;  // the taken keys' leading 11 bits
   if (tid == 0) {
     s_nbuf = 0;
     s_cand = 0;
@@ -360,8 +364,10 @@ __device__ bool repair_row_gather(const float *row, int row_end, int K, int top_
       const int bit = __ffs(take) - 1;
       take &= take - 1;
       const int i = base + ((bit >> 2) * kThreads + tid) * 4 + (bit & 3);
+      const uint32_t key = order_key(__ldg(row + i));
+      atomicAdd(&s_h[key >> 21], 1u);
       if (n < kBufKeys) {
-        s_bkey[n] = order_key(__ldg(row + i));
+        s_bkey[n] = key;
         s_bidx[n] = i;
       }
       ++n;
@@ -370,7 +376,7 @@ __device__ bool repair_row_gather(const float *row, int row_end, int K, int top_
   __syncthreads();
   const int nb = s_nbuf;
   if (nb < K || nb > kBufKeys) return false;
-  return finish_from_buffer(s_bkey, s_bidx, nb, -1, static_cast<unsigned>(K), K, top_k, slots,
+  return finish_from_buffer(s_bkey, s_bidx, nb, -2, static_cast<unsigned>(K), K, top_k, slots,
                             &s_cand, s_h, cand_out, tie_out, thr_out);
 }
 
