@@ -38,6 +38,10 @@ extern "C" {
 #define IDX_CUDA 3        /* a CUDA runtime/driver call or launch failed */
 #define IDX_CONTRACT 4    /* IDX_VALIDATE=1 found a violated content precondition */
 
+/* Element types of idx_logits_fp8's output (the pages' output_dtype). */
+#define IDX_DTYPE_F32 0 /* float32 (the default on the pages) */
+#define IDX_DTYPE_F16 1 /* IEEE binary16 */
+
 /* Device-side status bits (idx_device_status). */
 #define IDX_DEV_WAIT_TIMEOUT 1 /* a pipeline wait gave up after its time limit */
 #define IDX_DEV_BAD_PAGE 2     /* a needed block-table entry was outside [0, num_blocks) */
@@ -122,8 +126,13 @@ int idx_schedule(const int32_t *seq_lens, int64_t seq_lens_stride, int32_t batch
  *   schedule        device int32 [num_sms+1][2] from idx_schedule with the same seq_lens and
  *                   num_sms, or NULL to derive the split inside the kernel (recommended)
  *   num_sms         CTAs of the persistent grid (0 = this device's SM count)
- *   out             device float32, rows of out_row_stride floats, 16-byte aligned
- *   out_row_stride  >= idx_padded_seq_len(max_seq_len) and a multiple of 4
+ *   output_dtype    IDX_DTYPE_F32 or IDX_DTYPE_F16 (Parameters: output_dtype): the float32
+ *                   result is converted on store, to nearest even, so a float16 output holds
+ *                   +-inf where |logit| exceeds the half range; bfloat16 is not offered (as on
+ *                   the pages); anything else is IDX_UNSUPPORTED
+ *   out             device, output_dtype elements, rows of out_row_stride elements, 16-byte
+ *                   aligned
+ *   out_row_stride  >= idx_padded_seq_len(max_seq_len) and a multiple of 4 (elements)
  *   row_ends_out    NULL, or device int32 [batch*next_n] receiving
  *                   max(0, seq_lens[b] - next_n + t + 1) for every row (zero-length requests
  *                   included), ready for idx_threshold_select
@@ -133,8 +142,8 @@ int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t num_blocks
                    int64_t bt_row_stride, int32_t bt_width, const int32_t *seq_lens,
                    int64_t seq_lens_stride, int32_t batch, int32_t next_n, int32_t num_heads,
                    int32_t head_dim, int32_t max_seq_len, const int32_t *schedule,
-                   int32_t num_sms, float *out, int64_t out_row_stride, int32_t *row_ends_out,
-                   void *stream);
+                   int32_t num_sms, int32_t output_dtype, void *out, int64_t out_row_stride,
+                   int32_t *row_ends_out, void *stream);
 
 /*
  * idx_threshold_select ("flashinfer.sdsa.indexer_threshold_select": description; Parameters

@@ -22,6 +22,8 @@ IDX_INVALID_ARG = 1
 IDX_UNSUPPORTED = 2
 IDX_CUDA = 3
 IDX_CONTRACT = 4
+IDX_DTYPE_F32 = 0
+IDX_DTYPE_F16 = 1
 IDX_DEV_WAIT_TIMEOUT = 1
 IDX_DEV_BAD_PAGE = 2
 
@@ -63,7 +65,7 @@ def lib() -> ctypes.CDLL:
     L.idx_logits_fp8.restype = c.c_int
     L.idx_logits_fp8.argtypes = [P, P, c.c_int64, c.c_int32, P, P, c.c_int64, c.c_int32, P,
                                  c.c_int64, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
-                                 c.c_int32, P, c.c_int32, P, c.c_int64, P, P]
+                                 c.c_int32, P, c.c_int32, c.c_int32, P, c.c_int64, P, P]
     L.idx_threshold_select.restype = c.c_int
     L.idx_threshold_select.argtypes = [P, c.c_int64, P, c.c_int32, P, P, P, c.c_int32,
                                        c.c_int32, c.c_int32, P, P, P]
@@ -104,12 +106,12 @@ def idx_schedule(seq_lens, seq_lens_stride, batch, next_n, num_sms, schedule, st
 
 def idx_logits_fp8(q, kv_fused, num_blocks, block_size, weights, block_tables, bt_row_stride,
                    bt_width, seq_lens, seq_lens_stride, batch, next_n, num_heads, head_dim,
-                   max_seq_len, schedule, num_sms, out, out_row_stride, row_ends_out,
-                   stream) -> int:
+                   max_seq_len, schedule, num_sms, output_dtype, out, out_row_stride,
+                   row_ends_out, stream) -> int:
     return lib().idx_logits_fp8(q, kv_fused, num_blocks, block_size, weights, block_tables,
                                 bt_row_stride, bt_width, seq_lens, seq_lens_stride, batch, next_n,
-                                num_heads, head_dim, max_seq_len, schedule, num_sms, out,
-                                out_row_stride, row_ends_out, stream)
+                                num_heads, head_dim, max_seq_len, schedule, num_sms,
+                                output_dtype, out, out_row_stride, row_ends_out, stream)
 
 
 def idx_threshold_select(logits, logits_row_stride, row_ends, rows, thresholds, counters,
@@ -181,11 +183,13 @@ def schedule(seq_lens, next_n: int = 1, num_sms: int = 0, out=None, stream=None)
 
 
 def logits_fp8(q, kv_fused, weights, block_tables, seq_lens, max_seq_len: int, *, out=None,
-               schedule_meta=None, num_sms: int = 0, row_ends_out=None, stream=None):
+               schedule_meta=None, num_sms: int = 0, row_ends_out=None, stream=None,
+               output_dtype=None):
     """Paged FP8 MQA logits.  q: e4m3 (or its uint8 view) [B, next_n, 64, 128]; kv_fused: uint8
     whose leading dim is the block count and whose per-block bytes are 64*(128+4); weights:
     float32 [B*next_n, 64]; block_tables: int32 [B, W] with unit column stride; seq_lens: int32
-    [B] (any stride).  Returns the [B*next_n, max_seq_len] view of the padded output."""
+    [B] (any stride).  output_dtype: torch.float32 (default) or torch.float16; an `out` buffer
+    fixes it.  Returns the [B*next_n, max_seq_len] view of the padded output."""
     import torch
     _need(q, (torch.float8_e4m3fn, torch.uint8), "q", 4)
     _need(kv_fused, torch.uint8, "kv_fused")
@@ -200,15 +204,18 @@ def logits_fp8(q, kv_fused, weights, block_tables, seq_lens, max_seq_len: int, *
     num_blocks = kv_fused.shape[0]
     block_size = kv_fused.numel() // num_blocks // (D + 4) if num_blocks else 0
     if out is None:
-        out = torch.empty(B * n, idx_padded_seq_len(max_seq_len), dtype=torch.float32,
-                          device=q.device)
-    _need(out, torch.float32, "out", 2)
+        out = torch.empty(B * n, idx_padded_seq_len(max_seq_len),
+                          dtype=output_dtype or torch.float32, device=q.device)
+    elif output_dtype is not None and out.dtype != output_dtype:
+        raise ValueError(f"out is {out.dtype} but output_dtype is {output_dtype}")
+    _need(out, (torch.float32, torch.float16), "out", 2)
+    dtype_code = IDX_DTYPE_F16 if out.dtype == torch.float16 else IDX_DTYPE_F32
     if out.stride(1) != 1:
         raise ValueError("out rows must be contiguous")
     _check(idx_logits_fp8(_ptr(q), _ptr(kv_fused), num_blocks, block_size, _ptr(weights),
                           _ptr(block_tables), block_tables.stride(0), block_tables.shape[1],
                           _ptr(seq_lens), seq_lens.stride(0), B, n, H, D, max_seq_len,
-                          _ptr(schedule_meta), num_sms, _ptr(out), out.stride(0),
+                          _ptr(schedule_meta), num_sms, dtype_code, _ptr(out), out.stride(0),
                           _ptr(row_ends_out), _stream(stream)))
     return out[:B * n, :max_seq_len]
 

@@ -174,8 +174,8 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
                               int32_t bt_width, const int32_t *seq_lens, int64_t seq_lens_stride,
                               int32_t batch, int32_t next_n, int32_t num_heads, int32_t head_dim,
                               int32_t max_seq_len, const int32_t *schedule, int32_t num_sms,
-                              float *out, int64_t out_row_stride, int32_t *row_ends_out,
-                              void *stream) {
+                              int32_t output_dtype, void *out, int64_t out_row_stride,
+                              int32_t *row_ends_out, void *stream) {
   g_error.clear();
   if (q == nullptr || kv_fused == nullptr || weights == nullptr || block_tables == nullptr ||
       seq_lens == nullptr || out == nullptr)
@@ -187,6 +187,8 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
   if (num_heads != 64 || head_dim != 128 || block_size != 64)
     return fail(IDX_UNSUPPORTED, "this build supports num_heads 64, head_dim 128, block_size 64");
   if (next_n > 4) return fail(IDX_UNSUPPORTED, "next_n must be 1..4");
+  if (output_dtype != IDX_DTYPE_F32 && output_dtype != IDX_DTYPE_F16)
+    return fail(IDX_UNSUPPORTED, "output_dtype must be IDX_DTYPE_F32 or IDX_DTYPE_F16");
   if (batch > idx::kMaxBatch) return fail(IDX_UNSUPPORTED, "batch above 4096");
   if (out_row_stride < idx_padded_seq_len(max_seq_len) || out_row_stride % 4 != 0)
     return fail(IDX_INVALID_ARG,
@@ -231,7 +233,8 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
   a.row_ends = row_ends_out;
   a.num_blocks = num_blocks;
   a.batch = batch;
-  const cudaError_t e = idx::launch_logits_fp8(next_n, kv_map, q_map, a, ctas, s);
+  const cudaError_t e = idx::launch_logits_fp8(next_n, output_dtype == IDX_DTYPE_F16, kv_map,
+                                               q_map, a, ctas, s);
   if (e != cudaSuccess) return cuda_fail(e, "logits launch");
   return IDX_OK;
 }

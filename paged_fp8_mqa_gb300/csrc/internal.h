@@ -42,16 +42,17 @@ struct LogitsArgs {
   const int32_t *seq_lens;      // element b at seq_lens[b * sl_stride]
   int64_t sl_stride;
   const int32_t *schedule;      // nullable: [num_ctas + 1][2]
-  float *out;                   // row r at out + r * out_stride
+  void *out;                    // float or __half elements; row r at out + r * out_stride
   int64_t out_stride;
   int32_t *row_ends;            // nullable: [batch * next_n]
   int64_t num_blocks;
   int32_t batch;
 };
 
-// Launches the logits kernel for draft depth `next_n` (1..4) on `num_ctas` CTAs.
-cudaError_t launch_logits_fp8(int next_n, const CUtensorMap &kv_map, const CUtensorMap &q_map,
-                              const LogitsArgs &args, int num_ctas, cudaStream_t stream);
+// Launches the logits kernel for draft depth `next_n` (1..4), float16 output if `out_f16`.
+cudaError_t launch_logits_fp8(int next_n, bool out_f16, const CUtensorMap &kv_map,
+                              const CUtensorMap &q_map, const LogitsArgs &args, int num_ctas,
+                              cudaStream_t stream);
 
 // Launches the standalone schedule kernel.
 cudaError_t launch_schedule(const int32_t *seq_lens, int64_t stride, int batch, int num_ctas,

@@ -39,6 +39,7 @@
 // lists.
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -108,6 +109,10 @@ struct Cfg {
 };
 
 __device__ __forceinline__ void flag_error(int bits) { atomicOr(&g_logits_status, bits); }
+
+// The output element: float32, or float16 rounded to nearest even (the pages' output_dtype).
+__device__ __forceinline__ void store_out(float *p, float v) { *p = v; }
+__device__ __forceinline__ void store_out(__half *p, float v) { *p = __float2half_rn(v); }
 
 // relu(s) * 2^-25 on the FMA pipe: a saturating multiply clamps to [0, 1] (NaN to 0), and
 // every score satisfies |s| <= 128 * 448^2 < 2^25, so the product is exact.
@@ -180,8 +185,10 @@ __device__ __forceinline__ void warp_locate2(long long f0, long long f1, long lo
   const unsigned who0 = __ballot_sync(0xffffffffu, here0);
   const unsigned who1 = __ballot_sync(0xffffffffu, here1);
   const int src0 = who0 ? __ffs(who0) - 1 : 0, src1 = who1 ? __ffs(who1) - 1 : 0;
-  const int2 r0 = make_int2(__shfl_sync(0xffffffffu, at0.x, src0), __shfl_sync(0xffffffffu, at0.y, src0));
-  const int2 r1 = make_int2(__shfl_sync(0xffffffffu, at1.x, src1), __shfl_sync(0xffffffffu, at1.y, src1));
+  const int2 r0 = make_int2(__shfl_sync(0xffffffffu, at0.x, src0),
+                            __shfl_sync(0xffffffffu, at0.y, src0));
+  const int2 r1 = make_int2(__shfl_sync(0xffffffffu, at1.x, src1),
+                            __shfl_sync(0xffffffffu, at1.y, src1));
   if (who0) at0 = r0;
   if (who1) at1 = r1;
 }
@@ -309,7 +316,7 @@ __device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const i
   return ListResult{cur, n};
 }
 
-template <int NN>
+template <int NN, typename OutT>
 __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
     k_logits_fp8(const __grid_constant__ CUtensorMap kv_map,
                  const __grid_constant__ CUtensorMap q_map, const LogitsArgs a) {
@@ -604,7 +611,8 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
             const float scale = have ? s_scale[(k % C::SCALE_SLOTS) * kTileTokens + pos] : 0.0f;
             const int p = r.y * kTileTokens + pos;
             const bool store = p < s_len[b];
-            float *dst = a.out + static_cast<int64_t>(b * NN) * a.out_stride + p;
+            OutT *dst =
+                static_cast<OutT *>(a.out) + static_cast<int64_t>(b * NN) * a.out_stride + p;
             const uint32_t col0 = static_cast<uint32_t>((k % C::ACC) * C::N);
             const int nslots = min(C::SLOTS, NN - t_first);
             // The quadrant's two 16-lane windows hold positions (g, g + 8) and (g + 16, g + 24).
@@ -650,7 +658,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
               }
               float logit = scale * quad_reduce_scatter(p01.x, p01.y, p23.x, p23.y, c);
               if constexpr (C::SPLIT == 2) asm volatile("" : "+f"(logit));  // before the next load
-              if (store) dst[static_cast<int64_t>(t) * a.out_stride] = logit;
+              if (store) store_out(dst + static_cast<int64_t>(t) * a.out_stride, logit);
             }
           }
           if (r.x & kLastFlag) {
@@ -697,34 +705,42 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
-template <int NN>
+template <int NN, typename OutT>
 cudaError_t launch_nn(const CUtensorMap &kv_map, const CUtensorMap &q_map, const LogitsArgs &args,
                       int num_ctas, cudaStream_t stream) {
   using C = Cfg<NN>;
   const uint32_t smem = C::smem_bytes(args.batch);
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_logits_fp8<NN>,
+    cudaError_t e = cudaFuncSetAttribute(k_logits_fp8<NN, OutT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::smem_bytes(kMaxBatch));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_dependent(k_logits_fp8<NN>, dim3(num_ctas), dim3(C::THREADS), smem, stream, kv_map,
-                          q_map, args);
+  return launch_dependent(k_logits_fp8<NN, OutT>, dim3(num_ctas), dim3(C::THREADS), smem, stream,
+                          kv_map, q_map, args);
+}
+
+template <typename OutT>
+cudaError_t launch_out(int next_n, const CUtensorMap &kv_map, const CUtensorMap &q_map,
+                       const LogitsArgs &args, int num_ctas, cudaStream_t stream) {
+  switch (next_n) {
+    case 1: return launch_nn<1, OutT>(kv_map, q_map, args, num_ctas, stream);
+    case 2: return launch_nn<2, OutT>(kv_map, q_map, args, num_ctas, stream);
+    case 3: return launch_nn<3, OutT>(kv_map, q_map, args, num_ctas, stream);
+    case 4: return launch_nn<4, OutT>(kv_map, q_map, args, num_ctas, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_logits_fp8(int next_n, const CUtensorMap &kv_map, const CUtensorMap &q_map,
-                              const LogitsArgs &args, int num_ctas, cudaStream_t stream) {
-  switch (next_n) {
-    case 1: return launch_nn<1>(kv_map, q_map, args, num_ctas, stream);
-    case 2: return launch_nn<2>(kv_map, q_map, args, num_ctas, stream);
-    case 3: return launch_nn<3>(kv_map, q_map, args, num_ctas, stream);
-    case 4: return launch_nn<4>(kv_map, q_map, args, num_ctas, stream);
-    default: return cudaErrorInvalidValue;
-  }
+cudaError_t launch_logits_fp8(int next_n, bool out_f16, const CUtensorMap &kv_map,
+                              const CUtensorMap &q_map, const LogitsArgs &args, int num_ctas,
+                              cudaStream_t stream) {
+  return out_f16 ? launch_out<__half>(next_n, kv_map, q_map, args, num_ctas, stream)
+                 : launch_out<float>(next_n, kv_map, q_map, args, num_ctas, stream);
 }
 
 cudaError_t logits_status(int32_t *value, bool clear) {

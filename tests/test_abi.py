@@ -54,8 +54,8 @@ def _logits_args(**over):
     a = dict(q=FAKE, kv_fused=FAKE, num_blocks=10, block_size=64, weights=FAKE,
              block_tables=FAKE, bt_row_stride=16, bt_width=16, seq_lens=FAKE,
              seq_lens_stride=1, batch=2, next_n=1, num_heads=64, head_dim=128, max_seq_len=1024,
-             schedule=None, num_sms=4, out=FAKE, out_row_stride=1024, row_ends_out=None,
-             stream=None)
+             schedule=None, num_sms=4, output_dtype=idx.IDX_DTYPE_F32, out=FAKE,
+             out_row_stride=1024, row_ends_out=None, stream=None)
     a.update(over)
     return a
 
@@ -73,6 +73,8 @@ def _logits_args(**over):
     (dict(head_dim=64), idx.IDX_UNSUPPORTED),
     (dict(block_size=32), idx.IDX_UNSUPPORTED),
     (dict(next_n=5), idx.IDX_UNSUPPORTED),
+    (dict(output_dtype=2), idx.IDX_UNSUPPORTED),
+    (dict(output_dtype=-1), idx.IDX_UNSUPPORTED),
     (dict(batch=5000), idx.IDX_UNSUPPORTED),
     (dict(num_blocks=1 << 26), idx.IDX_INVALID_ARG),
 ])
@@ -107,3 +109,14 @@ def test_schedule_rejects_bad_arguments(lib):
     assert idx.idx_schedule(FAKE, 0, 4, 1, 8, FAKE, None) == idx.IDX_INVALID_ARG
     assert idx.idx_schedule(FAKE, 1, 4, 9, 8, FAKE, None) == idx.IDX_UNSUPPORTED
     assert idx.idx_schedule(FAKE, 1, 4, 1, 2000, FAKE, None) == idx.IDX_INVALID_ARG
+
+
+def test_binding_constants_match_the_header():
+    import re
+    from pathlib import Path
+    text = (Path(__file__).resolve().parents[1] / "include" / "idx.h").read_text()
+    defs = dict(re.findall(r"#define (IDX_\w+) (-?\d+)", text))
+    assert {"IDX_DTYPE_F32", "IDX_DTYPE_F16", "IDX_OK", "IDX_UNSUPPORTED"} <= defs.keys()
+    for name, value in defs.items():
+        if hasattr(idx, name):
+            assert getattr(idx, name) == int(value), name

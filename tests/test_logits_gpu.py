@@ -137,3 +137,63 @@ def test_stale_schedule_terminates():
     got = out.cpu().double().numpy()
     m = ~np.isnan(got) & ~np.isnan(ref)
     assert (np.abs(got[m] - ref[m]) <= 2e-6 * tol[m] + 1e-7).all()
+
+
+def _check_float16(w, out, ref, tol):
+    """float16 output ("flashinfer.attn_scores", Parameters: output_dtype): the float32 result
+    (within the float32 tolerance of the oracle) rounded to nearest even, so within that
+    tolerance plus half a binary16 ulp of the value; values past the half range are +-inf (where
+    the oracle's value is clear of the rounding boundary 65520 by more than the tolerance)."""
+    got = out.cpu().double().numpy()
+    re = w.row_ends().numpy()
+    lim32 = 2e-6 * tol + 1e-7
+    for r in range(w.rows):
+        L, e = int(w.seq_lens[r // w.next_n]), int(re[r])
+        g, x, l32 = got[r, :e], ref[r, :e], lim32[r, :e]
+        over = np.abs(x) - l32 >= 65520.0
+        under = np.abs(x) + l32 < 65520.0
+        assert (np.isinf(g[over]) & (np.sign(g[over]) == np.sign(x[over]))).all(), f"row {r}"
+        a = np.abs(x[under]) + l32[under]
+        half_ulp = 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -14))) - 11)
+        err = np.abs(g[under] - x[under])
+        assert (err <= l32[under] + half_ulp).all(), f"row {r}: max err {err.max()}"
+        assert np.isnan(got[r, L:]).all(), f"row {r}: columns >= seq_len were written"
+
+
+@pytest.mark.parametrize("next_n", [1, 2, 3, 4])
+def test_float16_output(next_n):
+    w = _small(310 + next_n, next_n, [1, 63, 64, 65, 300, 1000, 0, 4097], max_seq_len=4097)
+    ref, tol = _oracle(w)
+    t = to_device(w)
+    pad = idx.idx_padded_seq_len(w.max_seq_len)
+    out = torch.full((w.rows, pad), float("nan"), dtype=torch.float16, device="cuda")
+    got = idx.logits_fp8(t["q"], t["kv"], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len,
+                         out=out)
+    torch.cuda.synchronize()
+    assert got.dtype == torch.float16 and got.data_ptr() == out.data_ptr()
+    _check_float16(w, out, ref, tol)
+
+
+def test_float16_output_overflows_to_inf():
+    """Weights scaled so that many logits leave the binary16 range."""
+    w = _small(320, 2, [500, 130, 2000], max_seq_len=2000)
+    w.weights.mul_(3000.0)
+    ref, tol = _oracle(w)
+    assert (np.abs(np.nan_to_num(ref)) > 70000).any()
+    t = to_device(w)
+    out = torch.full((w.rows, idx.idx_padded_seq_len(w.max_seq_len)), float("nan"),
+                     dtype=torch.float16, device="cuda")
+    idx.logits_fp8(t["q"], t["kv"], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len, out=out)
+    torch.cuda.synchronize()
+    _check_float16(w, out, ref, tol)
+
+
+def test_output_dtype_keyword_allocates():
+    w = _small(321, 1, [200, 5])
+    t = to_device(w)
+    got = idx.logits_fp8(t["q"], t["kv"], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len,
+                         output_dtype=torch.float16)
+    assert got.dtype == torch.float16 and got.shape == (w.rows, w.max_seq_len)
+    with pytest.raises(ValueError):
+        idx.logits_fp8(t["q"], t["kv"], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len,
+                       out=torch.empty(w.rows, 256, device="cuda"), output_dtype=torch.float16)
