@@ -109,7 +109,6 @@ int idx_schedule(const int32_t *seq_lens, int64_t seq_lens_stride, int32_t batch
  *                   block_size*head_dim + 4*i)
  *   num_blocks      blocks in the pool (>= 1; num_blocks * (block_size*(head_dim+4)/128) must
  *                   stay below 2^31)
- *   block_size      tokens per block
  *   weights         device float32 [batch*next_n, num_heads], contiguous, 16-byte aligned
  *   block_tables    device int32; request b's j-th block id at block_tables[b*bt_row_stride+j];
  *                   only j < ceil(seq_lens[b]/block_size) is ever read
@@ -121,7 +120,8 @@ int idx_schedule(const int32_t *seq_lens, int64_t seq_lens_stride, int32_t batch
  *   batch           0 .. 4096
  *   next_n          1 .. 4 (draft depth; slot t = next_n - 1 is the newest and sees the whole
  *                   sequence)
- *   num_heads, head_dim, block_size   this build supports 64, 128, 64 (IDX_UNSUPPORTED else)
+ *   num_heads, head_dim   this build supports 64 and 128 (IDX_UNSUPPORTED else)
+ *   block_size      32, 64 or 128 tokens per block (IDX_UNSUPPORTED else)
  *   max_seq_len     >= every seq_lens[b]
  *   schedule        device int32 [num_sms+1][2] from idx_schedule with the same seq_lens and
  *                   num_sms, or NULL to derive the split inside the kernel (recommended)

@@ -94,7 +94,8 @@ bool validate_requested() {
 // IDX_VALIDATE=1: the content preconditions of the logits call, checked on host copies.
 int validate_logits_contents(const int32_t *block_tables, int64_t bt_row_stride, int32_t bt_width,
                              const int32_t *seq_lens, int64_t seq_lens_stride, int32_t batch,
-                             int32_t max_seq_len, int64_t num_blocks, cudaStream_t stream) {
+                             int32_t max_seq_len, int64_t num_blocks, int32_t block_size,
+                             cudaStream_t stream) {
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   cudaError_t e = cudaStreamIsCapturing(stream, &cap);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
@@ -115,10 +116,11 @@ int validate_logits_contents(const int32_t *block_tables, int64_t bt_row_stride,
     if (len < 0 || len > max_seq_len)
       return fail(IDX_CONTRACT, "seq_lens[" + std::to_string(b) + "] = " + std::to_string(len) +
                                     " is outside [0, max_seq_len]");
-    const int64_t pages = (len + 63) / 64;
+    const int64_t pages = (len + block_size - 1) / block_size;
     if (pages > bt_width)
       return fail(IDX_CONTRACT, "block table width " + std::to_string(bt_width) +
-                                    " < ceil(seq_lens[" + std::to_string(b) + "] / 64)");
+                                    " < ceil(seq_lens[" + std::to_string(b) + "] / " +
+                                    std::to_string(block_size) + ")");
     for (int64_t j = 0; j < pages; ++j) {
       const int32_t id = table[static_cast<size_t>(b) * bt_width + j];
       if (id < 0 || id >= num_blocks)
@@ -184,8 +186,10 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
       bt_row_stride < bt_width || block_size <= 0 || num_heads <= 0 || head_dim <= 0 ||
       next_n <= 0)
     return fail(IDX_INVALID_ARG, "negative or inconsistent size or stride");
-  if (num_heads != 64 || head_dim != 128 || block_size != 64)
-    return fail(IDX_UNSUPPORTED, "this build supports num_heads 64, head_dim 128, block_size 64");
+  if (num_heads != 64 || head_dim != 128 ||
+      (block_size != 32 && block_size != 64 && block_size != 128))
+    return fail(IDX_UNSUPPORTED,
+                "this build supports num_heads 64, head_dim 128, block_size 32, 64 or 128");
   if (next_n > 4) return fail(IDX_UNSUPPORTED, "next_n must be 1..4");
   if (output_dtype != IDX_DTYPE_F32 && output_dtype != IDX_DTYPE_F16)
     return fail(IDX_UNSUPPORTED, "output_dtype must be IDX_DTYPE_F32 or IDX_DTYPE_F16");
@@ -209,12 +213,12 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (validate_requested()) {
     st = validate_logits_contents(block_tables, bt_row_stride, bt_width, seq_lens,
-                                  seq_lens_stride, batch, max_seq_len, num_blocks, s);
+                                  seq_lens_stride, batch, max_seq_len, num_blocks, block_size, s);
     if (st != IDX_OK) return st;
   }
   CUtensorMap kv_map, q_map;
   st = encode_rows128(&kv_map, kv_fused, static_cast<uint64_t>(num_blocks) * (page_bytes / 128),
-                      128, 64);
+                      128, static_cast<uint32_t>(block_size));
   if (st != IDX_OK) return st;
   st = encode_rows128(&q_map, q, static_cast<uint64_t>(batch) * next_n * num_heads, 128,
                       static_cast<uint32_t>(next_n * num_heads));
@@ -232,6 +236,7 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
   a.out_stride = out_row_stride;
   a.row_ends = row_ends_out;
   a.num_blocks = num_blocks;
+  a.block_size = block_size;
   a.batch = batch;
   const cudaError_t e = idx::launch_logits_fp8(next_n, output_dtype == IDX_DTYPE_F16, kv_map,
                                                q_map, a, ctas, s);

@@ -47,6 +47,7 @@ struct LogitsArgs {
   int32_t *row_ends;            // nullable: [batch * next_n]
   int64_t num_blocks;
   int32_t batch;
+  int32_t block_size;           // tokens per page: 32, 64 or 128
 };
 
 // Launches the logits kernel for draft depth `next_n` (1..4), float16 output if `out_f16`.

@@ -43,6 +43,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "../../include/idx.h"
 #include "internal.h"
@@ -58,15 +59,11 @@ namespace {
 constexpr int kEpiWarpBase = 2;                  // epilogue warps 2, 3, ...
 constexpr int kHeads = 64;
 constexpr int kHeadDim = 128;
-constexpr int kBlock = 64;                        // tokens per page
-constexpr int kPageBytes = kBlock * (kHeadDim + 4);  // 8448
-constexpr int kPageRows = kPageBytes / 128;       // 66 rows of 128 bytes per page
-constexpr int kValueBytes = kBlock * kHeadDim;    // 8192
-constexpr uint32_t kStageBytes = kTileTokens * kHeadDim;  // 16384: two pages of values
+constexpr uint32_t kStageBytes = kTileTokens * kHeadDim;  // 16384: a tile's values
 constexpr int kMaxList = 256;                     // tiles per tile list
-constexpr int kScaleBytes = kBlock * 4;          // 256: a page's float32 scales
-constexpr int kFirstFlag = 1 << 16;               // record.x = request | flags
+constexpr int kFirstFlag = 1 << 16;               // record.x = request | flags | page mask
 constexpr int kLastFlag = 1 << 17;
+constexpr int kMaskShift = 18;                    // bit 18 + p: the tile's page p is present
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
 
 template <int NN>
@@ -94,7 +91,8 @@ struct Cfg {
   static constexpr int SCALE_SLOTS = STAGES + ACC;
   static constexpr uint32_t OFF_SCALE = OFF_W + 2 * W_FLOATS * 4;
   static constexpr uint32_t OFF_LIST = OFF_SCALE + SCALE_SLOTS * kTileTokens * 4;
-  static constexpr uint32_t OFF_BAR = OFF_LIST + kMaxList * 16;
+  static constexpr uint32_t OFF_PG2 = OFF_LIST + kMaxList * 16;  // pages 2, 3 (32-token pages)
+  static constexpr uint32_t OFF_BAR = OFF_PG2 + kMaxList * 8;
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t OFF_LEN = OFF_MISC + 64;
@@ -206,9 +204,10 @@ struct ListResult {
   int n;
 };
 
-// Writes the next list (at most kMaxList tiles) into s_list; called by all 32 lanes of one warp.
-// Record: x = request | kFirstFlag | kLastFlag, y = tile, z / w = page id of the tile's first /
-// second page (-1: absent, or outside the pool).
+// Writes the next list (at most kMaxList tiles) into s_list (and s_pg2); called by all 32 lanes of
+// one warp.  A tile of 128 positions spans 1 << PPT_SHIFT pages.  Record: x = request |
+// kFirstFlag | kLastFlag | (mask of the tile's present pages) << kMaskShift, y = tile, z / w =
+// page id of the tile's page 0 / 1, s_pg2 = pages 2 / 3 (-1: absent, or outside the pool).
 //
 // Requests are taken 32 at a time, lane l covering request b + l.  After a scan of their tile
 // counts every record is produced by one lane, 32 * PER records per round (PER per lane), which
@@ -216,10 +215,13 @@ struct ListResult {
 // all its records, then issues all their block-table reads, then writes: a list of up to
 // 32 * PER tiles costs one memory round trip.  (PER = 1 where the kernel's register budget is
 // tight.)  Everything is passed by value, so that nothing of the caller's lives in local memory.
-template <int PER>
+template <int PER, int PPT_SHIFT>
 __device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const int *s_len,
-                                              int4 *s_list, const int32_t *block_tables,
-                                              int64_t bt_stride, int64_t num_blocks, int lane) {
+                                              int4 *s_list, int2 *s_pg2,
+                                              const int32_t *block_tables, int64_t bt_stride,
+                                              int64_t num_blocks, int lane) {
+  constexpr int PPT = 1 << PPT_SHIFT;  // pages per tile: 1, 2 or 4
+  constexpr int BS_SHIFT = 7 - PPT_SHIFT;
   int n = 0;
   int b = cur.b, j = cur.j;
   while (n < kMaxList && b < batch && (b < cur.b_end || (b == cur.b_end && j < cur.j_end))) {
@@ -244,8 +246,7 @@ __device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const i
     const int room = kMaxList - n;
     const int take = min(total, room);
     for (int c0 = 0; c0 < take; c0 += 32 * PER) {
-      int rx[PER], rj[PER], p0[PER], p1[PER];
-      bool has1[PER];
+      int rx[PER], rj[PER], npg[PER], id[PER][PPT];
       const int32_t *row[PER];
 #pragma unroll
       for (int h = 0; h < PER; ++h) {
@@ -260,7 +261,7 @@ __device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const i
         const int j_s = __shfl_sync(0xffffffffu, jlo, src);
         rx[h] = -1;
         rj[h] = 0;
-        has1[h] = false;
+        npg[h] = 0;
         row[h] = block_tables;
         if (idx < take) {
           const int req = b + src;
@@ -270,28 +271,36 @@ __device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const i
           rx[h] = req | (first ? kFirstFlag : 0) | (last ? kLastFlag : 0);
           rj[h] = tile;
           const int len = s_len[req];
-          const int npages = len / kBlock + (len % kBlock != 0 ? 1 : 0);
-          row[h] = block_tables + static_cast<int64_t>(req) * bt_stride;
-          has1[h] = 2 * tile + 1 < npages;
+          const int npages = (len + (1 << BS_SHIFT) - 1) >> BS_SHIFT;
+          const int first_page = tile << PPT_SHIFT;
+          row[h] = block_tables + static_cast<int64_t>(req) * bt_stride + first_page;
+          npg[h] = min(npages - first_page, PPT);  // the tile's pages, >= 1
         }
       }
 #pragma unroll
-      for (int h = 0; h < PER; ++h) {
-        p0[h] = rx[h] >= 0 ? __ldg(row[h] + 2 * rj[h]) : -1;
-        p1[h] = has1[h] ? __ldg(row[h] + 2 * rj[h] + 1) : -1;
-      }
+      for (int h = 0; h < PER; ++h)
+#pragma unroll
+        for (int pg = 0; pg < PPT; ++pg) id[h][pg] = pg < npg[h] ? __ldg(row[h] + pg) : -1;
 #pragma unroll
       for (int h = 0; h < PER; ++h) {
         if (rx[h] >= 0) {
-          int q0 = p0[h], q1 = p1[h];
-          bool bad = q0 < 0 || q0 >= num_blocks;
-          if (bad) q0 = -1;
-          if (has1[h] && (q1 < 0 || q1 >= num_blocks)) {
-            bad = true;
-            q1 = -1;
+          int mask = 0;
+          bool bad = false;
+#pragma unroll
+          for (int pg = 0; pg < PPT; ++pg) {
+            if (pg >= npg[h]) continue;
+            if (id[h][pg] < 0 || id[h][pg] >= num_blocks) {
+              bad = true;
+              id[h][pg] = -1;
+            } else {
+              mask |= 1 << pg;
+            }
           }
           if (bad) flag_error(IDX_DEV_BAD_PAGE);
-          s_list[n + c0 + 32 * h + lane] = make_int4(rx[h], rj[h], q0, q1);
+          const int k = n + c0 + 32 * h + lane;
+          s_list[k] = make_int4(rx[h] | (mask << kMaskShift), rj[h], id[h][0],
+                                PPT >= 2 ? id[h][PPT >= 2 ? 1 : 0] : -1);
+          if constexpr (PPT == 4) s_pg2[k] = make_int2(id[h][2], id[h][3]);
         }
       }
     }
@@ -316,7 +325,7 @@ __device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const i
   return ListResult{cur, n};
 }
 
-template <int NN, typename OutT>
+template <int NN, typename OutT, int BS_SHIFT>
 __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
     k_logits_fp8(const __grid_constant__ CUtensorMap kv_map,
                  const __grid_constant__ CUtensorMap q_map, const LogitsArgs a) {
@@ -329,6 +338,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   float *s_w = reinterpret_cast<float *>(smem + C::OFF_W);
   float *s_scale = reinterpret_cast<float *>(smem + C::OFF_SCALE);
   int4 *s_list = reinterpret_cast<int4 *>(smem + C::OFF_LIST);
+  int2 *s_pg2 = reinterpret_cast<int2 *>(smem + C::OFF_PG2);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *done = full + C::STAGES;
   uint64_t *q_full = done + C::STAGES;
@@ -366,6 +376,9 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   griddep_launch_dependents();
 
   const int batch = a.batch;
+  // Pages of 1 << BS_SHIFT = 32, 64 or 128 tokens: that many 128-byte value rows, then that
+  // many float32 scales.
+  constexpr int bs_shift = BS_SHIFT;
   ListCursor cursor{};
 
   // ---- 1. set-up: warp 0 finds the CTA's tile run, warp 1 prepares barriers and TMEM --------
@@ -450,9 +463,10 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
 
   for (;;) {
     if (warp == 0) {
-      const ListResult lr = build_list<NN <= 2 ? 2 : 1>(cursor, batch, s_len, s_list,
-                                                         a.block_tables, a.bt_stride,
-                                                         a.num_blocks, lane);
+      constexpr int PER = NN <= 2 ? 2 : 1;
+      const ListResult lr = build_list<PER, 7 - BS_SHIFT>(cursor, batch, s_len, s_list, s_pg2,
+                                                           a.block_tables, a.bt_stride,
+                                                           a.num_blocks, lane);
       cursor = lr.cur;
       if (lane == 0) *s_count = lr.n;
     }
@@ -465,52 +479,64 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
 
     if (warp == 0) {
       // ============================== producer ================================================
+      // This thread's per-tile work sits on the pipeline's critical path, so its loop is
+      // specialised on the page size (one to four pages per tile) and keeps to constants.
       if (lane == 0 && ok) {
         const uint64_t pol_stream = l2_policy_evict_first();
         const uint64_t pol_keep = l2_policy_evict_last();
-        for (int i = 0; i < n; ++i) {
-          const int4 r = s_list[i];
-          if (!mbar_wait(&done[stage], phase ^ 1, kWaitLimitNs)) {
-            ok = false;
-            break;
-          }
-          const uint32_t pages = (r.z >= 0 ? 1u : 0u) + (r.w >= 0 ? 1u : 0u);
-          mbar_arrive_expect_tx(&full[stage], (kValueBytes + kScaleBytes) * pages);
-          // The first ACC tiles' accumulators were never read: stand in for their readers.
-          if (kbase + i < C::ACC) mbar_arrive_count(&full[stage], C::TEAM_WARPS);
-          uint8_t *dst = s_kv + stage * kStageBytes;
-          float *sdst = s_scale + ((kbase + i) % C::SCALE_SLOTS) * kTileTokens;
-          if (r.z >= 0) {
-            tma_load_2d(dst, &kv_map, &full[stage], 0, r.z * kPageRows, pol_stream);
-            bulk_load(sdst, a.kv + static_cast<int64_t>(r.z) * kPageBytes + kValueBytes,
-                      kScaleBytes, &full[stage], pol_stream);
-          }
-          if (r.w >= 0) {
-            tma_load_2d(dst + kValueBytes, &kv_map, &full[stage], 0, r.w * kPageRows,
-                        pol_stream);
-            bulk_load(sdst + kBlock, a.kv + static_cast<int64_t>(r.w) * kPageBytes + kValueBytes,
-                      kScaleBytes, &full[stage], pol_stream);
-          }
-          if (++stage == C::STAGES) {  // (before the q wait, so a timeout there still drains)
-            stage = 0;
-            phase ^= 1;
-          }
-          // A new request's q and w go out after its first KV tile, whose latency is longer.
-          if (r.x & kFirstFlag) {
-            const int b = r.x & 0xFFFF;
-            const int buf = qcount & 1;
-            if (!mbar_wait(&q_empty[buf], ((qcount >> 1) & 1) ^ 1, kWaitLimitNs)) {
+        const auto produce = [&](auto page_tokens) {
+          constexpr int BS = decltype(page_tokens)::value;
+          constexpr uint32_t kValue = BS * kHeadDim, kScale = BS * 4;
+          constexpr int64_t kPage = BS * (kHeadDim + 4);
+          constexpr int kRows = static_cast<int>(kPage / 128);
+          const auto page = [&](int pg, int id, uint8_t *dst, float *sdst) {
+            if (id < 0) return;
+            tma_load_2d(dst + pg * kValue, &kv_map, &full[stage], 0, id * kRows, pol_stream);
+            bulk_load(sdst + pg * BS, a.kv + static_cast<int64_t>(id) * kPage + kValue, kScale,
+                      &full[stage], pol_stream);
+          };
+          for (int i = 0; i < n; ++i) {
+            const int4 r = s_list[i];
+            const int2 hi = BS == 32 ? s_pg2[i] : make_int2(-1, -1);
+            if (!mbar_wait(&done[stage], phase ^ 1, kWaitLimitNs)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&q_full[buf], C::Q_BYTES + C::W_FLOATS * 4);
-            tma_load_2d(s_q + buf * C::Q_BYTES, &q_map, &q_full[buf], 0, b * C::N, pol_keep);
-            bulk_load(s_w + buf * C::W_FLOATS,
-                      a.weights + static_cast<int64_t>(b) * C::W_FLOATS, C::W_FLOATS * 4,
-                      &q_full[buf], pol_keep);
-            ++qcount;
+            const uint32_t pages = (r.z >= 0 ? 1u : 0u) + (r.w >= 0 ? 1u : 0u) +
+                                   (hi.x >= 0 ? 1u : 0u) + (hi.y >= 0 ? 1u : 0u);
+            mbar_arrive_expect_tx(&full[stage], (kValue + kScale) * pages);
+            // The first ACC tiles' accumulators were never read: stand in for their readers.
+            if (kbase + i < C::ACC) mbar_arrive_count(&full[stage], C::TEAM_WARPS);
+            uint8_t *dst = s_kv + stage * kStageBytes;
+            float *sdst = s_scale + ((kbase + i) % C::SCALE_SLOTS) * kTileTokens;
+            page(0, r.z, dst, sdst);
+            if (BS <= 64) page(1, r.w, dst, sdst);
+            if (BS == 32) {
+              page(2, hi.x, dst, sdst);
+              page(3, hi.y, dst, sdst);
+            }
+            if (++stage == C::STAGES) {  // (before the q wait, so a timeout there still drains)
+              stage = 0;
+              phase ^= 1;
+            }
+            // A new request's q and w go out after its first KV tile, whose latency is longer.
+            if (r.x & kFirstFlag) {
+              const int b = r.x & 0xFFFF;
+              const int buf = qcount & 1;
+              if (!mbar_wait(&q_empty[buf], ((qcount >> 1) & 1) ^ 1, kWaitLimitNs)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&q_full[buf], C::Q_BYTES + C::W_FLOATS * 4);
+              tma_load_2d(s_q + buf * C::Q_BYTES, &q_map, &q_full[buf], 0, b * C::N, pol_keep);
+              bulk_load(s_w + buf * C::W_FLOATS,
+                        a.weights + static_cast<int64_t>(b) * C::W_FLOATS, C::W_FLOATS * 4,
+                        &q_full[buf], pol_keep);
+              ++qcount;
+            }
           }
-        }
+        };
+        produce(std::integral_constant<int, 1 << BS_SHIFT>{});
       }
       __syncwarp();
     } else if (warp == 1) {
@@ -607,7 +633,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
               break;
             }
             tc_fence_after_sync();
-            const bool have = (pos < kBlock ? r.z : r.w) >= 0;
+            const bool have = (static_cast<uint32_t>(r.x) >> (kMaskShift + (pos >> bs_shift))) & 1u;
             const float scale = have ? s_scale[(k % C::SCALE_SLOTS) * kTileTokens + pos] : 0.0f;
             const int p = r.y * kTileTokens + pos;
             const bool store = p < s_len[b];
@@ -705,31 +731,42 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
-template <int NN, typename OutT>
+template <int NN, typename OutT, int BS_SHIFT>
 cudaError_t launch_nn(const CUtensorMap &kv_map, const CUtensorMap &q_map, const LogitsArgs &args,
                       int num_ctas, cudaStream_t stream) {
   using C = Cfg<NN>;
   const uint32_t smem = C::smem_bytes(args.batch);
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_logits_fp8<NN, OutT>,
+    cudaError_t e = cudaFuncSetAttribute(k_logits_fp8<NN, OutT, BS_SHIFT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::smem_bytes(kMaxBatch));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_dependent(k_logits_fp8<NN, OutT>, dim3(num_ctas), dim3(C::THREADS), smem, stream,
-                          kv_map, q_map, args);
+  return launch_dependent(k_logits_fp8<NN, OutT, BS_SHIFT>, dim3(num_ctas), dim3(C::THREADS), smem,
+                          stream, kv_map, q_map, args);
+}
+
+template <typename OutT, int BS_SHIFT>
+cudaError_t launch_bs(int next_n, const CUtensorMap &kv_map, const CUtensorMap &q_map,
+                      const LogitsArgs &args, int num_ctas, cudaStream_t stream) {
+  switch (next_n) {
+    case 1: return launch_nn<1, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
+    case 2: return launch_nn<2, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
+    case 3: return launch_nn<3, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
+    case 4: return launch_nn<4, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <typename OutT>
 cudaError_t launch_out(int next_n, const CUtensorMap &kv_map, const CUtensorMap &q_map,
                        const LogitsArgs &args, int num_ctas, cudaStream_t stream) {
-  switch (next_n) {
-    case 1: return launch_nn<1, OutT>(kv_map, q_map, args, num_ctas, stream);
-    case 2: return launch_nn<2, OutT>(kv_map, q_map, args, num_ctas, stream);
-    case 3: return launch_nn<3, OutT>(kv_map, q_map, args, num_ctas, stream);
-    case 4: return launch_nn<4, OutT>(kv_map, q_map, args, num_ctas, stream);
+  switch (args.block_size) {
+    case 32: return launch_bs<OutT, 5>(next_n, kv_map, q_map, args, num_ctas, stream);
+    case 64: return launch_bs<OutT, 6>(next_n, kv_map, q_map, args, num_ctas, stream);
+    case 128: return launch_bs<OutT, 7>(next_n, kv_map, q_map, args, num_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }

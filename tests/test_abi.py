@@ -71,7 +71,8 @@ def _logits_args(**over):
     (dict(num_sms=-3), idx.IDX_INVALID_ARG),
     (dict(num_heads=32), idx.IDX_UNSUPPORTED),
     (dict(head_dim=64), idx.IDX_UNSUPPORTED),
-    (dict(block_size=32), idx.IDX_UNSUPPORTED),
+    (dict(block_size=48), idx.IDX_UNSUPPORTED),
+    (dict(block_size=256), idx.IDX_UNSUPPORTED),
     (dict(next_n=5), idx.IDX_UNSUPPORTED),
     (dict(output_dtype=2), idx.IDX_UNSUPPORTED),
     (dict(output_dtype=-1), idx.IDX_UNSUPPORTED),

@@ -197,3 +197,43 @@ def test_output_dtype_keyword_allocates():
     with pytest.raises(ValueError):
         idx.logits_fp8(t["q"], t["kv"], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len,
                        out=torch.empty(w.rows, 256, device="cuda"), output_dtype=torch.float16)
+
+
+BLOCK_LENS = [1, 31, 32, 33, 63, 64, 65, 127, 128, 129, 300, 0, 2049]
+
+
+@pytest.mark.parametrize("block_size", [32, 128])
+@pytest.mark.parametrize("next_n", [1, 2, 3, 4])
+def test_block_sizes(block_size, next_n):
+    """Pages of 32 or 128 tokens ("flashinfer.attn_scores", Parameters: kv_fused, block_size):
+    a 128-position tile then spans four pages or one."""
+    w = _small(330 + next_n + block_size, next_n, BLOCK_LENS, max_seq_len=2049,
+               block_size=block_size)
+    ref, tol = _oracle(w)
+    got, row_ends = gpu_logits(w)
+    check_logits(w, got, ref, tol)
+    assert (row_ends.cpu() == w.row_ends()).all()
+
+
+@pytest.mark.parametrize("block_size", [32, 128])
+def test_block_sizes_ragged_and_poisoned(block_size):
+    """Many ragged requests with outlier keys; table entries past each request's pages hold an
+    out-of-pool id that must never be read."""
+    g = torch.Generator().manual_seed(block_size)
+    lens = torch.randint(0, 5000, (41,), generator=g).tolist()
+    w = _small(340 + block_size, 3, lens, max_seq_len=5000, block_size=block_size,
+               scale_range=(0.25, 4.0), outlier_frac=0.01, unused_entries="poison")
+    ref, tol = _oracle(w)
+    got, _ = gpu_logits(w)
+    check_logits(w, got, ref, tol)
+
+
+def test_block_size_32_float16_output():
+    w = _small(350, 4, [4000, 33, 1, 700], max_seq_len=4000, block_size=32)
+    ref, tol = _oracle(w)
+    t = to_device(w)
+    out = torch.full((w.rows, idx.idx_padded_seq_len(w.max_seq_len)), float("nan"),
+                     dtype=torch.float16, device="cuda")
+    idx.logits_fp8(t["q"], t["kv"], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len, out=out)
+    torch.cuda.synchronize()
+    _check_float16(w, out, ref, tol)
