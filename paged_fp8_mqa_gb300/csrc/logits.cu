@@ -5,12 +5,14 @@
 //
 // One persistent CTA per SM owns a contiguous run of 128-position KV tiles (split.cuh).  Warp 0
 // first turns the run into a tile list in shared memory, up to kMaxList tiles at a time:
-// {request | first/last-of-request flags, tile, page id of each of its two 64-token pages},
-// issuing the block-table reads of the whole list in parallel.  Every role then walks the list:
-//   warp 0     producer (one thread): per tile, TMA-loads the two pages' e4m3 values (8 KiB
-//              each, 128-byte swizzled) into a KV stage and bulk-copies their float32 scales
-//              (256 B each) into a scale slot; per request, TMA-loads q and bulk-copies w into
-//              one of two q/w buffers.
+// {request | first/last-of-request flags | present pages | request ordinal, tile, page ids of
+// its one to four pages (of 128, 64 or 32 tokens; the kernel is instantiated per page size)},
+// issuing the block-table reads of the whole list in parallel.  The producer and the MMA issuer
+// then walk the whole list, each epilogue team only its own tiles:
+//   warp 0     producer (one thread): per tile, TMA-loads the pages' e4m3 values (128-byte
+//              swizzled, 16 KiB per tile) into a KV stage and bulk-copies their float32 scales
+//              (512 B per tile) into a scale slot; per request, TMA-loads q and bulk-copies w
+//              into one of two q/w buffers.
 //   warp 1     MMA issuer (one thread): 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each),
 //              D[128 positions, n*64 query rows] += K_tile[128, 32] * q[n*64, 32]^T into a
 //              float32 TMEM accumulator, then one commit that marks the tile done.
@@ -64,6 +66,7 @@ constexpr int kMaxList = 256;                     // tiles per tile list
 constexpr int kFirstFlag = 1 << 16;               // record.x = request | flags | page mask
 constexpr int kLastFlag = 1 << 17;
 constexpr int kMaskShift = 18;                    // bit 18 + p: the tile's page p is present
+constexpr int kOrdShift = 22;                     // bits 22-29: the request's ordinal mod 256
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
 
 template <int NN>
@@ -72,8 +75,9 @@ struct Cfg {
   // with next_n >= 3 the two warps of a quadrant share a tile's draft slots, which gives each
   // scheduler four epilogue warps to hide the arithmetic's latency with.
   static constexpr int SPLIT = NN <= 2 ? 1 : 2;
+  static constexpr int TEAMS = 2;                       // teams taking tiles in turn
   static constexpr int TEAM_WARPS = 4 * SPLIT;          // warps reading one tile
-  static constexpr int EPI_WARPS = 2 * TEAM_WARPS;
+  static constexpr int EPI_WARPS = TEAMS * TEAM_WARPS;
   static constexpr int THREADS = (kEpiWarpBase + EPI_WARPS) * 32;
   static constexpr int SLOTS = (NN + SPLIT - 1) / SPLIT;  // draft slots per epilogue warp (max)
   static constexpr int N = NN * kHeads;  // MMA N: query rows of one request
@@ -196,6 +200,7 @@ struct ListCursor {
   int b, j;      // next tile to list
   int b_end, j_end;
   int prev_b;    // request of the last tile of the previous list (-1 before the first)
+  int ord;       // ordinal of that request in the run (requests with tiles count 1, 2, ...)
 };
 
 // The list builder's state after a list: where the next list starts, and this list's length.
@@ -208,6 +213,7 @@ struct ListResult {
 // one warp.  A tile of 128 positions spans 1 << PPT_SHIFT pages.  Record: x = request |
 // kFirstFlag | kLastFlag | (mask of the tile's present pages) << kMaskShift, y = tile, z / w =
 // page id of the tile's page 0 / 1, s_pg2 = pages 2 / 3 (-1: absent, or outside the pool).
+// x also carries the request's ordinal in the CTA's run (mod 256) << kOrdShift.
 //
 // Requests are taken 32 at a time, lane l covering request b + l.  After a scan of their tile
 // counts every record is produced by one lane, 32 * PER records per round (PER per lane), which
@@ -245,6 +251,12 @@ __device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const i
     const int total = __shfl_sync(0xffffffffu, incl, 31);
     const int room = kMaxList - n;
     const int take = min(total, room);
+    // Request ordinals: the requests with tiles are numbered along the run; lane 0's request
+    // keeps its number when it continues the previous list's last request.
+    const unsigned act = __ballot_sync(0xffffffffu, cnt > 0);
+    const bool cont = n == 0 && cur.prev_b == b;
+    const unsigned le = lane == 31 ? 0xffffffffu : (2u << lane) - 1u;
+    const int my_ord = cur.ord + __popc(act & le) - (cont ? 1 : 0);
     for (int c0 = 0; c0 < take; c0 += 32 * PER) {
       int rx[PER], rj[PER], npg[PER], id[PER][PPT];
       const int32_t *row[PER];
@@ -259,6 +271,7 @@ __device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const i
         const int e_s = __shfl_sync(0xffffffffu, excl, src);
         const int c_s = __shfl_sync(0xffffffffu, cnt, src);
         const int j_s = __shfl_sync(0xffffffffu, jlo, src);
+        const int o_s = __shfl_sync(0xffffffffu, my_ord, src) & 255;
         rx[h] = -1;
         rj[h] = 0;
         npg[h] = 0;
@@ -268,7 +281,7 @@ __device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const i
           const int tile = j_s + (idx - e_s);
           const bool first = n + idx == 0 ? cur.prev_b != req : idx == e_s;
           const bool last = idx == e_s + c_s - 1;
-          rx[h] = req | (first ? kFirstFlag : 0) | (last ? kLastFlag : 0);
+          rx[h] = req | (first ? kFirstFlag : 0) | (last ? kLastFlag : 0) | (o_s << kOrdShift);
           rj[h] = tile;
           const int len = s_len[req];
           const int npages = (len + (1 << BS_SHIFT) - 1) >> BS_SHIFT;
@@ -308,11 +321,13 @@ __device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const i
       n += total;
       b += 32;
       j = 0;
+      cur.ord += __popc(act) - (cont ? 1 : 0);
     } else {
       // The list ends inside request L, which continues in the next list.
       const int L = __ffs(__ballot_sync(0xffffffffu, incl > room)) - 1;
       const int l_excl = __shfl_sync(0xffffffffu, excl, L);
       const int l_jlo = __shfl_sync(0xffffffffu, jlo, L);
+      cur.ord = __shfl_sync(0xffffffffu, my_ord, L);
       b += L;
       j = l_jlo + (room - l_excl);
       n = kMaxList;
@@ -424,7 +439,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
     __syncwarp();
     // Start at the first tile that exists (a stale schedule or empty requests may point past it).
     const TileIter it = make_iter(s0.x, s0.y, s1.x, s1.y, batch, s_len);
-    cursor = ListCursor{it.b, it.j, it.b_end, it.j_end, -1};
+    cursor = ListCursor{it.b, it.j, it.b_end, it.j_end, -1, 0};
     if (a.row_ends != nullptr) {
       for (int b = blockIdx.x + lane * gridDim.x; b < batch; b += 32 * gridDim.x) {
         const int len = s_len[b];
@@ -591,37 +606,45 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
       __syncwarp();
     } else {
       // ============================== epilogue ================================================
-      const int team = (warp - kEpiWarpBase) / C::TEAM_WARPS;  // takes tiles k with k % 2 == team
+      const int team = (warp - kEpiWarpBase) / C::TEAM_WARPS;  // takes tiles k % TEAMS == team
       const int t_first = ((warp - kEpiWarpBase) / 4) % C::SPLIT * C::SLOTS;  // first draft slot
       const int quarter = warp & 3;
       const int c = lane & 3;
       const int pos = quarter * 32 + (lane >> 2) + 8 * c;  // the position this thread stores
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
       float2 wreg[C::SLOTS][8];  // weights of this thread's heads {8r + 2c, 8r + 2c + 1}, per slot
-      int wseq = -1;       // the request (by q/w buffer sequence number) wreg belongs to
+      // A warp walks only its team's tiles.  The q/w buffers it no longer needs are released
+      // lazily: on reaching a tile of a new request (by ordinal o), it first arrives on q_empty
+      // for every earlier request it has not released, then waits for the new request's q/w.
+      // (The producer needs request j released only to load request j + 2's q/w, and a warp
+      // releases j before it waits for anything beyond j, so the two cannot wait on each other.)
+      int wseq = 0;      // ordinal (mod 256) of the request whose weights are in wreg (0: none)
+      int released = 0;  // ordinal up to which this warp has arrived on q_empty
       if (ok) {
-        for (int i = 0; i < n; ++i) {
+        for (int i = (team - kbase % C::TEAMS + C::TEAMS) % C::TEAMS; i < n; i += C::TEAMS) {
           const int4 r = s_list[i];
           const int b = r.x & 0xFFFF;
           const int k = kbase + i;
-          if (r.x & kFirstFlag) {
-            qb = qcount & 1;
-            if (!mbar_wait(&q_full[qb], (qcount >> 1) & 1, kWaitLimitNs)) {
-              ok = false;
-              break;
-            }
-            ++qcount;
-          }
-          if ((k & 1) == team) {
-            if (wseq != qcount) {
-              const float2 *w2 = reinterpret_cast<const float2 *>(s_w + qb * C::W_FLOATS);
+          {
+            const int o = (r.x >> kOrdShift) & 255;
+            if (o != wseq) {
+              __syncwarp();
+              for (int q = (released + 1) & 255; q != o; q = (q + 1) & 255)
+                if (lane == 0) mbar_arrive(&q_empty[(q - 1) & 1]);
+              released = (o - 1) & 255;
+              const int qbuf = (o - 1) & 1;
+              if (!mbar_wait(&q_full[qbuf], ((o - 1) >> 1) & 1, kWaitLimitNs)) {
+                ok = false;
+                break;
+              }
+              const float2 *w2 = reinterpret_cast<const float2 *>(s_w + qbuf * C::W_FLOATS);
 #pragma unroll
               for (int u = 0; u < C::SLOTS; ++u)
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
                   wreg[u][q] = t_first + u < NN ? w2[(t_first + u) * (kHeads / 2) + 4 * q + c]
                                                 : make_float2(0.0f, 0.0f);
-              wseq = qcount;
+              wseq = o;
             }
             const int stage = k % C::STAGES;
             const uint32_t par = (k / C::STAGES) & 1;
@@ -686,10 +709,6 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
               if constexpr (C::SPLIT == 2) asm volatile("" : "+f"(logit));  // before the next load
               if (store) store_out(dst + static_cast<int64_t>(t) * a.out_stride, logit);
             }
-          }
-          if (r.x & kLastFlag) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&q_empty[qb]);
           }
         }
       }
