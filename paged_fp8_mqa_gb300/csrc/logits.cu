@@ -621,10 +621,23 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
       int wseq = 0;      // ordinal (mod 256) of the request whose weights are in wreg (0: none)
       int released = 0;  // ordinal up to which this warp has arrived on q_empty
       if (ok) {
-        for (int i = (team - kbase % C::TEAMS + C::TEAMS) % C::TEAMS; i < n; i += C::TEAMS) {
+        // Tile k's stage, its parity, scale slot and accumulator, advanced by TEAMS per own tile
+        // (no division in the loop; with the slot split, where registers are scarcer and the
+        // moduli cheaper, they are derived from k instead).
+        const int i0 = (team - kbase % C::TEAMS + C::TEAMS) % C::TEAMS;
+        int e_stage = (kbase + i0) % C::STAGES, e_sslot = (kbase + i0) % C::SCALE_SLOTS;
+        int e_acc = (kbase + i0) % C::ACC;
+        uint32_t par = ((kbase + i0) / C::STAGES) & 1;
+        for (int i = i0; i < n; i += C::TEAMS) {
           const int4 r = s_list[i];
           const int b = r.x & 0xFFFF;
-          const int k = kbase + i;
+          if constexpr (C::SPLIT == 2) {
+            const int k = kbase + i;
+            e_stage = k % C::STAGES;
+            e_sslot = k % C::SCALE_SLOTS;
+            e_acc = k % C::ACC;
+            par = (k / C::STAGES) & 1;
+          }
           {
             const int o = (r.x >> kOrdShift) & 255;
             if (o != wseq) {
@@ -646,8 +659,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
                                                 : make_float2(0.0f, 0.0f);
               wseq = o;
             }
-            const int stage = k % C::STAGES;
-            const uint32_t par = (k / C::STAGES) & 1;
+            const int stage = e_stage;
             // done: tile k's MMAs (so its accumulator) completed.  full: makes the tile's
             // TMA-written scales visible to this thread (the phase is complete by then).
             if (!mbar_wait(&done[stage], par, kWaitLimitNs) ||
@@ -657,12 +669,12 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
             }
             tc_fence_after_sync();
             const bool have = (static_cast<uint32_t>(r.x) >> (kMaskShift + (pos >> bs_shift))) & 1u;
-            const float scale = have ? s_scale[(k % C::SCALE_SLOTS) * kTileTokens + pos] : 0.0f;
+            const float scale = have ? s_scale[e_sslot * kTileTokens + pos] : 0.0f;
             const int p = r.y * kTileTokens + pos;
             const bool store = p < s_len[b];
             OutT *dst =
                 static_cast<OutT *>(a.out) + static_cast<int64_t>(b * NN) * a.out_stride + p;
-            const uint32_t col0 = static_cast<uint32_t>((k % C::ACC) * C::N);
+            const uint32_t col0 = static_cast<uint32_t>(e_acc * C::N);
             const int nslots = min(C::SLOTS, NN - t_first);
             // The quadrant's two 16-lane windows hold positions (g, g + 8) and (g + 16, g + 24).
             // With the slot split (more warps, fewer registers each) they are read one after the
@@ -694,7 +706,8 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
                 // The accumulator is in registers: free it for tile k + ACC before the arithmetic.
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full[(k + C::ACC) % C::STAGES]);
+                const int rel = e_stage + C::ACC;  // tile k + ACC's stage
+                if (lane == 0) mbar_arrive(&full[rel >= C::STAGES ? rel - C::STAGES : rel]);
               }
               if constexpr (C::SPLIT == 1) p01 = quad_partials(va, wreg[u]);
               float2 p23 = quad_partials(vb, wreg[u]);
@@ -709,6 +722,14 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
               if constexpr (C::SPLIT == 2) asm volatile("" : "+f"(logit));  // before the next load
               if (store) store_out(dst + static_cast<int64_t>(t) * a.out_stride, logit);
             }
+          }
+          if constexpr (C::SPLIT == 1) {
+            if ((e_stage += C::TEAMS) >= C::STAGES) {
+              e_stage -= C::STAGES;
+              par ^= 1;
+            }
+            if ((e_sslot += C::TEAMS) >= C::SCALE_SLOTS) e_sslot -= C::SCALE_SLOTS;
+            if ((e_acc += C::TEAMS) >= C::ACC) e_acc -= C::ACC;
           }
         }
       }
