@@ -682,6 +682,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
             // issued before this slot's quad reduction, so the shuffles overlap their latency
             // (with the split that ordering measured slower).
             uint32_t va[32], vb[32];
+            float4 part[C::SLOTS];  // (slot split) each slot's partial sums, reduced at the end
 #pragma unroll
             for (int u = 0; u < C::SLOTS; ++u) {
               if (u >= nslots) break;
@@ -718,9 +719,23 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
                 tmem_ld_16x256b_x8(lane_base + col + kHeads, va);
                 tmem_ld_16x256b_x8(lane_base + (16u << 16) + col + kHeads, vb);
               }
-              float logit = scale * quad_reduce_scatter(p01.x, p01.y, p23.x, p23.y, c);
-              if constexpr (C::SPLIT == 2) asm volatile("" : "+f"(logit));  // before the next load
-              if (store) store_out(dst + static_cast<int64_t>(t) * a.out_stride, logit);
+              if constexpr (C::SPLIT == 2) {
+                // The shuffles and stores wait until every slot has been read, which frees the
+                // accumulator earlier (its release gates the MMA of tile k + ACC).
+                part[u] = make_float4(p01.x, p01.y, p23.x, p23.y);
+              } else {
+                const float logit = scale * quad_reduce_scatter(p01.x, p01.y, p23.x, p23.y, c);
+                if (store) store_out(dst + static_cast<int64_t>(t) * a.out_stride, logit);
+              }
+            }
+            if constexpr (C::SPLIT == 2) {
+#pragma unroll
+              for (int u = 0; u < C::SLOTS; ++u) {
+                if (u >= nslots) break;
+                const float4 q = part[u];
+                const float logit = scale * quad_reduce_scatter(q.x, q.y, q.z, q.w, c);
+                if (store) store_out(dst + static_cast<int64_t>(t_first + u) * a.out_stride, logit);
+              }
             }
           }
           if constexpr (C::SPLIT == 1) {
