@@ -475,6 +475,12 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   bool ok = true;
   bool drained = false;  // (MMA issuer) the drain commit is out
   uint32_t tmem_base = 0;
+  // (epilogue) The request whose weights are in registers, by its ordinal in the run (mod 256;
+  // 0: none yet), the ordinal up to which this warp has arrived on q_empty, and the weights of
+  // this thread's heads {8r + 2c, 8r + 2c + 1} per draft slot.
+  int wseq = 0;
+  int released = 0;
+  float2 wreg[C::SLOTS][8];
 
   for (;;) {
     if (warp == 0) {
@@ -612,14 +618,12 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
       const int c = lane & 3;
       const int pos = quarter * 32 + (lane >> 2) + 8 * c;  // the position this thread stores
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-      float2 wreg[C::SLOTS][8];  // weights of this thread's heads {8r + 2c, 8r + 2c + 1}, per slot
       // A warp walks only its team's tiles.  The q/w buffers it no longer needs are released
       // lazily: on reaching a tile of a new request (by ordinal o), it first arrives on q_empty
       // for every earlier request it has not released, then waits for the new request's q/w.
       // (The producer needs request j released only to load request j + 2's q/w, and a warp
       // releases j before it waits for anything beyond j, so the two cannot wait on each other.)
-      int wseq = 0;      // ordinal (mod 256) of the request whose weights are in wreg (0: none)
-      int released = 0;  // ordinal up to which this warp has arrived on q_empty
+      // wseq, released and wreg carry over from one tile list to the next.
       if (ok) {
         // Tile k's stage, its parity, scale slot and accumulator, advanced by TEAMS per own tile
         // (no division in the loop; with the slot split, where registers are scarcer and the

@@ -120,6 +120,21 @@ def test_runs_longer_than_one_tile_list(num_sms):
     check_logits(w, got, ref, tol)
 
 
+@pytest.mark.parametrize("next_n", [1, 3])
+def test_many_short_requests_over_several_tile_lists(next_n):
+    """One CTA's run of ~300 requests of one to three tiles spans three tile lists: the q/w
+    buffers, reused every second request, are released exactly once per request across the
+    lists' boundaries (each list's first tile is a continued or a new request)."""
+    g = torch.Generator().manual_seed(40 + next_n)
+    lens = torch.randint(1, 330, (300,), generator=g).tolist()
+    lens[100:110] = [0] * 10
+    w = _small(307 + next_n, next_n, lens)
+    ref, tol = _oracle(w)
+    for num_sms in (1, 2):
+        got, _ = gpu_logits(w, num_sms=num_sms)
+        check_logits(w, got, ref, tol)
+
+
 def test_stale_schedule_terminates():
     """A schedule computed for other lengths gives wrong coverage but no hang, no fault and no
     read past any request's pages."""
