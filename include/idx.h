@@ -5,8 +5,9 @@
  *   1. paged FP8 MQA logits   ("flashinfer.attn_scores", fp8_paged_mqa_logits)
  *   2. threshold top-k select  ("flashinfer.sdsa.indexer_threshold_select"), reading stage 1's
  *      logits
- * plus the persistent work split of stage 1 ("flashinfer.attn_scores", Scheduling and Setup)
- * and the two integer helpers named there.
+ * and both fused into one pass that writes no logits (idx_indexer_threshold_select), plus the
+ * persistent work split of stage 1 ("flashinfer.attn_scores", Scheduling and Setup) and the two
+ * integer helpers named there.
  *
  * Conventions shared by every entry point
  *   - Pointers marked "device" are caller-owned device memory; the library never allocates,
@@ -186,7 +187,7 @@ int idx_threshold_select(const float *logits, int64_t logits_row_stride, const i
                          int32_t *ranges, void *stream);
 
 /*
- * idx_threshold_select_static -- the paper has no counterpart to this entry point; it exists
+ * idx_threshold_select_static -- the pages have no counterpart to this entry point; it exists
  * for callers that cannot allocate device memory.
  *
  * idx_threshold_select with repair needs an `arrivals` workspace of one int32 per row.  Some
@@ -212,6 +213,56 @@ int idx_threshold_select_static(const float *logits, int64_t logits_row_stride,
                                 int32_t *counters, int32_t *candidates, int32_t top_k,
                                 int32_t capacity, int32_t max_context, int32_t *ranges,
                                 void *stream);
+
+/*
+ * idx_indexer_threshold_select ("flashinfer.sdsa.indexer_threshold_select": description;
+ * Parameters thresholds, counters, candidates, top_k, arrivals, ranges): the logits of
+ * idx_logits_fp8 and the selection of idx_threshold_select in one pass over each request's
+ * paged keys, without writing the scores.  The rows are those of idx_logits_fp8 (row
+ * b*next_n + t sees keys p < max(0, seq_lens[b] - next_n + t + 1)), and every output --
+ * counters, the slot contents (as sets), ranges, repaired thresholds -- equals what
+ * idx_logits_fp8 (float32) followed by idx_threshold_select with those row ends would give:
+ * each score is computed by the same arithmetic, then classified instead of stored.
+ *
+ * The pages' query "tile" is here one request: its next_n * 64 query-head rows are the tensor
+ * core's N side, so the arrivals are counted per request (int32 [batch]).
+ *
+ * Without arrivals: one launch; the rows' counts and slots only (rows that do not fit are not
+ * repaired, and ranges is not written).
+ * With arrivals: every row fits on return.  Three launches on `stream`, no host
+ * synchronisation (capturable once run eagerly):
+ *   1. the fused pass; the last of a request's tiles to finish applies the fit rule to its
+ *      rows, writes their ranges, and marks the request in arrivals[b] if a row does not fit;
+ *   2. the marked requests' logits recomputed into `scratch` (float32, by the same kernel;
+ *      every other request counts as empty, so nothing else is read or written);
+ *   3. the radix repair of idx_threshold_select for each row that does not fit, from its
+ *      scratch row; arrivals[b] returns to zero.
+ * When no row needs a repair, launches 2 and 3 read only seq_lens and arrivals.
+ *
+ * q, kv_fused, num_blocks, block_size, weights, block_tables, bt_row_stride, bt_width,
+ * seq_lens, seq_lens_stride, batch, next_n, num_heads, head_dim, max_seq_len, num_sms
+ *                     as for idx_logits_fp8 (the work split is always derived in the kernel)
+ *   thresholds        device float32 [batch*next_n], read, and written for repaired rows
+ *   counters          device int32 [batch*next_n][2] (candidates, ties), ZEROED BY THE CALLER
+ *   candidates        device int32 [batch*next_n][top_k + capacity][2], 8-byte aligned
+ *   top_k, capacity   as for idx_threshold_select (capacity >= top_k - 1 with arrivals)
+ *   arrivals          NULL, or device int32 [batch], zeroed once; every call leaves it zeroed
+ *                     (unless a device wait timed out: see idx_device_status)
+ *   ranges            device int32 [2][batch*next_n]; required with arrivals
+ *   scratch           device float32, 16-byte aligned, rows of scratch_row_stride elements
+ *                     (>= idx_padded_seq_len(max_seq_len), a multiple of 4); required with
+ *                     arrivals; only rows of requests that need a repair are written
+ */
+int idx_indexer_threshold_select(const uint8_t *q, const uint8_t *kv_fused, int64_t num_blocks,
+                                 int32_t block_size, const float *weights,
+                                 const int32_t *block_tables, int64_t bt_row_stride,
+                                 int32_t bt_width, const int32_t *seq_lens,
+                                 int64_t seq_lens_stride, int32_t batch, int32_t next_n,
+                                 int32_t num_heads, int32_t head_dim, int32_t max_seq_len,
+                                 int32_t num_sms, float *thresholds, int32_t *counters,
+                                 int32_t *candidates, int32_t top_k, int32_t capacity,
+                                 int32_t *arrivals, int32_t *ranges, float *scratch,
+                                 int64_t scratch_row_stride, void *stream);
 
 /*
  * Reads (and, if clear != 0, resets) the OR of the device-side status bits (IDX_DEV_*) that

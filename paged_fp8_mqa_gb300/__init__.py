@@ -4,9 +4,10 @@ A thin ctypes binding over ``libidx.so`` (declared in ``include/idx.h``).  It on
 arguments: every step of the indexer runs in the library's CUDA kernels, and there is no CPU
 fallback -- if the library has not been built, every call raises.
 
-Low-level names mirror the C ABI (``idx_logits_fp8``, ``idx_threshold_select``, ``idx_schedule``,
-``idx_padded_seq_len``, ``idx_min_block_table_width``, ...); they take raw pointers and sizes.
-The torch-facing helpers (``logits_fp8``, ``threshold_select``, ``schedule``) take tensors,
+Low-level names mirror the C ABI (``idx_logits_fp8``, ``idx_threshold_select``,
+``idx_indexer_threshold_select``, ``idx_schedule``, ``idx_padded_seq_len``,
+``idx_min_block_table_width``, ...); they take raw pointers and sizes.  The torch-facing helpers
+(``logits_fp8``, ``threshold_select``, ``indexer_threshold_select``, ``schedule``) take tensors,
 check dtypes/devices, and pass pointers, strides and the current CUDA stream through.
 """
 from __future__ import annotations
@@ -69,6 +70,11 @@ def lib() -> ctypes.CDLL:
     L.idx_threshold_select.restype = c.c_int
     L.idx_threshold_select.argtypes = [P, c.c_int64, P, c.c_int32, P, P, P, c.c_int32,
                                        c.c_int32, c.c_int32, P, P, P]
+    L.idx_indexer_threshold_select.restype = c.c_int
+    L.idx_indexer_threshold_select.argtypes = [
+        P, P, c.c_int64, c.c_int32, P, P, c.c_int64, c.c_int32, P, c.c_int64, c.c_int32,
+        c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32, P, P, P, c.c_int32, c.c_int32, P,
+        P, P, c.c_int64, P]
     L.idx_device_status.restype = c.c_int
     L.idx_device_status.argtypes = [P, c.c_int32]
     _lib = L
@@ -140,6 +146,18 @@ def idx_threshold_select_static(logits, logits_row_stride, row_ends, rows, thres
 
 
 IDX_STATIC_SELECT_MAX_ROWS = 16384
+
+
+def idx_indexer_threshold_select(q, kv_fused, num_blocks, block_size, weights, block_tables,
+                                 bt_row_stride, bt_width, seq_lens, seq_lens_stride, batch,
+                                 next_n, num_heads, head_dim, max_seq_len, num_sms, thresholds,
+                                 counters, candidates, top_k, capacity, arrivals, ranges,
+                                 scratch, scratch_row_stride, stream) -> int:
+    return lib().idx_indexer_threshold_select(
+        q, kv_fused, num_blocks, block_size, weights, block_tables, bt_row_stride, bt_width,
+        seq_lens, seq_lens_stride, batch, next_n, num_heads, head_dim, max_seq_len, num_sms,
+        thresholds, counters, candidates, top_k, capacity, arrivals, ranges, scratch,
+        scratch_row_stride, stream)
 
 
 def idx_device_status(clear: bool = False) -> int:
@@ -245,6 +263,58 @@ def threshold_select(logits, row_ends, thresholds, counters, candidates, top_k: 
                                 _ptr(thresholds), _ptr(counters), _ptr(candidates), top_k,
                                 capacity, max_context, _ptr(arrivals), _ptr(ranges),
                                 _stream(stream)))
+
+
+def indexer_threshold_select(q, kv_fused, weights, block_tables, seq_lens, max_seq_len: int, *,
+                             thresholds, counters, candidates, top_k: int, arrivals=None,
+                             ranges=None, scratch=None, num_sms: int = 0, stream=None):
+    """Scores and threshold select in one pass, without writing the scores.  Inputs as for
+    ``logits_fp8``; rows b*next_n + t as there.  thresholds float32 [rows]; counters int32
+    [rows, 2] zeroed by the caller; candidates int32 [rows, top_k + capacity, 2].  With
+    ``arrivals`` (int32 [batch], zeroed once) every row is repaired to fit and ``ranges`` (int32
+    [2, rows]) is written; ``scratch`` (float32 [rows, >= padded_seq_len]) receives the rescored
+    rows of the requests that need the repair, and is allocated here if not given."""
+    import torch
+    _need(q, (torch.float8_e4m3fn, torch.uint8), "q", 4)
+    _need(kv_fused, torch.uint8, "kv_fused")
+    _need(weights, torch.float32, "weights", 2)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(thresholds, torch.float32, "thresholds", 1)
+    _need(counters, torch.int32, "counters", 2)
+    _need(candidates, torch.int32, "candidates", 3)
+    B, n, H, D = q.shape
+    rows = B * n
+    if not q.is_contiguous() or not weights.is_contiguous() or not kv_fused.is_contiguous():
+        raise ValueError("q, weights and kv_fused must be contiguous")
+    if block_tables.stride(1) != 1:
+        raise ValueError("block_tables rows must be contiguous (stride(1) == 1)")
+    for t, name in ((thresholds, "thresholds"), (counters, "counters"),
+                    (candidates, "candidates")):
+        if not t.is_contiguous() or t.shape[0] < rows:
+            raise ValueError(f"{name} must be contiguous with at least {rows} rows")
+    capacity = candidates.shape[1] - top_k
+    if capacity < 0 or candidates.shape[2] != 2:
+        raise ValueError("candidates must be [rows, top_k + capacity, 2]")
+    if arrivals is not None:
+        _need(arrivals, torch.int32, "arrivals", 1)
+        if ranges is None:
+            raise ValueError("ranges is required with arrivals")
+        _need(ranges, torch.int32, "ranges", 2)
+        if scratch is None:
+            scratch = torch.empty(rows, idx_padded_seq_len(max_seq_len), dtype=torch.float32,
+                                  device=q.device)
+        _need(scratch, torch.float32, "scratch", 2)
+        if scratch.stride(1) != 1:
+            raise ValueError("scratch rows must be contiguous")
+    num_blocks = kv_fused.shape[0]
+    block_size = kv_fused.numel() // num_blocks // (D + 4) if num_blocks else 0
+    _check(idx_indexer_threshold_select(
+        _ptr(q), _ptr(kv_fused), num_blocks, block_size, _ptr(weights), _ptr(block_tables),
+        block_tables.stride(0), block_tables.shape[1], _ptr(seq_lens), seq_lens.stride(0), B, n,
+        H, D, max_seq_len, num_sms, _ptr(thresholds), _ptr(counters), _ptr(candidates), top_k,
+        capacity, _ptr(arrivals), _ptr(ranges), _ptr(scratch),
+        scratch.stride(0) if scratch is not None else 0, _stream(stream)))
 
 
 def device_status(clear: bool = False) -> int:

@@ -223,7 +223,7 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
   st = encode_rows128(&q_map, q, static_cast<uint64_t>(batch) * next_n * num_heads, 128,
                       static_cast<uint32_t>(next_n * num_heads));
   if (st != IDX_OK) return st;
-  idx::LogitsArgs a;
+  idx::LogitsArgs a{};
   a.kv = kv_fused;
   a.weights = weights;
   a.block_tables = block_tables;
@@ -238,9 +238,133 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.batch = batch;
-  const cudaError_t e = idx::launch_logits_fp8(next_n, output_dtype == IDX_DTYPE_F16, kv_map,
-                                               q_map, a, ctas, s);
+  const cudaError_t e = idx::launch_logits_fp8(
+      next_n, output_dtype == IDX_DTYPE_F16 ? idx::LogitsOut::kF16 : idx::LogitsOut::kF32, kv_map,
+      q_map, a, ctas, s);
   if (e != cudaSuccess) return cuda_fail(e, "logits launch");
+  return IDX_OK;
+}
+
+IDX_EXPORT int idx_indexer_threshold_select(
+    const uint8_t *q, const uint8_t *kv_fused, int64_t num_blocks, int32_t block_size,
+    const float *weights, const int32_t *block_tables, int64_t bt_row_stride, int32_t bt_width,
+    const int32_t *seq_lens, int64_t seq_lens_stride, int32_t batch, int32_t next_n,
+    int32_t num_heads, int32_t head_dim, int32_t max_seq_len, int32_t num_sms, float *thresholds,
+    int32_t *counters, int32_t *candidates, int32_t top_k, int32_t capacity, int32_t *arrivals,
+    int32_t *ranges, float *scratch, int64_t scratch_row_stride, void *stream) {
+  g_error.clear();
+  if (q == nullptr || kv_fused == nullptr || weights == nullptr || block_tables == nullptr ||
+      seq_lens == nullptr || thresholds == nullptr || counters == nullptr || candidates == nullptr)
+    return fail(IDX_INVALID_ARG,
+                "q, kv_fused, weights, block_tables, seq_lens, thresholds, counters, "
+                "candidates: NULL");
+  if (batch < 0 || max_seq_len < 0 || num_blocks < 1 || bt_width < 0 || seq_lens_stride < 1 ||
+      bt_row_stride < bt_width || block_size <= 0 || num_heads <= 0 || head_dim <= 0 ||
+      next_n <= 0)
+    return fail(IDX_INVALID_ARG, "negative or inconsistent size or stride");
+  if (num_heads != 64 || head_dim != 128 ||
+      (block_size != 32 && block_size != 64 && block_size != 128))
+    return fail(IDX_UNSUPPORTED,
+                "this build supports num_heads 64, head_dim 128, block_size 32, 64 or 128");
+  if (next_n > 4) return fail(IDX_UNSUPPORTED, "next_n must be 1..4");
+  if (batch > idx::kMaxBatch) return fail(IDX_UNSUPPORTED, "batch above 4096");
+  if (top_k < 1 || capacity < 0 || static_cast<int64_t>(top_k) + capacity > (INT32_MAX / 2))
+    return fail(IDX_INVALID_ARG, "top_k >= 1 and capacity >= 0 required");
+  const int64_t page_bytes = static_cast<int64_t>(block_size) * (head_dim + 4);
+  if (num_blocks > (INT64_C(1) << 31) / (page_bytes / 128) - 1)
+    return fail(IDX_INVALID_ARG, "num_blocks too large for 32-bit TMA row coordinates");
+  if (!aligned(q, 16) || !aligned(kv_fused, 16) || !aligned(weights, 16))
+    return fail(IDX_INVALID_ARG, "q, kv_fused and weights must be 16-byte aligned");
+  if (!aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(thresholds, 4) ||
+      !aligned(counters, 4) || !aligned(candidates, 8) ||
+      (arrivals != nullptr && !aligned(arrivals, 4)) || (ranges != nullptr && !aligned(ranges, 4)))
+    return fail(IDX_INVALID_ARG, "candidates must be 8-byte aligned, int32/float32 4-byte");
+  if (arrivals != nullptr) {
+    if (ranges == nullptr || scratch == nullptr)
+      return fail(IDX_INVALID_ARG, "ranges and scratch are required with arrivals");
+    if (capacity < top_k - 1)
+      return fail(IDX_INVALID_ARG, "with arrivals, capacity must be >= top_k - 1");
+    if (scratch_row_stride < idx_padded_seq_len(max_seq_len) || scratch_row_stride % 4 != 0 ||
+        !aligned(scratch, 16))
+      return fail(IDX_INVALID_ARG,
+                  "scratch must be 16-byte aligned with a row stride >= "
+                  "idx_padded_seq_len(max_seq_len), a multiple of 4");
+  }
+  int32_t ctas = 0;
+  int st = resolve_sms(num_sms, &ctas);
+  if (st != IDX_OK) return st;
+  if (batch == 0) return IDX_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (validate_requested()) {
+    st = validate_logits_contents(block_tables, bt_row_stride, bt_width, seq_lens,
+                                  seq_lens_stride, batch, max_seq_len, num_blocks, block_size, s);
+    if (st != IDX_OK) return st;
+  }
+  CUtensorMap kv_map, q_map;
+  st = encode_rows128(&kv_map, kv_fused, static_cast<uint64_t>(num_blocks) * (page_bytes / 128),
+                      128, static_cast<uint32_t>(block_size));
+  if (st != IDX_OK) return st;
+  st = encode_rows128(&q_map, q, static_cast<uint64_t>(batch) * next_n * num_heads, 128,
+                      static_cast<uint32_t>(next_n * num_heads));
+  if (st != IDX_OK) return st;
+  idx::LogitsArgs a{};
+  a.kv = kv_fused;
+  a.weights = weights;
+  a.block_tables = block_tables;
+  a.bt_stride = bt_row_stride;
+  a.bt_width = bt_width;
+  a.seq_lens = seq_lens;
+  a.sl_stride = seq_lens_stride;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.batch = batch;
+  a.thresholds = thresholds;
+  a.counters = counters;
+  a.candidates = candidates;
+  a.arrivals = arrivals;
+  a.ranges = ranges;
+  a.top_k = top_k;
+  a.capacity = capacity;
+  a.repair = arrivals != nullptr ? 1 : 0;
+  // 1. Scores classified into the slots; the last arrival of each request applies the fit rule.
+  cudaError_t e = idx::launch_logits_fp8(next_n, idx::LogitsOut::kSelect, kv_map, q_map, a, ctas, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fused logits launch");
+  if (arrivals == nullptr) return IDX_OK;
+  // 2. The flagged requests' scores again, this time stored (every other request counts as
+  // empty, and the work split covers only the flagged ones).
+  idx::LogitsArgs r{};
+  r.kv = kv_fused;
+  r.weights = weights;
+  r.block_tables = block_tables;
+  r.bt_stride = bt_row_stride;
+  r.bt_width = bt_width;
+  r.seq_lens = seq_lens;
+  r.sl_stride = seq_lens_stride;
+  r.num_blocks = num_blocks;
+  r.block_size = block_size;
+  r.batch = batch;
+  r.out = scratch;
+  r.out_stride = scratch_row_stride;
+  r.len_mask = arrivals;
+  e = idx::launch_logits_fp8(next_n, idx::LogitsOut::kF32, kv_map, q_map, r, ctas, s);
+  if (e != cudaSuccess) return cuda_fail(e, "rescoring launch");
+  // 3. The radix repair of the rows that do not fit, from the rescored rows.
+  idx::FusedRepairArgs f{};
+  f.scratch = scratch;
+  f.scratch_stride = scratch_row_stride;
+  f.seq_lens = seq_lens;
+  f.sl_stride = seq_lens_stride;
+  f.thresholds = thresholds;
+  f.counters = counters;
+  f.candidates = candidates;
+  f.arrivals = arrivals;
+  f.ranges = ranges;
+  f.batch = batch;
+  f.next_n = next_n;
+  f.top_k = top_k;
+  f.capacity = capacity;
+  e = idx::launch_fused_repair(f, s);
+  if (e != cudaSuccess) return cuda_fail(e, "repair launch");
   return IDX_OK;
 }
 

@@ -48,10 +48,27 @@ struct LogitsArgs {
   int64_t num_blocks;
   int32_t batch;
   int32_t block_size;           // tokens per page: 32, 64 or 128
+  // Rescoring (nullable): requests b with len_mask[b] >= 0 count as empty.
+  const int32_t *len_mask;
+  // Fused select (LogitsOut::kSelect; rows b * next_n + t): the select's per-row state.
+  const float *thresholds;
+  int32_t *counters;            // [rows][2], zeroed by the caller
+  int32_t *candidates;          // [rows][top_k + capacity][2]
+  int32_t *arrivals;            // nullable: [batch], zero on entry and on exit
+  int32_t *ranges;              // [2][rows], required with arrivals
+  int32_t top_k;
+  int32_t capacity;
+  int32_t repair;               // nonzero: flag requests whose rows do not fit for the repair
 };
 
-// Launches the logits kernel for draft depth `next_n` (1..4), float16 output if `out_f16`.
-cudaError_t launch_logits_fp8(int next_n, bool out_f16, const CUtensorMap &kv_map,
+// After the fused logits kernel, arrivals[b] = -next_n marks request b as having a row that does
+// not fit; each of the request's next_n repair CTAs adds one when done, which returns it to zero.
+
+// What the logits kernel does with each score.
+enum class LogitsOut { kF32, kF16, kSelect };
+
+// Launches the logits kernel for draft depth `next_n` (1..4).
+cudaError_t launch_logits_fp8(int next_n, LogitsOut mode, const CUtensorMap &kv_map,
                               const CUtensorMap &q_map, const LogitsArgs &args, int num_ctas,
                               cudaStream_t stream);
 
@@ -75,6 +92,25 @@ struct SelectArgs {
 };
 
 cudaError_t launch_threshold_select(const SelectArgs &args, cudaStream_t stream);
+
+// The fused score + select's repair stage: one CTA per row of each request marked in arrivals.
+struct FusedRepairArgs {
+  const float *scratch;    // rescored logits, row r at scratch + r * scratch_stride
+  int64_t scratch_stride;
+  const int32_t *seq_lens;
+  int64_t sl_stride;
+  float *thresholds;
+  int32_t *counters;
+  int32_t *candidates;
+  int32_t *arrivals;
+  int32_t *ranges;
+  int32_t batch;
+  int32_t next_n;
+  int32_t top_k;
+  int32_t capacity;
+};
+
+cudaError_t launch_fused_repair(const FusedRepairArgs &args, cudaStream_t stream);
 
 // The same launch with `args.arrivals` replaced by the library's own static device array
 // (at most IDX_STATIC_SELECT_MAX_ROWS rows; the caller checks).

@@ -27,6 +27,12 @@
 //              threads of a quad exchange them (reduce-scatter) so that each ends with one
 //              position's complete sum, and the warp stores 32 consecutive positions (one
 //              128-byte line per output row) after multiplying by the position's scale.
+// Fused select ("flashinfer.sdsa.indexer_threshold_select": description).  Instantiated with
+// SelectOut, the epilogue classifies each score against its row's threshold into the row's
+// candidate and tie slots (slots.cuh) instead of storing it.  With arrivals, each epilogue warp
+// adds its tile count of a request to arrivals[b] when it moves on to the next request (or ends
+// its run); the warp whose addition completes the request's count applies the fit rule to the
+// request's rows.  A launch with len_mask rescores only the requests marked there.
 // Barriers.  The issuing thread is the serial point of the pipeline, so it waits on one barrier
 // and commits to one barrier per tile:
 //   full[s]   tile k may be multiplied: its TMA bytes landed (producer's expect_tx), and the
@@ -50,6 +56,7 @@
 #include "../../include/idx.h"
 #include "internal.h"
 #include "ptx.cuh"
+#include "slots.cuh"
 #include "split.cuh"
 
 namespace idx {
@@ -115,6 +122,11 @@ __device__ __forceinline__ void flag_error(int bits) { atomicOr(&g_logits_status
 // The output element: float32, or float16 rounded to nearest even (the pages' output_dtype).
 __device__ __forceinline__ void store_out(float *p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__half *p, float v) { *p = __float2half_rn(v); }
+
+// The fused score + select output ("flashinfer.sdsa.indexer_threshold_select": description):
+// instead of being stored, each score is classified against its row's threshold into the row's
+// candidate and tie slots.
+struct SelectOut {};
 
 // relu(s) * 2^-25 on the FMA pipe: a saturating multiply clamps to [0, 1] (NaN to 0), and
 // every score satisfies |s| <= 128 * 448^2 < 2^25, so the product is exact.
@@ -323,11 +335,14 @@ __device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const i
       j = 0;
       cur.ord += __popc(act) - (cont ? 1 : 0);
     } else {
-      // The list ends inside request L, which continues in the next list.
+      // The list ends inside request L, which continues in the next list, or just before L's
+      // first tile here: then L is not in this list, and the ordinal carried over is that of
+      // the list's last request, so that L numbers itself in the next list.
       const int L = __ffs(__ballot_sync(0xffffffffu, incl > room)) - 1;
       const int l_excl = __shfl_sync(0xffffffffu, excl, L);
       const int l_jlo = __shfl_sync(0xffffffffu, jlo, L);
-      cur.ord = __shfl_sync(0xffffffffu, my_ord, L);
+      const int l_ord = __shfl_sync(0xffffffffu, my_ord, L);
+      cur.ord = room == l_excl ? l_ord - 1 : l_ord;
       b += L;
       j = l_jlo + (room - l_excl);
       n = kMaxList;
@@ -345,6 +360,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
     k_logits_fp8(const __grid_constant__ CUtensorMap kv_map,
                  const __grid_constant__ CUtensorMap q_map, const LogitsArgs a) {
   using C = Cfg<NN>;
+  constexpr bool kSelect = std::is_same<OutT, SelectOut>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~static_cast<uintptr_t>(1023u));
@@ -371,13 +387,14 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   // L2 prefetches read nothing (L2 is where that kernel's writes land, so later loads still see
   // them): seq_lens and this CTA's share of the block table start their way from DRAM while the
   // previous kernel drains.  Block-table lines hold at least one byte of a row's declared width.
+  // (A rescoring launch reads few rows of the table, if any: it prefetches none.)
   if (warp == 0) {
     if (a.sl_stride == 1) {
       for (int l = lane; l * 32 < a.batch; l += 32) prefetch_l2(a.seq_lens + l * 32);
     } else {
       for (int b = lane; b < a.batch; b += 32) prefetch_l2(a.seq_lens + b * a.sl_stride);
     }
-  } else if (warp == kEpiWarpBase && a.bt_width > 0 &&
+  } else if (warp == kEpiWarpBase && a.bt_width > 0 && a.len_mask == nullptr &&
              static_cast<int64_t>(a.batch) * a.bt_width <= (int64_t{1} << 21)) {
     for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
       const int32_t *row = a.block_tables + static_cast<int64_t>(b) * a.bt_stride;
@@ -405,6 +422,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
     for (int b = lo; b < hi; ++b) {
       int len = __ldg(a.seq_lens + static_cast<int64_t>(b) * a.sl_stride);
       len = len < 0 ? 0 : len;
+      if (a.len_mask != nullptr && a.len_mask[b] >= 0) len = 0;  // rescoring: marked requests only
       s_len[b] = len;
       mine += tiles_of(len);
     }
@@ -447,6 +465,18 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
         for (int t = 0; t < NN; ++t) a.row_ends[b * NN + t] = max(0, len - NN + t + 1);
       }
     }
+    if (kSelect && a.arrivals != nullptr) {
+      // An empty request has no tiles, so no arrival finishes its rows: they fit (K' = 0) with
+      // nothing stored.
+      for (int b = blockIdx.x + lane * gridDim.x; b < batch; b += 32 * gridDim.x) {
+        if (s_len[b] != 0) continue;
+#pragma unroll
+        for (int t = 0; t < NN; ++t) {
+          a.ranges[b * NN + t] = a.top_k;
+          a.ranges[batch * NN + b * NN + t] = a.top_k;
+        }
+      }
+    }
   } else if (warp == 1) {
     if (lane == 0) {
       prefetch_tensor_map(&kv_map);
@@ -481,6 +511,41 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   int wseq = 0;
   int released = 0;
   float2 wreg[C::SLOTS][8];
+  // (epilogue, fused select) The request being classified, this warp's tiles of it so far, and
+  // its rows' thresholds per draft slot.
+  int cur_b = -1, cur_tiles = 0;
+  float thr_u[C::SLOTS];
+
+  // (fused select) Counts this warp's `tiles` tiles of request rb toward arrivals[rb].  Every tile
+  // is read by TEAM_WARPS warps, so the warp whose arrival completes TEAM_WARPS x the request's
+  // tiles is the last, and all other warps' slot reservations are visible to it: it applies the
+  // fit rule to the request's rows, writes the range of each row that fits, and leaves
+  // arrivals[rb] = -next_n (marked for the repair launches) if a row does not, else zero.
+  const auto request_done = [&](int rb, int tiles) {
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      const int expected = C::TEAM_WARPS * tiles_of(s_len[rb]);
+      last = atomicAdd(a.arrivals + rb, tiles) + tiles == expected;
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __threadfence();
+    bool bad = false;
+    if (lane < NN) {
+      const int r = rb * NN + lane;
+      const int K = min(max(0, s_len[rb] - NN + lane + 1), a.top_k);
+      const int nc = atomicAdd(a.counters + 2 * r, 0);
+      const int nt = atomicAdd(a.counters + 2 * r + 1, 0);
+      bad = !row_fits(nc, nt, K, a.top_k, a.capacity);
+      if (!bad) {
+        a.ranges[r] = a.top_k - min(nt, a.top_k);
+        a.ranges[batch * NN + r] = a.top_k + min(nc, a.capacity);
+      }
+    }
+    const bool any = __any_sync(0xffffffffu, bad);
+    if (lane == 0) a.arrivals[rb] = any && a.repair ? -NN : 0;
+  };
 
   for (;;) {
     if (warp == 0) {
@@ -646,6 +711,14 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
             const int o = (r.x >> kOrdShift) & 255;
             if (o != wseq) {
               __syncwarp();
+              if constexpr (kSelect) {
+                if (a.arrivals != nullptr && cur_b >= 0) request_done(cur_b, cur_tiles);
+                cur_b = b;
+                cur_tiles = 0;
+#pragma unroll
+                for (int u = 0; u < C::SLOTS; ++u)
+                  thr_u[u] = t_first + u < NN ? a.thresholds[b * NN + t_first + u] : 0.0f;
+              }
               for (int q = (released + 1) & 255; q != o; q = (q + 1) & 255)
                 if (lane == 0) mbar_arrive(&q_empty[(q - 1) & 1]);
               released = (o - 1) & 255;
@@ -675,9 +748,29 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
             const bool have = (static_cast<uint32_t>(r.x) >> (kMaskShift + (pos >> bs_shift))) & 1u;
             const float scale = have ? s_scale[e_sslot * kTileTokens + pos] : 0.0f;
             const int p = r.y * kTileTokens + pos;
-            const bool store = p < s_len[b];
-            OutT *dst =
-                static_cast<OutT *>(a.out) + static_cast<int64_t>(b * NN) * a.out_stride + p;
+            const int len_b = s_len[b];
+            const bool store = p < len_b;
+            OutT *dst = nullptr;
+            if constexpr (!kSelect)
+              dst = static_cast<OutT *>(a.out) + static_cast<int64_t>(b * NN) * a.out_stride + p;
+            // Draft slot t_first + u's score at position p: stored (p < seq_lens[b]), or
+            // classified (p inside the row's extent, p < seq_lens[b] - next_n + t + 1), which
+            // the whole warp does together.
+            const auto emit = [&](int u, float logit) {
+              const int t = t_first + u;
+              if constexpr (kSelect) {
+                const int row = b * NN + t;
+                const bool valid = p + (NN - 1 - t) < len_b;
+                const float thr = thr_u[u];
+                offer(valid && logit > thr, valid && !(logit > thr) && !(logit < thr), p, logit,
+                      a.counters + 2 * row,
+                      reinterpret_cast<int2 *>(a.candidates) +
+                          static_cast<int64_t>(row) * (a.top_k + a.capacity),
+                      a.top_k, a.capacity);
+              } else {
+                if (store) store_out(dst + static_cast<int64_t>(t) * a.out_stride, logit);
+              }
+            };
             const uint32_t col0 = static_cast<uint32_t>(e_acc * C::N);
             const int nslots = min(C::SLOTS, NN - t_first);
             // The quadrant's two 16-lane windows hold positions (g, g + 8) and (g + 16, g + 24).
@@ -728,8 +821,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
                 // accumulator earlier (its release gates the MMA of tile k + ACC).
                 part[u] = make_float4(p01.x, p01.y, p23.x, p23.y);
               } else {
-                const float logit = scale * quad_reduce_scatter(p01.x, p01.y, p23.x, p23.y, c);
-                if (store) store_out(dst + static_cast<int64_t>(t) * a.out_stride, logit);
+                emit(u, scale * quad_reduce_scatter(p01.x, p01.y, p23.x, p23.y, c));
               }
             }
             if constexpr (C::SPLIT == 2) {
@@ -737,11 +829,11 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
               for (int u = 0; u < C::SLOTS; ++u) {
                 if (u >= nslots) break;
                 const float4 q = part[u];
-                const float logit = scale * quad_reduce_scatter(q.x, q.y, q.z, q.w, c);
-                if (store) store_out(dst + static_cast<int64_t>(t_first + u) * a.out_stride, logit);
+                emit(u, scale * quad_reduce_scatter(q.x, q.y, q.z, q.w, c));
               }
             }
           }
+          if constexpr (kSelect) ++cur_tiles;
           if constexpr (C::SPLIT == 1) {
             if ((e_stage += C::TEAMS) >= C::STAGES) {
               e_stage -= C::STAGES;
@@ -759,6 +851,13 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+  }
+
+  if constexpr (kSelect) {
+    // The warp's last request of the run.
+    if (warp >= kEpiWarpBase && a.arrivals != nullptr && __all_sync(0xffffffffu, ok) &&
+        cur_b >= 0)
+      request_done(cur_b, cur_tiles);
   }
 
   // ---- 3. teardown ----------------------------------------------------------------------------
@@ -832,11 +931,16 @@ cudaError_t launch_out(int next_n, const CUtensorMap &kv_map, const CUtensorMap 
 
 }  // namespace
 
-cudaError_t launch_logits_fp8(int next_n, bool out_f16, const CUtensorMap &kv_map,
+cudaError_t launch_logits_fp8(int next_n, LogitsOut mode, const CUtensorMap &kv_map,
                               const CUtensorMap &q_map, const LogitsArgs &args, int num_ctas,
                               cudaStream_t stream) {
-  return out_f16 ? launch_out<__half>(next_n, kv_map, q_map, args, num_ctas, stream)
-                 : launch_out<float>(next_n, kv_map, q_map, args, num_ctas, stream);
+  switch (mode) {
+    case LogitsOut::kF32: return launch_out<float>(next_n, kv_map, q_map, args, num_ctas, stream);
+    case LogitsOut::kF16: return launch_out<__half>(next_n, kv_map, q_map, args, num_ctas, stream);
+    case LogitsOut::kSelect:
+      return launch_out<SelectOut>(next_n, kv_map, q_map, args, num_ctas, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t logits_status(int32_t *value, bool clear) {

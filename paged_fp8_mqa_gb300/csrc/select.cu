@@ -31,6 +31,7 @@
 #include "../../include/idx.h"
 #include "internal.h"
 #include "ptx.cuh"
+#include "slots.cuh"
 
 namespace idx {
 
@@ -57,40 +58,6 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-__device__ __forceinline__ unsigned lanemask_lt() {
-  unsigned m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-
-// One warp-wide classification step: every lane offers at most one key.
-__device__ __forceinline__ void offer(bool is_cand, bool is_tie, int index, float score,
-                                      int *counter, int2 *slots, int top_k, int capacity) {
-  const int lane = threadIdx.x & 31;
-  const unsigned mc = __ballot_sync(0xffffffffu, is_cand);
-  if (mc) {
-    const int leader = __ffs(mc) - 1;
-    int base = 0;
-    if (lane == leader) base = atomicAdd(counter, __popc(mc));
-    base = __shfl_sync(0xffffffffu, base, leader);
-    if (is_cand) {
-      const int n = base + __popc(mc & lanemask_lt());
-      if (n < capacity) slots[top_k + n] = make_int2(index, __float_as_int(score));
-    }
-  }
-  const unsigned mt = __ballot_sync(0xffffffffu, is_tie);
-  if (mt) {
-    const int leader = __ffs(mt) - 1;
-    int base = 0;
-    if (lane == leader) base = atomicAdd(counter + 1, __popc(mt));
-    base = __shfl_sync(0xffffffffu, base, leader);
-    if (is_tie) {
-      const int n = base + __popc(mt & lanemask_lt());
-      if (n < top_k) slots[top_k - 1 - n] = make_int2(index, __float_as_int(score));
-    }
-  }
 }
 
 // Block-wide exclusive scan of one int per thread; returns the prefix, *total the sum.
@@ -588,6 +555,26 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
   }
 }
 
+// Repairs a row that does not fit (every thread of the CTA calls it): its slots get exactly its
+// top-K', and *c_out / *m_out / *v_out (shared) the keys above v, the keys equal to v kept, and v.
+// thr, nc, nt: the row's threshold and classification counts.
+__device__ __forceinline__ void repair_any(const float *row, int row_end, int K, float thr, int nc,
+                                           int nt, int top_k, int2 *slots, int *c_out, int *m_out,
+                                           float *v_out, uint8_t *dyn) {
+  // The threshold bounds the K'-th key from below when at least K' and at most a buffer's worth
+  // of keys were counted at or above it (NaN thresholds excepted).
+  const bool hint = thr == thr && nc + nt >= K && nc + nt <= kBufKeys;
+  if (!repair_row_gather(row, row_end, K, top_k, slots, hint, order_key(thr), c_out, m_out, v_out,
+                         dyn)) {
+    __syncthreads();
+    if (!repair_row_fast(row, row_end, K, top_k, slots, c_out, m_out, v_out, dyn)) {
+      __syncthreads();
+      repair_row(row, row_end, K, top_k, slots, c_out, m_out, v_out);
+    }
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs a) {
   // The previous kernel in the stream may still be running: no global memory before this.
   griddep_wait();
@@ -650,7 +637,7 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
     const int nt = atomicAdd(counter + 1, 0);
     s_nc = nc;
     s_nt = nt;
-    s_fits = nc <= a.capacity && (nc >= K || (nt <= a.top_k && nc + nt >= K));
+    s_fits = row_fits(nc, nt, K, a.top_k, a.capacity);
   }
   __syncthreads();
   if (s_fits) {
@@ -661,18 +648,7 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
   } else {
     __shared__ int s_c, s_m;
     __shared__ float s_v;
-    // The threshold bounds the K'-th key from below when at least K' and at most a buffer's worth
-    // of keys were counted at or above it (NaN thresholds excepted).
-    const bool hint = thr == thr && s_nc + s_nt >= K && s_nc + s_nt <= kBufKeys;
-    if (!repair_row_gather(row, row_end, K, a.top_k, slots, hint, order_key(thr), &s_c, &s_m, &s_v,
-                           select_smem)) {
-      __syncthreads();
-      if (!repair_row_fast(row, row_end, K, a.top_k, slots, &s_c, &s_m, &s_v, select_smem)) {
-        __syncthreads();
-        repair_row(row, row_end, K, a.top_k, slots, &s_c, &s_m, &s_v);
-      }
-    }
-    __syncthreads();
+    repair_any(row, row_end, K, thr, s_nc, s_nt, a.top_k, slots, &s_c, &s_m, &s_v, select_smem);
     if (tid == 0) {
       counter[0] = s_c;
       counter[1] = s_m;
@@ -682,6 +658,43 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
     }
   }
   if (tid == 0) a.arrivals[r] = 0;
+}
+
+// The repair stage of the fused score + select: CTA (b, t) for row b * next_n + t.  The fused
+// logits kernel left arrivals[b] = -next_n for every request with a row that does not fit, and
+// the rescoring launch wrote those requests' logits into the scratch rows; each such row is
+// repaired from them (rows that fit were finished by the fused kernel).  Each of the request's
+// CTAs adds one to arrivals[b] when done, so a marked request reads negative to all of them and
+// ends at zero.
+__global__ void __launch_bounds__(kThreads) k_fused_repair(const FusedRepairArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
+  extern __shared__ __align__(16) uint8_t select_smem[];
+  const int b = blockIdx.x, t = blockIdx.y;
+  if (a.arrivals[b] >= 0) return;
+  const int len = max(0, a.seq_lens[static_cast<int64_t>(b) * a.sl_stride]);
+  const int r = b * a.next_n + t;
+  const int row_end = max(0, len - a.next_n + t + 1);
+  const int K = min(row_end, a.top_k);
+  int *counter = a.counters + 2 * r;
+  const int nc = counter[0], nt = counter[1];
+  if (!row_fits(nc, nt, K, a.top_k, a.capacity)) {
+    __shared__ int s_c, s_m;
+    __shared__ float s_v;
+    int2 *slots = reinterpret_cast<int2 *>(a.candidates) +
+                  static_cast<int64_t>(r) * (a.top_k + a.capacity);
+    repair_any(a.scratch + static_cast<int64_t>(r) * a.scratch_stride, row_end, K,
+               a.thresholds[r], nc, nt, a.top_k, slots, &s_c, &s_m, &s_v, select_smem);
+    if (threadIdx.x == 0) {
+      counter[0] = s_c;
+      counter[1] = s_m;
+      a.thresholds[r] = s_v;
+      a.ranges[r] = a.top_k - s_m;
+      a.ranges[a.batch * a.next_n + r] = a.top_k + s_c;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) atomicAdd(a.arrivals + b, 1);
 }
 
 }  // namespace
@@ -697,6 +710,18 @@ cudaError_t launch_threshold_select(const SelectArgs &args, cudaStream_t stream)
     configured = true;
   }
   return launch_dependent(k_threshold_select, grid, dim3(kThreads), kSelectSmem, stream, args);
+}
+
+cudaError_t launch_fused_repair(const FusedRepairArgs &args, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        k_fused_repair, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelectSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  return launch_dependent(k_fused_repair, dim3(args.batch, args.next_n), dim3(kThreads),
+                          kSelectSmem, stream, args);
 }
 
 // ---- allocation-free variant ---------------------------------------------------------------

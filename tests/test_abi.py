@@ -105,6 +105,51 @@ def test_select_rejects_bad_arguments(lib, over, code):
     assert idx.idx_threshold_select(*a.values()) == code, idx.idx_last_error()
 
 
+def _fused_args(**over):
+    a = dict(q=FAKE, kv_fused=FAKE, num_blocks=10, block_size=64, weights=FAKE,
+             block_tables=FAKE, bt_row_stride=16, bt_width=16, seq_lens=FAKE,
+             seq_lens_stride=1, batch=2, next_n=1, num_heads=64, head_dim=128, max_seq_len=1024,
+             num_sms=4, thresholds=FAKE, counters=FAKE, candidates=FAKE, top_k=64, capacity=64,
+             arrivals=FAKE, ranges=FAKE, scratch=FAKE, scratch_row_stride=1024, stream=None)
+    a.update(over)
+    return a
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), idx.IDX_INVALID_ARG),
+    (dict(thresholds=None), idx.IDX_INVALID_ARG),
+    (dict(candidates=None), idx.IDX_INVALID_ARG),
+    (dict(batch=-1), idx.IDX_INVALID_ARG),
+    (dict(top_k=0), idx.IDX_INVALID_ARG),
+    (dict(capacity=-1), idx.IDX_INVALID_ARG),
+    (dict(capacity=10), idx.IDX_INVALID_ARG),          # < top_k - 1 with arrivals
+    (dict(ranges=None), idx.IDX_INVALID_ARG),
+    (dict(scratch=None), idx.IDX_INVALID_ARG),
+    (dict(scratch_row_stride=1000), idx.IDX_INVALID_ARG),
+    (dict(scratch_row_stride=1026), idx.IDX_INVALID_ARG),
+    (dict(scratch=P((1 << 20) + 4)), idx.IDX_INVALID_ARG),
+    (dict(candidates=P((1 << 20) + 4)), idx.IDX_INVALID_ARG),
+    (dict(num_sms=-3), idx.IDX_INVALID_ARG),
+    (dict(num_heads=32), idx.IDX_UNSUPPORTED),
+    (dict(block_size=48), idx.IDX_UNSUPPORTED),
+    (dict(next_n=5), idx.IDX_UNSUPPORTED),
+    (dict(batch=5000), idx.IDX_UNSUPPORTED),
+])
+def test_fused_rejects_bad_arguments(lib, over, code):
+    a = _fused_args(**over)
+    st = idx.idx_indexer_threshold_select(*a.values())
+    assert st == code, idx.idx_last_error()
+    assert idx.idx_last_error()
+
+
+def test_fused_accepts_missing_repair_buffers_without_arrivals(lib):
+    """Without arrivals neither ranges nor scratch is needed, and capacity may be small: with
+    batch 0 the call then succeeds without touching the GPU."""
+    a = _fused_args(arrivals=None, ranges=None, scratch=None, scratch_row_stride=0, capacity=0,
+                    batch=0)
+    assert idx.idx_indexer_threshold_select(*a.values()) == idx.IDX_OK, idx.idx_last_error()
+
+
 def test_schedule_rejects_bad_arguments(lib):
     assert idx.idx_schedule(None, 1, 4, 1, 8, FAKE, None) == idx.IDX_INVALID_ARG
     assert idx.idx_schedule(FAKE, 0, 4, 1, 8, FAKE, None) == idx.IDX_INVALID_ARG
