@@ -225,29 +225,31 @@ int idx_threshold_select_static(const float *logits, int64_t logits_row_stride,
  * each score is computed by the same arithmetic, then classified instead of stored.
  *
  * The pages' query "tile" is here one request: its next_n * 64 query-head rows are the tensor
- * core's N side, so the arrivals are counted per request (int32 [batch]).
+ * core's N side.
  *
  * Without arrivals: one launch; the rows' counts and slots only (rows that do not fit are not
  * repaired, and ranges is not written).
  * With arrivals: every row fits on return.  Three launches on `stream`, no host
  * synchronisation (capturable once run eagerly):
- *   1. the fused pass; the last of a request's tiles to finish applies the fit rule to its
- *      rows, writes their ranges, and marks the request in arrivals[b] if a row does not fit;
- *   2. the marked requests' logits recomputed into `scratch` (float32, by the same kernel;
- *      every other request counts as empty, so nothing else is read or written);
- *   3. the radix repair of idx_threshold_select for each row that does not fit, from its
- *      scratch row; arrivals[b] returns to zero.
- * When no row needs a repair, launches 2 and 3 read only seq_lens and arrivals.
+ *   1. the fused pass: every score classified into its row's slots;
+ *   2. the logits of every request with a row that does not fit (the fit rule applied to the
+ *      counts of launch 1) recomputed into `scratch` (float32, by the same kernel; every other
+ *      request counts as empty, so nothing else is read or written);
+ *   3. per row: the slot range of a row that fits, else the radix repair of
+ *      idx_threshold_select from its scratch row.
+ * When no row needs a repair, launch 2 reads only seq_lens and counters.  The follow-up
+ * launches start after the fused pass has finished, so no arrival counting is needed: arrivals
+ * is the switch that asks for the repair (as on the pages), and is neither read nor written.
  *
  * q, kv_fused, num_blocks, block_size, weights, block_tables, bt_row_stride, bt_width,
  * seq_lens, seq_lens_stride, batch, next_n, num_heads, head_dim, max_seq_len, num_sms
  *                     as for idx_logits_fp8 (the work split is always derived in the kernel)
  *   thresholds        device float32 [batch*next_n], read, and written for repaired rows
- *   counters          device int32 [batch*next_n][2] (candidates, ties), ZEROED BY THE CALLER
+ *   counters          device int32 [batch*next_n][2] (candidates, ties), ZEROED BY THE CALLER,
+ *                     8-byte aligned
  *   candidates        device int32 [batch*next_n][top_k + capacity][2], 8-byte aligned
  *   top_k, capacity   as for idx_threshold_select (capacity >= top_k - 1 with arrivals)
- *   arrivals          NULL, or device int32 [batch], zeroed once; every call leaves it zeroed
- *                     (unless a device wait timed out: see idx_device_status)
+ *   arrivals          NULL (no repair), or any non-NULL device pointer (repair); untouched
  *   ranges            device int32 [2][batch*next_n]; required with arrivals
  *   scratch           device float32, 16-byte aligned, rows of scratch_row_stride elements
  *                     (>= idx_padded_seq_len(max_seq_len), a multiple of 4); required with

@@ -270,10 +270,11 @@ def indexer_threshold_select(q, kv_fused, weights, block_tables, seq_lens, max_s
                              ranges=None, scratch=None, num_sms: int = 0, stream=None):
     """Scores and threshold select in one pass, without writing the scores.  Inputs as for
     ``logits_fp8``; rows b*next_n + t as there.  thresholds float32 [rows]; counters int32
-    [rows, 2] zeroed by the caller; candidates int32 [rows, top_k + capacity, 2].  With
-    ``arrivals`` (int32 [batch], zeroed once) every row is repaired to fit and ``ranges`` (int32
-    [2, rows]) is written; ``scratch`` (float32 [rows, >= padded_seq_len]) receives the rescored
-    rows of the requests that need the repair, and is allocated here if not given."""
+    [rows, 2] zeroed by the caller; candidates int32 [rows, top_k + capacity, 2].  Passing
+    ``arrivals`` (any int32 CUDA tensor; it is not read or written) asks for the repair: every
+    row then fits and ``ranges`` (int32 [2, rows]) is written; ``scratch`` (float32
+    [rows, >= padded_seq_len]) receives the rescored rows of the requests that need the repair,
+    and is allocated here if not given."""
     import torch
     _need(q, (torch.float8_e4m3fn, torch.uint8), "q", 4)
     _need(kv_fused, torch.uint8, "kv_fused")

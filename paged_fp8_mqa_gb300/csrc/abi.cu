@@ -276,9 +276,10 @@ IDX_EXPORT int idx_indexer_threshold_select(
   if (!aligned(q, 16) || !aligned(kv_fused, 16) || !aligned(weights, 16))
     return fail(IDX_INVALID_ARG, "q, kv_fused and weights must be 16-byte aligned");
   if (!aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(thresholds, 4) ||
-      !aligned(counters, 4) || !aligned(candidates, 8) ||
+      !aligned(counters, 8) || !aligned(candidates, 8) ||
       (arrivals != nullptr && !aligned(arrivals, 4)) || (ranges != nullptr && !aligned(ranges, 4)))
-    return fail(IDX_INVALID_ARG, "candidates must be 8-byte aligned, int32/float32 4-byte");
+    return fail(IDX_INVALID_ARG,
+                "counters and candidates must be 8-byte aligned, other int32/float32 4-byte");
   if (arrivals != nullptr) {
     if (ranges == nullptr || scratch == nullptr)
       return fail(IDX_INVALID_ARG, "ranges and scratch are required with arrivals");
@@ -321,17 +322,14 @@ IDX_EXPORT int idx_indexer_threshold_select(
   a.thresholds = thresholds;
   a.counters = counters;
   a.candidates = candidates;
-  a.arrivals = arrivals;
-  a.ranges = ranges;
   a.top_k = top_k;
   a.capacity = capacity;
-  a.repair = arrivals != nullptr ? 1 : 0;
-  // 1. Scores classified into the slots; the last arrival of each request applies the fit rule.
+  // 1. Every score classified into its row's slots.
   cudaError_t e = idx::launch_logits_fp8(next_n, idx::LogitsOut::kSelect, kv_map, q_map, a, ctas, s);
   if (e != cudaSuccess) return cuda_fail(e, "fused logits launch");
   if (arrivals == nullptr) return IDX_OK;
-  // 2. The flagged requests' scores again, this time stored (every other request counts as
-  // empty, and the work split covers only the flagged ones).
+  // 2. The scores of every request with a row that does not fit, this time stored (the other
+  // requests count as empty, and the work split covers only these).
   idx::LogitsArgs r{};
   r.kv = kv_fused;
   r.weights = weights;
@@ -345,10 +343,13 @@ IDX_EXPORT int idx_indexer_threshold_select(
   r.batch = batch;
   r.out = scratch;
   r.out_stride = scratch_row_stride;
-  r.len_mask = arrivals;
+  r.fit_counters = counters;
+  r.top_k = top_k;
+  r.capacity = capacity;
   e = idx::launch_logits_fp8(next_n, idx::LogitsOut::kF32, kv_map, q_map, r, ctas, s);
   if (e != cudaSuccess) return cuda_fail(e, "rescoring launch");
-  // 3. The radix repair of the rows that do not fit, from the rescored rows.
+  // 3. Each row's slot range, after the radix repair of a row that does not fit from its
+  // rescored logits.
   idx::FusedRepairArgs f{};
   f.scratch = scratch;
   f.scratch_stride = scratch_row_stride;
@@ -357,7 +358,6 @@ IDX_EXPORT int idx_indexer_threshold_select(
   f.thresholds = thresholds;
   f.counters = counters;
   f.candidates = candidates;
-  f.arrivals = arrivals;
   f.ranges = ranges;
   f.batch = batch;
   f.next_n = next_n;

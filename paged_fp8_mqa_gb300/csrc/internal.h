@@ -48,21 +48,16 @@ struct LogitsArgs {
   int64_t num_blocks;
   int32_t batch;
   int32_t block_size;           // tokens per page: 32, 64 or 128
-  // Rescoring (nullable): requests b with len_mask[b] >= 0 count as empty.
-  const int32_t *len_mask;
+  // Rescoring (nullable): the counts of a finished fused pass ([rows][2], 8-byte aligned); only
+  // requests with a row that does not fit (by top_k and capacity below) are scored.
+  const int32_t *fit_counters;
   // Fused select (LogitsOut::kSelect; rows b * next_n + t): the select's per-row state.
   const float *thresholds;
   int32_t *counters;            // [rows][2], zeroed by the caller
   int32_t *candidates;          // [rows][top_k + capacity][2]
-  int32_t *arrivals;            // nullable: [batch], zero on entry and on exit
-  int32_t *ranges;              // [2][rows], required with arrivals
   int32_t top_k;
   int32_t capacity;
-  int32_t repair;               // nonzero: flag requests whose rows do not fit for the repair
 };
-
-// After the fused logits kernel, arrivals[b] = -next_n marks request b as having a row that does
-// not fit; each of the request's next_n repair CTAs adds one when done, which returns it to zero.
 
 // What the logits kernel does with each score.
 enum class LogitsOut { kF32, kF16, kSelect };
@@ -93,7 +88,8 @@ struct SelectArgs {
 
 cudaError_t launch_threshold_select(const SelectArgs &args, cudaStream_t stream);
 
-// The fused score + select's repair stage: one CTA per row of each request marked in arrivals.
+// The fused score + select's last stage: one CTA per row, which writes the range of a row that
+// fits and repairs one that does not from its rescored logits.
 struct FusedRepairArgs {
   const float *scratch;    // rescored logits, row r at scratch + r * scratch_stride
   int64_t scratch_stride;
@@ -102,7 +98,6 @@ struct FusedRepairArgs {
   float *thresholds;
   int32_t *counters;
   int32_t *candidates;
-  int32_t *arrivals;
   int32_t *ranges;
   int32_t batch;
   int32_t next_n;

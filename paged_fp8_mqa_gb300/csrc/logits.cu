@@ -29,10 +29,8 @@
 //              128-byte line per output row) after multiplying by the position's scale.
 // Fused select ("flashinfer.sdsa.indexer_threshold_select": description).  Instantiated with
 // SelectOut, the epilogue classifies each score against its row's threshold into the row's
-// candidate and tie slots (slots.cuh) instead of storing it.  With arrivals, each epilogue warp
-// adds its tile count of a request to arrivals[b] when it moves on to the next request (or ends
-// its run); the warp whose addition completes the request's count applies the fit rule to the
-// request's rows.  A launch with len_mask rescores only the requests marked there.
+// candidate and tie slots (slots.cuh) instead of storing it.  A launch given fit_counters (the
+// counts of a finished fused pass) rescores only the requests with a row that does not fit.
 // Barriers.  The issuing thread is the serial point of the pipeline, so it waits on one barrier
 // and commits to one barrier per tile:
 //   full[s]   tile k may be multiplied: its TMA bytes landed (producer's expect_tx), and the
@@ -127,6 +125,31 @@ __device__ __forceinline__ void store_out(__half *p, float v) { *p = __float2hal
 // instead of being stored, each score is classified against its row's threshold into the row's
 // candidate and tie slots.
 struct SelectOut {};
+
+// A warp's candidate-slot reservation for one draft slot, whose atomicAdd result is used only at
+// the warp's next tile (or request change), so that the atomic's round trip to L2 overlaps that
+// tile's work instead of stalling the epilogue.  mask: lanes holding a candidate (warp-uniform;
+// 0 = nothing pending); base: the reserved position (leader lane only).
+struct PendingCands {
+  unsigned mask;
+  int base;
+  int row;
+  int index;
+  float score;
+};
+
+__device__ __forceinline__ void finish_cands(PendingCands &pc, int2 *candidates, int top_k,
+                                             int capacity, int lane) {
+  if (pc.mask == 0u) return;
+  const int base = __shfl_sync(0xffffffffu, pc.base, __ffs(pc.mask) - 1);
+  if ((pc.mask >> lane) & 1u) {
+    const int n = base + __popc(pc.mask & lanemask_lt());
+    if (n < capacity)
+      candidates[static_cast<int64_t>(pc.row) * (top_k + capacity) + top_k + n] =
+          make_int2(pc.index, __float_as_int(pc.score));
+  }
+  pc.mask = 0u;
+}
 
 // relu(s) * 2^-25 on the FMA pipe: a saturating multiply clamps to [0, 1] (NaN to 0), and
 // every score satisfies |s| <= 128 * 448^2 < 2^25, so the product is exact.
@@ -394,7 +417,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
     } else {
       for (int b = lane; b < a.batch; b += 32) prefetch_l2(a.seq_lens + b * a.sl_stride);
     }
-  } else if (warp == kEpiWarpBase && a.bt_width > 0 && a.len_mask == nullptr &&
+  } else if (warp == kEpiWarpBase && a.bt_width > 0 && a.fit_counters == nullptr &&
              static_cast<int64_t>(a.batch) * a.bt_width <= (int64_t{1} << 21)) {
     for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
       const int32_t *row = a.block_tables + static_cast<int64_t>(b) * a.bt_stride;
@@ -422,7 +445,17 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
     for (int b = lo; b < hi; ++b) {
       int len = __ldg(a.seq_lens + static_cast<int64_t>(b) * a.sl_stride);
       len = len < 0 ? 0 : len;
-      if (a.len_mask != nullptr && a.len_mask[b] >= 0) len = 0;  // rescoring: marked requests only
+      if (a.fit_counters != nullptr) {
+        // Rescoring: a request whose rows all fit counts as empty.
+        bool fits = true;
+#pragma unroll
+        for (int t = 0; t < NN; ++t) {
+          const int2 c = *reinterpret_cast<const int2 *>(a.fit_counters + 2 * (b * NN + t));
+          fits = fits && row_fits(c.x, c.y, min(max(0, len - NN + t + 1), a.top_k), a.top_k,
+                                  a.capacity);
+        }
+        if (fits) len = 0;
+      }
       s_len[b] = len;
       mine += tiles_of(len);
     }
@@ -458,6 +491,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
     // Start at the first tile that exists (a stale schedule or empty requests may point past it).
     const TileIter it = make_iter(s0.x, s0.y, s1.x, s1.y, batch, s_len);
     cursor = ListCursor{it.b, it.j, it.b_end, it.j_end, -1, 0};
+    if (lane == 0) *s_count = it.valid() ? 1 : 0;  // (rescoring) whether the run has a tile
     if (a.row_ends != nullptr) {
       for (int b = blockIdx.x + lane * gridDim.x; b < batch; b += 32 * gridDim.x) {
         const int len = s_len[b];
@@ -465,19 +499,14 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
         for (int t = 0; t < NN; ++t) a.row_ends[b * NN + t] = max(0, len - NN + t + 1);
       }
     }
-    if (kSelect && a.arrivals != nullptr) {
-      // An empty request has no tiles, so no arrival finishes its rows: they fit (K' = 0) with
-      // nothing stored.
-      for (int b = blockIdx.x + lane * gridDim.x; b < batch; b += 32 * gridDim.x) {
-        if (s_len[b] != 0) continue;
-#pragma unroll
-        for (int t = 0; t < NN; ++t) {
-          a.ranges[b * NN + t] = a.top_k;
-          a.ranges[batch * NN + b * NN + t] = a.top_k;
-        }
-      }
-    }
-  } else if (warp == 1) {
+  }
+  // Warp 1: barriers and TMEM.  A rescoring launch first learns whether this CTA has any tile to
+  // rescore (usually none): an empty CTA leaves here, having set up nothing.
+  if (a.fit_counters != nullptr) {
+    __syncthreads();
+    if (*s_count == 0) return;
+  }
+  if (warp == 1) {
     if (lane == 0) {
       prefetch_tensor_map(&kv_map);
       prefetch_tensor_map(&q_map);
@@ -511,40 +540,18 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   int wseq = 0;
   int released = 0;
   float2 wreg[C::SLOTS][8];
-  // (epilogue, fused select) The request being classified, this warp's tiles of it so far, and
-  // its rows' thresholds per draft slot.
-  int cur_b = -1, cur_tiles = 0;
+  // (epilogue, fused select) The thresholds of the current request's rows, per draft slot.
   float thr_u[C::SLOTS];
-
-  // (fused select) Counts this warp's `tiles` tiles of request rb toward arrivals[rb].  Every tile
-  // is read by TEAM_WARPS warps, so the warp whose arrival completes TEAM_WARPS x the request's
-  // tiles is the last, and all other warps' slot reservations are visible to it: it applies the
-  // fit rule to the request's rows, writes the range of each row that fits, and leaves
-  // arrivals[rb] = -next_n (marked for the repair launches) if a row does not, else zero.
-  const auto request_done = [&](int rb, int tiles) {
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-      const int expected = C::TEAM_WARPS * tiles_of(s_len[rb]);
-      last = atomicAdd(a.arrivals + rb, tiles) + tiles == expected;
-    }
-    if (!__shfl_sync(0xffffffffu, last, 0)) return;
-    __threadfence();
-    bool bad = false;
-    if (lane < NN) {
-      const int r = rb * NN + lane;
-      const int K = min(max(0, s_len[rb] - NN + lane + 1), a.top_k);
-      const int nc = atomicAdd(a.counters + 2 * r, 0);
-      const int nt = atomicAdd(a.counters + 2 * r + 1, 0);
-      bad = !row_fits(nc, nt, K, a.top_k, a.capacity);
-      if (!bad) {
-        a.ranges[r] = a.top_k - min(nt, a.top_k);
-        a.ranges[batch * NN + r] = a.top_k + min(nc, a.capacity);
-      }
-    }
-    const bool any = __any_sync(0xffffffffu, bad);
-    if (lane == 0) a.arrivals[rb] = any && a.repair ? -NN : 0;
+  // (fused select, one warp per lane quadrant) Each draft slot's candidate reservation of the
+  // warp's previous tile.
+  constexpr bool kDefer = kSelect && C::SPLIT == 1;
+  PendingCands pend[C::SLOTS];
+#pragma unroll
+  for (int u = 0; u < C::SLOTS; ++u) pend[u].mask = 0u;
+  const auto finish_all = [&]() {
+#pragma unroll
+    for (int u = 0; u < C::SLOTS; ++u)
+      finish_cands(pend[u], reinterpret_cast<int2 *>(a.candidates), a.top_k, a.capacity, lane);
   };
 
   for (;;) {
@@ -712,9 +719,6 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
             if (o != wseq) {
               __syncwarp();
               if constexpr (kSelect) {
-                if (a.arrivals != nullptr && cur_b >= 0) request_done(cur_b, cur_tiles);
-                cur_b = b;
-                cur_tiles = 0;
 #pragma unroll
                 for (int u = 0; u < C::SLOTS; ++u)
                   thr_u[u] = t_first + u < NN ? a.thresholds[b * NN + t_first + u] : 0.0f;
@@ -758,7 +762,28 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
             // the whole warp does together.
             const auto emit = [&](int u, float logit) {
               const int t = t_first + u;
-              if constexpr (kSelect) {
+              if constexpr (kDefer) {
+                const int row = b * NN + t;
+                const bool valid = p + (NN - 1 - t) < len_b;
+                const float thr = thr_u[u];
+                const bool is_c = valid && logit > thr;
+                finish_cands(pend[u], reinterpret_cast<int2 *>(a.candidates), a.top_k,
+                             a.capacity, lane);
+                const unsigned mc = __ballot_sync(0xffffffffu, is_c);
+                if (mc) {
+                  pend[u].mask = mc;
+                  pend[u].row = row;
+                  pend[u].index = p;
+                  pend[u].score = logit;
+                  if (lane == __ffs(mc) - 1) pend[u].base = atomicAdd(a.counters + 2 * row, __popc(mc));
+                }
+                // Ties (rare: equal scores or NaN) are reserved and stored at once.
+                offer(false, valid && !(logit > thr) && !(logit < thr), p, logit,
+                      a.counters + 2 * row,
+                      reinterpret_cast<int2 *>(a.candidates) +
+                          static_cast<int64_t>(row) * (a.top_k + a.capacity),
+                      a.top_k, a.capacity);
+              } else if constexpr (kSelect) {
                 const int row = b * NN + t;
                 const bool valid = p + (NN - 1 - t) < len_b;
                 const float thr = thr_u[u];
@@ -833,7 +858,6 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
               }
             }
           }
-          if constexpr (kSelect) ++cur_tiles;
           if constexpr (C::SPLIT == 1) {
             if ((e_stage += C::TEAMS) >= C::STAGES) {
               e_stage -= C::STAGES;
@@ -854,10 +878,8 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   }
 
   if constexpr (kSelect) {
-    // The warp's last request of the run.
-    if (warp >= kEpiWarpBase && a.arrivals != nullptr && __all_sync(0xffffffffu, ok) &&
-        cur_b >= 0)
-      request_done(cur_b, cur_tiles);
+    // The candidates still pending from the warp's last tile.
+    if (warp >= kEpiWarpBase) finish_all();
   }
 
   // ---- 3. teardown ----------------------------------------------------------------------------

@@ -108,6 +108,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
 // ---------------------------------------------------------------------------------------------
 // TMA (bulk async copies global -> shared, completing on an mbarrier)
 // ---------------------------------------------------------------------------------------------
+// ---------------------------------------------------------------------------------------------
+// Global-memory synchronisation between CTAs (no waiting)
+// ---------------------------------------------------------------------------------------------
+// Adds v at device scope with acquire-release semantics and returns the old value: the caller's
+// earlier writes (and those of warp mates ordered before it by __syncwarp) are visible to a
+// thread that later observes the sum, and the caller sees every write released before the
+// additions it observes.
+__device__ __forceinline__ int atomic_add_acq_rel(int *p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Two adjacent int32 read at L2 (bypassing L1), after an acquire that ordered them.
+__device__ __forceinline__ int2 load_l2_int2(const int *p) {
+  int2 v;
+  asm volatile("ld.global.cg.v2.s32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));

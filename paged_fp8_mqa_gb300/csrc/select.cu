@@ -660,41 +660,42 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
   if (tid == 0) a.arrivals[r] = 0;
 }
 
-// The repair stage of the fused score + select: CTA (b, t) for row b * next_n + t.  The fused
-// logits kernel left arrivals[b] = -next_n for every request with a row that does not fit, and
-// the rescoring launch wrote those requests' logits into the scratch rows; each such row is
-// repaired from them (rows that fit were finished by the fused kernel).  Each of the request's
-// CTAs adds one to arrivals[b] when done, so a marked request reads negative to all of them and
-// ends at zero.
+// The last stage of the fused score + select: CTA (b, t) for row r = b * next_n + t, after the
+// fused pass (counts and slots) and the rescoring launch (the logits of every request with a row
+// that does not fit, in the scratch rows).  A row that fits gets its slot range; one that does
+// not is repaired from its scratch row.
 __global__ void __launch_bounds__(kThreads) k_fused_repair(const FusedRepairArgs a) {
   griddep_wait();
   griddep_launch_dependents();
   extern __shared__ __align__(16) uint8_t select_smem[];
   const int b = blockIdx.x, t = blockIdx.y;
-  if (a.arrivals[b] >= 0) return;
   const int len = max(0, a.seq_lens[static_cast<int64_t>(b) * a.sl_stride]);
   const int r = b * a.next_n + t;
+  const int rows = a.batch * a.next_n;
   const int row_end = max(0, len - a.next_n + t + 1);
   const int K = min(row_end, a.top_k);
   int *counter = a.counters + 2 * r;
   const int nc = counter[0], nt = counter[1];
-  if (!row_fits(nc, nt, K, a.top_k, a.capacity)) {
-    __shared__ int s_c, s_m;
-    __shared__ float s_v;
-    int2 *slots = reinterpret_cast<int2 *>(a.candidates) +
-                  static_cast<int64_t>(r) * (a.top_k + a.capacity);
-    repair_any(a.scratch + static_cast<int64_t>(r) * a.scratch_stride, row_end, K,
-               a.thresholds[r], nc, nt, a.top_k, slots, &s_c, &s_m, &s_v, select_smem);
+  if (row_fits(nc, nt, K, a.top_k, a.capacity)) {
     if (threadIdx.x == 0) {
-      counter[0] = s_c;
-      counter[1] = s_m;
-      a.thresholds[r] = s_v;
-      a.ranges[r] = a.top_k - s_m;
-      a.ranges[a.batch * a.next_n + r] = a.top_k + s_c;
+      a.ranges[r] = a.top_k - min(nt, a.top_k);
+      a.ranges[rows + r] = a.top_k + min(nc, a.capacity);
     }
+    return;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) atomicAdd(a.arrivals + b, 1);
+  __shared__ int s_c, s_m;
+  __shared__ float s_v;
+  int2 *slots = reinterpret_cast<int2 *>(a.candidates) +
+                static_cast<int64_t>(r) * (a.top_k + a.capacity);
+  repair_any(a.scratch + static_cast<int64_t>(r) * a.scratch_stride, row_end, K, a.thresholds[r],
+             nc, nt, a.top_k, slots, &s_c, &s_m, &s_v, select_smem);
+  if (threadIdx.x == 0) {
+    counter[0] = s_c;
+    counter[1] = s_m;
+    a.thresholds[r] = s_v;
+    a.ranges[r] = a.top_k - s_m;
+    a.ranges[rows + r] = a.top_k + s_c;
+  }
 }
 
 }  // namespace

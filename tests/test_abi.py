@@ -129,6 +129,7 @@ def _fused_args(**over):
     (dict(scratch_row_stride=1026), idx.IDX_INVALID_ARG),
     (dict(scratch=P((1 << 20) + 4)), idx.IDX_INVALID_ARG),
     (dict(candidates=P((1 << 20) + 4)), idx.IDX_INVALID_ARG),
+    (dict(counters=P((1 << 20) + 4)), idx.IDX_INVALID_ARG),
     (dict(num_sms=-3), idx.IDX_INVALID_ARG),
     (dict(num_heads=32), idx.IDX_UNSUPPORTED),
     (dict(block_size=48), idx.IDX_UNSUPPORTED),
