@@ -607,6 +607,11 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
         v[u].w = 0.0f;
       }
     }
+    // The thread's candidates and ties as bit masks; one warp scan of both counts and one
+    // atomicAdd per warp and kind reserve all the warp's slots at once (a reservation per
+    // 32 keys would put a round trip to L2 on the path for each of them).
+    static_assert(kSweepLoads * 4 <= 16, "16 keys per thread fit the 16-bit counts");
+    uint32_t cm = 0, tm = 0;
 #pragma unroll
     for (int u = 0; u < kSweepLoads; ++u) {
       const int i = begin + (u * kThreads + tid) * 4;
@@ -615,9 +620,38 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
       for (int k = 0; k < 4; ++k) {
         const bool valid = i + k < end;
         const float s = e[k];
-        const bool is_cand = valid && s > thr;
-        const bool is_tie = valid && !(s > thr) && !(s < thr);
-        offer(is_cand, is_tie, i + k, s, counter, slots, a.top_k, a.capacity);
+        cm |= (valid && s > thr ? 1u : 0u) << (4 * u + k);
+        tm |= (valid && !(s > thr) && !(s < thr) ? 1u : 0u) << (4 * u + k);
+      }
+    }
+    const int lane = tid & 31;
+    const int mine = __popc(cm) | (__popc(tm) << 16);  // a warp's sums stay below 2^16
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int excl = incl - mine;
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    int bc = 0, bt = 0;
+    if (lane == 0) {
+      if (total & 0xFFFF) bc = atomicAdd(counter, total & 0xFFFF);
+      if (total >> 16) bt = atomicAdd(counter + 1, total >> 16);
+    }
+    int nc = __shfl_sync(0xffffffffu, bc, 0) + (excl & 0xFFFF);
+    int nt = __shfl_sync(0xffffffffu, bt, 0) + (excl >> 16);
+    // The few keys taken are re-read (L1 hits) rather than kept in registers.
+    for (uint32_t m = cm | tm; m != 0u; m &= m - 1u) {
+      const int bit = __ffs(m) - 1;
+      const int i = begin + ((bit >> 2) * kThreads + tid) * 4 + (bit & 3);
+      const int2 item = make_int2(i, __float_as_int(__ldg(row + i)));
+      if ((cm >> bit) & 1u) {
+        if (nc < a.capacity) slots[a.top_k + nc] = item;
+        ++nc;
+      } else {
+        if (nt < a.top_k) slots[a.top_k - 1 - nt] = item;
+        ++nt;
       }
     }
   }
