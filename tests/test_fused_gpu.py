@@ -126,8 +126,9 @@ def test_fused_full_workloads(name):
 
 @pytest.mark.parametrize("num_sms", [1, 3])
 def test_fused_runs_over_several_tile_lists(num_sms):
-    """Few CTAs: each run spans several tile lists and many requests, so every request's arrival
-    count is assembled from warps of several lists (and CTAs)."""
+    """Few CTAs: each run spans several tile lists and many requests, so a request's rows are
+    classified by warps of several lists (and CTAs), and the rescoring launch's own work split
+    covers the requests left to repair."""
     g = torch.Generator().manual_seed(77)
     lens = torch.randint(1, 700, (160,), generator=g).tolist()
     lens[5:9] = [0, 1, 2, 3]
@@ -219,3 +220,19 @@ def test_fused_graph_replay_and_repeat():
         torch.cuda.synchronize()
         assert (arrivals == 0).all()
         assert selection() == first
+
+
+@pytest.mark.parametrize("next_n", [1, 4])
+def test_fused_empty_and_short_requests(next_n):
+    """Requests with no keys at all, or fewer than next_n (some rows empty): every row fits
+    with nothing stored (K' = 0) or holds its few keys; ranges are written for all rows."""
+    for lens in ([0, 0, 0], [0, 1, 0, 2, 3]):
+        w = _small(560 + next_n + len(lens), next_n, lens, max_seq_len=256)
+        t = to_device(w)
+        logits, _ = gpu_logits(w, fill=0.0, tensors=t)
+        thr = torch.full((w.rows,), math.inf)
+        compare(w, logits, thr, 16, 15, t=t)
+        fused = gpu_fused(w, t, thr, 16, 15)
+        re = w.row_ends().numpy()
+        for r in range(w.rows):
+            assert fused["ranges"][1, r] - fused["ranges"][0, r] == min(int(re[r]), 16)
