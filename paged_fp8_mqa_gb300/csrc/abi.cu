@@ -186,10 +186,10 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
       bt_row_stride < bt_width || block_size <= 0 || num_heads <= 0 || head_dim <= 0 ||
       next_n <= 0)
     return fail(IDX_INVALID_ARG, "negative or inconsistent size or stride");
-  if (num_heads != 64 || head_dim != 128 ||
+  if ((num_heads != 32 && num_heads != 64) || head_dim != 128 ||
       (block_size != 32 && block_size != 64 && block_size != 128))
     return fail(IDX_UNSUPPORTED,
-                "this build supports num_heads 64, head_dim 128, block_size 32, 64 or 128");
+                "this build supports num_heads 32 or 64, head_dim 128, block_size 32, 64 or 128");
   if (next_n > 4) return fail(IDX_UNSUPPORTED, "next_n must be 1..4");
   if (output_dtype != IDX_DTYPE_F32 && output_dtype != IDX_DTYPE_F16)
     return fail(IDX_UNSUPPORTED, "output_dtype must be IDX_DTYPE_F32 or IDX_DTYPE_F16");
@@ -237,6 +237,7 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
   a.row_ends = row_ends_out;
   a.num_blocks = num_blocks;
   a.block_size = block_size;
+  a.num_heads = num_heads;
   a.batch = batch;
   const cudaError_t e = idx::launch_logits_fp8(
       next_n, output_dtype == IDX_DTYPE_F16 ? idx::LogitsOut::kF16 : idx::LogitsOut::kF32, kv_map,
@@ -262,10 +263,10 @@ IDX_EXPORT int idx_indexer_threshold_select(
       bt_row_stride < bt_width || block_size <= 0 || num_heads <= 0 || head_dim <= 0 ||
       next_n <= 0)
     return fail(IDX_INVALID_ARG, "negative or inconsistent size or stride");
-  if (num_heads != 64 || head_dim != 128 ||
+  if ((num_heads != 32 && num_heads != 64) || head_dim != 128 ||
       (block_size != 32 && block_size != 64 && block_size != 128))
     return fail(IDX_UNSUPPORTED,
-                "this build supports num_heads 64, head_dim 128, block_size 32, 64 or 128");
+                "this build supports num_heads 32 or 64, head_dim 128, block_size 32, 64 or 128");
   if (next_n > 4) return fail(IDX_UNSUPPORTED, "next_n must be 1..4");
   if (batch > idx::kMaxBatch) return fail(IDX_UNSUPPORTED, "batch above 4096");
   if (top_k < 1 || capacity < 0 || static_cast<int64_t>(top_k) + capacity > (INT32_MAX / 2))
@@ -318,6 +319,7 @@ IDX_EXPORT int idx_indexer_threshold_select(
   a.sl_stride = seq_lens_stride;
   a.num_blocks = num_blocks;
   a.block_size = block_size;
+  a.num_heads = num_heads;
   a.batch = batch;
   a.thresholds = thresholds;
   a.counters = counters;
@@ -340,6 +342,7 @@ IDX_EXPORT int idx_indexer_threshold_select(
   r.sl_stride = seq_lens_stride;
   r.num_blocks = num_blocks;
   r.block_size = block_size;
+  r.num_heads = num_heads;
   r.batch = batch;
   r.out = scratch;
   r.out_stride = scratch_row_stride;

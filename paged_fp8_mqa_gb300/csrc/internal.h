@@ -48,6 +48,7 @@ struct LogitsArgs {
   int64_t num_blocks;
   int32_t batch;
   int32_t block_size;           // tokens per page: 32, 64 or 128
+  int32_t num_heads;            // 32 or 64
   // Rescoring (nullable): the counts of a finished fused pass ([rows][2], 8-byte aligned); only
   // requests with a row that does not fit (by top_k and capacity below) are scored.
   const int32_t *fit_counters;

@@ -64,7 +64,6 @@ __device__ int g_logits_status;
 namespace {
 
 constexpr int kEpiWarpBase = 2;                  // epilogue warps 2, 3, ...
-constexpr int kHeads = 64;
 constexpr int kHeadDim = 128;
 constexpr uint32_t kStageBytes = kTileTokens * kHeadDim;  // 16384: a tile's values
 constexpr int kMaxList = 256;                     // tiles per tile list
@@ -74,23 +73,25 @@ constexpr int kMaskShift = 18;                    // bit 18 + p: the tile's page
 constexpr int kOrdShift = 22;                     // bits 22-29: the request's ordinal mod 256
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
 
-template <int NN>
+// next_n = NN draft slots of H heads each (H = 32 or 64).
+template <int NN, int H>
 struct Cfg {
+  static constexpr int N = NN * H;  // MMA N: query rows of one request
+  static constexpr int R = H / 8;   // head pairs a thread holds per position and slot
   // Epilogue: two teams take alternate tiles.  A team has SPLIT warps per TMEM lane quadrant;
-  // with next_n >= 3 the two warps of a quadrant share a tile's draft slots, which gives each
+  // with N >= 192 the two warps of a quadrant share a tile's draft slots, which gives each
   // scheduler four epilogue warps to hide the arithmetic's latency with.
-  static constexpr int SPLIT = NN <= 2 ? 1 : 2;
+  static constexpr int SPLIT = N <= 128 ? 1 : 2;
   static constexpr int TEAMS = 2;                       // teams taking tiles in turn
   static constexpr int TEAM_WARPS = 4 * SPLIT;          // warps reading one tile
   static constexpr int EPI_WARPS = TEAMS * TEAM_WARPS;
   static constexpr int THREADS = (kEpiWarpBase + EPI_WARPS) * 32;
   static constexpr int SLOTS = (NN + SPLIT - 1) / SPLIT;  // draft slots per epilogue warp (max)
-  static constexpr int N = NN * kHeads;  // MMA N: query rows of one request
-  static constexpr int STAGES = NN <= 2 ? 10 : (NN == 3 ? 9 : 8);
-  static constexpr int ACC = NN <= 2 ? 4 : 2;  // even: tile k's accumulator belongs to team k&1
+  static constexpr int STAGES = N <= 128 ? 10 : (N == 192 ? 9 : 8);
+  static constexpr int ACC = N <= 128 ? 4 : 2;  // even: tile k's accumulator belongs to team k&1
   static constexpr int TMEM_COLS = (ACC * N <= 256) ? 256 : 512;
   static constexpr uint32_t Q_BYTES = N * kHeadDim;
-  static constexpr uint32_t W_FLOATS = NN * kHeads;
+  static constexpr uint32_t W_FLOATS = NN * H;
   static constexpr uint32_t OFF_KV = 0;
   static constexpr uint32_t OFF_Q = OFF_KV + STAGES * kStageBytes;
   static constexpr uint32_t OFF_W = OFF_Q + 2 * Q_BYTES;
@@ -159,17 +160,19 @@ __device__ __forceinline__ float relu_scaled(float s) {
   return r;
 }
 
-// Partial logits of the two positions one 16x256b.x8 load covers (lanes g and g + 8 of its
-// window): sums over this thread's 16 heads {8r + 2c, 8r + 2c + 1 : r < 8} of w_h * max(s_h, 0)
-// in float32, the head pair of each r in one packed FMA.  Even r take the ReLU as max(s, 0) on
-// the ALU pipe, odd r as relu_scaled on the FMA pipe, which balances the two pipes; the latter's
-// sums are 2^-25 times what max(s, 0) would have produced (a power-of-two scaling commutes with
-// every rounding), so the final 2^25 rescale makes the result identical to an all-max(s, 0)
-// evaluation of the same summation order.
-__device__ __forceinline__ float2 quad_partials(const uint32_t (&v)[32], const float2 (&w)[8]) {
+// Partial logits of the two positions one 16x256b load of R 8-column chunks covers (lanes g and
+// g + 8 of its window): sums over this thread's 2R heads {8r + 2c, 8r + 2c + 1 : r < R} (of
+// H = 8R) of w_h * max(s_h, 0) in float32, the head pair of each r in one packed FMA.  Even r
+// take the ReLU as max(s, 0) on the ALU pipe, odd r as relu_scaled on the FMA pipe, which
+// balances the two pipes; the latter's sums are 2^-25 times what max(s, 0) would have produced
+// (a power-of-two scaling commutes with every rounding), so the final 2^25 rescale makes the
+// result identical to an all-max(s, 0) evaluation of the same summation order.
+template <int R>
+__device__ __forceinline__ float2 quad_partials(const uint32_t (&v)[4 * R],
+                                                const float2 (&w)[R]) {
   float2 u0 = make_float2(0.0f, 0.0f), u1 = u0, s0 = u0, s1 = u0;
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
+  for (int r = 0; r < R; ++r) {
     const float a0 = __uint_as_float(v[4 * r]), a1 = __uint_as_float(v[4 * r + 1]);
     const float b0 = __uint_as_float(v[4 * r + 2]), b1 = __uint_as_float(v[4 * r + 3]);
     if (r & 1) {
@@ -378,11 +381,11 @@ __device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const i
   return ListResult{cur, n};
 }
 
-template <int NN, typename OutT, int BS_SHIFT>
-__global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
+template <int NN, int H, typename OutT, int BS_SHIFT>
+__global__ void __launch_bounds__(Cfg<NN, H>::THREADS, 1)
     k_logits_fp8(const __grid_constant__ CUtensorMap kv_map,
                  const __grid_constant__ CUtensorMap q_map, const LogitsArgs a) {
-  using C = Cfg<NN>;
+  using C = Cfg<NN, H>;
   constexpr bool kSelect = std::is_same<OutT, SelectOut>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -539,7 +542,7 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   // this thread's heads {8r + 2c, 8r + 2c + 1} per draft slot.
   int wseq = 0;
   int released = 0;
-  float2 wreg[C::SLOTS][8];
+  float2 wreg[C::SLOTS][C::R];
   // (epilogue, fused select) The thresholds of the current request's rows, per draft slot.
   float thr_u[C::SLOTS];
   // (fused select, one warp per lane quadrant) Each draft slot's candidate reservation of the
@@ -735,8 +738,8 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
 #pragma unroll
               for (int u = 0; u < C::SLOTS; ++u)
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                  wreg[u][q] = t_first + u < NN ? w2[(t_first + u) * (kHeads / 2) + 4 * q + c]
+                for (int q = 0; q < C::R; ++q)
+                  wreg[u][q] = t_first + u < NN ? w2[(t_first + u) * (H / 2) + 4 * q + c]
                                                 : make_float2(0.0f, 0.0f);
               wseq = o;
             }
@@ -803,24 +806,24 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
             // other, so that only 32 values are live.  Without it, the next slot's loads are
             // issued before this slot's quad reduction, so the shuffles overlap their latency
             // (with the split that ordering measured slower).
-            uint32_t va[32], vb[32];
+            uint32_t va[4 * C::R], vb[4 * C::R];
             float4 part[C::SLOTS];  // (slot split) each slot's partial sums, reduced at the end
 #pragma unroll
             for (int u = 0; u < C::SLOTS; ++u) {
               if (u >= nslots) break;
               const int t = t_first + u;
-              const uint32_t col = col0 + static_cast<uint32_t>(t * kHeads);
+              const uint32_t col = col0 + static_cast<uint32_t>(t * H);
               float2 p01;
               if (C::SPLIT == 2 || u == 0) {
-                tmem_ld_16x256b_x8(lane_base + col, va);
-                if constexpr (C::SPLIT == 1) tmem_ld_16x256b_x8(lane_base + (16u << 16) + col, vb);
+                tmem_ld_16x256b<C::R>(lane_base + col, va);
+                if constexpr (C::SPLIT == 1) tmem_ld_16x256b<C::R>(lane_base + (16u << 16) + col, vb);
               }
               if constexpr (C::SPLIT == 2) {
                 tmem_ld_wait();
                 reg_fence(va);
-                p01 = quad_partials(va, wreg[u]);
+                p01 = quad_partials<C::R>(va, wreg[u]);
                 asm volatile("" : "+f"(p01.x), "+f"(p01.y));  // before the next load
-                tmem_ld_16x256b_x8(lane_base + (16u << 16) + col, vb);
+                tmem_ld_16x256b<C::R>(lane_base + (16u << 16) + col, vb);
               }
               tmem_ld_wait();
               if constexpr (C::SPLIT == 1) reg_fence(va);
@@ -832,14 +835,14 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
                 const int rel = e_stage + C::ACC;  // tile k + ACC's stage
                 if (lane == 0) mbar_arrive(&full[rel >= C::STAGES ? rel - C::STAGES : rel]);
               }
-              if constexpr (C::SPLIT == 1) p01 = quad_partials(va, wreg[u]);
-              float2 p23 = quad_partials(vb, wreg[u]);
+              if constexpr (C::SPLIT == 1) p01 = quad_partials<C::R>(va, wreg[u]);
+              float2 p23 = quad_partials<C::R>(vb, wreg[u]);
               // This slot's values are consumed before the next slot's loads reuse the registers
               // (volatile asm keeps its order).
               asm volatile("" : "+f"(p01.x), "+f"(p01.y), "+f"(p23.x), "+f"(p23.y));
               if (C::SPLIT == 1 && u + 1 < nslots) {
-                tmem_ld_16x256b_x8(lane_base + col + kHeads, va);
-                tmem_ld_16x256b_x8(lane_base + (16u << 16) + col + kHeads, vb);
+                tmem_ld_16x256b<C::R>(lane_base + col + H, va);
+                tmem_ld_16x256b<C::R>(lane_base + (16u << 16) + col + H, vb);
               }
               if constexpr (C::SPLIT == 2) {
                 // The shuffles and stores wait until every slot has been read, which frees the
@@ -911,44 +914,59 @@ __global__ void __launch_bounds__(Cfg<NN>::THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
-template <int NN, typename OutT, int BS_SHIFT>
+template <int NN, int H, typename OutT, int BS_SHIFT>
 cudaError_t launch_nn(const CUtensorMap &kv_map, const CUtensorMap &q_map, const LogitsArgs &args,
                       int num_ctas, cudaStream_t stream) {
-  using C = Cfg<NN>;
+  using C = Cfg<NN, H>;
   const uint32_t smem = C::smem_bytes(args.batch);
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_logits_fp8<NN, OutT, BS_SHIFT>,
+    cudaError_t e = cudaFuncSetAttribute(k_logits_fp8<NN, H, OutT, BS_SHIFT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::smem_bytes(kMaxBatch));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_dependent(k_logits_fp8<NN, OutT, BS_SHIFT>, dim3(num_ctas), dim3(C::THREADS), smem,
-                          stream, kv_map, q_map, args);
+  return launch_dependent(k_logits_fp8<NN, H, OutT, BS_SHIFT>, dim3(num_ctas), dim3(C::THREADS),
+                          smem, stream, kv_map, q_map, args);
 }
 
-template <typename OutT, int BS_SHIFT>
+template <int H, typename OutT, int BS_SHIFT>
 cudaError_t launch_bs(int next_n, const CUtensorMap &kv_map, const CUtensorMap &q_map,
                       const LogitsArgs &args, int num_ctas, cudaStream_t stream) {
   switch (next_n) {
-    case 1: return launch_nn<1, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
-    case 2: return launch_nn<2, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
-    case 3: return launch_nn<3, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
-    case 4: return launch_nn<4, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
+    case 1: return launch_nn<1, H, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
+    case 2: return launch_nn<2, H, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
+    case 3: return launch_nn<3, H, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
+    case 4: return launch_nn<4, H, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <typename OutT>
+template <int H, typename OutT>
 cudaError_t launch_out(int next_n, const CUtensorMap &kv_map, const CUtensorMap &q_map,
                        const LogitsArgs &args, int num_ctas, cudaStream_t stream) {
   switch (args.block_size) {
-    case 32: return launch_bs<OutT, 5>(next_n, kv_map, q_map, args, num_ctas, stream);
-    case 64: return launch_bs<OutT, 6>(next_n, kv_map, q_map, args, num_ctas, stream);
-    case 128: return launch_bs<OutT, 7>(next_n, kv_map, q_map, args, num_ctas, stream);
+    case 32: return launch_bs<H, OutT, 5>(next_n, kv_map, q_map, args, num_ctas, stream);
+    case 64: return launch_bs<H, OutT, 6>(next_n, kv_map, q_map, args, num_ctas, stream);
+    case 128: return launch_bs<H, OutT, 7>(next_n, kv_map, q_map, args, num_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+template <int H>
+cudaError_t launch_heads(int next_n, LogitsOut mode, const CUtensorMap &kv_map,
+                         const CUtensorMap &q_map, const LogitsArgs &args, int num_ctas,
+                         cudaStream_t stream) {
+  switch (mode) {
+    case LogitsOut::kF32:
+      return launch_out<H, float>(next_n, kv_map, q_map, args, num_ctas, stream);
+    case LogitsOut::kF16:
+      return launch_out<H, __half>(next_n, kv_map, q_map, args, num_ctas, stream);
+    case LogitsOut::kSelect:
+      return launch_out<H, SelectOut>(next_n, kv_map, q_map, args, num_ctas, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -956,13 +974,11 @@ cudaError_t launch_out(int next_n, const CUtensorMap &kv_map, const CUtensorMap 
 cudaError_t launch_logits_fp8(int next_n, LogitsOut mode, const CUtensorMap &kv_map,
                               const CUtensorMap &q_map, const LogitsArgs &args, int num_ctas,
                               cudaStream_t stream) {
-  switch (mode) {
-    case LogitsOut::kF32: return launch_out<float>(next_n, kv_map, q_map, args, num_ctas, stream);
-    case LogitsOut::kF16: return launch_out<__half>(next_n, kv_map, q_map, args, num_ctas, stream);
-    case LogitsOut::kSelect:
-      return launch_out<SelectOut>(next_n, kv_map, q_map, args, num_ctas, stream);
+  switch (args.num_heads) {
+    case 32: return launch_heads<32>(next_n, mode, kv_map, q_map, args, num_ctas, stream);
+    case 64: return launch_heads<64>(next_n, mode, kv_map, q_map, args, num_ctas, stream);
+    default: return cudaErrorInvalidValue;
   }
-  return cudaErrorInvalidValue;
 }
 
 cudaError_t logits_status(int32_t *value, bool clear) {

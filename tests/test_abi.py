@@ -69,7 +69,8 @@ def _logits_args(**over):
     (dict(out_row_stride=1026), idx.IDX_INVALID_ARG),
     (dict(q=P((1 << 20) + 4)), idx.IDX_INVALID_ARG),
     (dict(num_sms=-3), idx.IDX_INVALID_ARG),
-    (dict(num_heads=32), idx.IDX_UNSUPPORTED),
+    (dict(num_heads=48), idx.IDX_UNSUPPORTED),
+    (dict(num_heads=16), idx.IDX_UNSUPPORTED),
     (dict(head_dim=64), idx.IDX_UNSUPPORTED),
     (dict(block_size=48), idx.IDX_UNSUPPORTED),
     (dict(block_size=256), idx.IDX_UNSUPPORTED),
@@ -131,7 +132,8 @@ def _fused_args(**over):
     (dict(candidates=P((1 << 20) + 4)), idx.IDX_INVALID_ARG),
     (dict(counters=P((1 << 20) + 4)), idx.IDX_INVALID_ARG),
     (dict(num_sms=-3), idx.IDX_INVALID_ARG),
-    (dict(num_heads=32), idx.IDX_UNSUPPORTED),
+    (dict(num_heads=48), idx.IDX_UNSUPPORTED),
+    (dict(num_heads=16), idx.IDX_UNSUPPORTED),
     (dict(block_size=48), idx.IDX_UNSUPPORTED),
     (dict(next_n=5), idx.IDX_UNSUPPORTED),
     (dict(batch=5000), idx.IDX_UNSUPPORTED),

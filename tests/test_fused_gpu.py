@@ -67,10 +67,10 @@ def compare(w, logits, thr, top_k, capacity, num_sms=0, t=None):
     return repaired
 
 
-def _small(seed, next_n, lens, block_size=64, max_seq_len=None):
+def _small(seed, next_n, lens, block_size=64, max_seq_len=None, num_heads=64):
     m = max_seq_len or max(max(lens), 1)
     return synth.make_workload("edge", seed, len(lens), next_n, m, "fixed", values=list(lens),
-                               block_size=block_size)
+                               block_size=block_size, num_heads=num_heads)
 
 
 def _threshold_variants(lc, re, top_k, seed):
@@ -236,3 +236,13 @@ def test_fused_empty_and_short_requests(next_n):
         re = w.row_ends().numpy()
         for r in range(w.rows):
             assert fused["ranges"][1, r] - fused["ranges"][0, r] == min(int(re[r]), 16)
+
+
+@pytest.mark.parametrize("next_n", [1, 2, 4])
+def test_fused_32_heads(next_n):
+    w = _small(570 + next_n, next_n, [4000, 3, 0, 900, 7000], num_heads=32)
+    t = to_device(w)
+    logits, _ = gpu_logits(w, fill=0.0, tensors=t)
+    lc = logits.cpu().numpy()
+    for thr in _threshold_variants(lc, w.row_ends().numpy(), 64, seed=next_n).values():
+        compare(w, logits, thr, 64, 63, t=t)

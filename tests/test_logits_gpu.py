@@ -135,6 +135,41 @@ def test_many_short_requests_over_several_tile_lists(next_n):
         check_logits(w, got, ref, tol)
 
 
+HEADS32 = [
+    (1, 64, [5000, 1, 0, 777, 129, 64, 65]),
+    (2, 32, [3000, 0, 2, 31, 33, 9000]),
+    (3, 128, [2500, 3, 2, 0, 127, 129, 6000]),
+    (4, 64, [4000, 4, 3, 100, 0, 8191, 8193]),
+]
+
+
+@pytest.mark.parametrize("next_n,block_size,lens", HEADS32,
+                         ids=[f"n{n}-bs{b}" for n, b, _ in HEADS32])
+def test_32_heads(next_n, block_size, lens):
+    """num_heads = 32: MMA N = 32 * next_n, a thread holds 8 of the heads per slot."""
+    w = _small(320 + next_n, next_n, lens, num_heads=32, block_size=block_size)
+    ref, tol = _oracle(w)
+    got, row_ends = gpu_logits(w)
+    check_logits(w, got, ref, tol)
+    assert (row_ends.cpu() == w.row_ends()).all()
+
+
+def test_32_heads_long_runs_and_float16():
+    """num_heads = 32 over runs of several tile lists (one CTA), and with float16 output."""
+    g = torch.Generator().manual_seed(32)
+    lens = torch.randint(1, 900, (120,), generator=g).tolist()
+    w = _small(330, 2, lens, num_heads=32)
+    ref, tol = _oracle(w)
+    got, _ = gpu_logits(w, num_sms=1)
+    check_logits(w, got, ref, tol)
+    t = to_device(w)
+    out = torch.full((w.rows, idx.idx_padded_seq_len(w.max_seq_len)), float("nan"),
+                     dtype=torch.float16, device="cuda")
+    idx.logits_fp8(t["q"], t["kv"], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len, out=out)
+    torch.cuda.synchronize()
+    _check_float16(w, out, ref, tol)
+
+
 def test_stale_schedule_terminates():
     """A schedule computed for other lengths gives wrong coverage but no hang, no fault and no
     read past any request's pages."""
