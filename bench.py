@@ -113,7 +113,8 @@ class ClockSampler:
 
 
 # Sources compiled into the logits kernel: the committed traffic figures hold only for them.
-KERNEL_SOURCES = ("logits.cu", "ptx.cuh", "split.cuh", "slots.cuh", "internal.h")
+KERNEL_SOURCES = ("logits.cu", "logits_kernel.cuh", "ptx.cuh", "split.cuh", "slots.cuh",
+                  "internal.h")
 
 
 def kernel_sources_digest() -> str:

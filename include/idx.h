@@ -121,7 +121,8 @@ int idx_schedule(const int32_t *seq_lens, int64_t seq_lens_stride, int32_t batch
  *   batch           0 .. 4096
  *   next_n          1 .. 4 (draft depth; slot t = next_n - 1 is the newest and sees the whole
  *                   sequence)
- *   num_heads, head_dim   this build supports 32 or 64 heads of 128 (IDX_UNSUPPORTED else)
+ *   num_heads, head_dim   this build supports 32 or 64 heads of 64 or 128 (IDX_UNSUPPORTED
+ *                   else); kv_fused blocks are then block_size*(head_dim+4) bytes
  *   block_size      32, 64 or 128 tokens per block (IDX_UNSUPPORTED else)
  *   max_seq_len     >= every seq_lens[b]
  *   schedule        device int32 [num_sms+1][2] from idx_schedule with the same seq_lens and

@@ -52,20 +52,21 @@ EncodeTiled encode_tiled() {
   return fn;
 }
 
-// A 2-D uint8 tensor of `rows` rows of 128 bytes, `row_bytes` apart, read in boxes of
-// `box_rows` rows with the 128-byte swizzle (the layout the tensor core's descriptors expect).
-int encode_rows128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t row_bytes,
-                   uint32_t box_rows) {
+// A 2-D uint8 tensor of `rows` rows of `row_bytes` = 128 or 64 bytes (one e4m3 row of head_dim
+// elements), read in boxes of `box_rows` rows with the 128- or 64-byte swizzle: the layout the
+// tensor core's descriptors expect.
+int encode_rows(CUtensorMap *map, const void *base, uint64_t rows, uint32_t row_bytes,
+                uint32_t box_rows) {
   EncodeTiled fn = encode_tiled();
   if (fn == nullptr) return fail(IDX_CUDA, "cuTensorMapEncodeTiled is not available");
-  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t dims[2] = {row_bytes, rows};
   const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t box[2] = {row_bytes, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(IDX_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
   return IDX_OK;
@@ -186,10 +187,10 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
       bt_row_stride < bt_width || block_size <= 0 || num_heads <= 0 || head_dim <= 0 ||
       next_n <= 0)
     return fail(IDX_INVALID_ARG, "negative or inconsistent size or stride");
-  if ((num_heads != 32 && num_heads != 64) || head_dim != 128 ||
+  if ((num_heads != 32 && num_heads != 64) || (head_dim != 64 && head_dim != 128) ||
       (block_size != 32 && block_size != 64 && block_size != 128))
-    return fail(IDX_UNSUPPORTED,
-                "this build supports num_heads 32 or 64, head_dim 128, block_size 32, 64 or 128");
+    return fail(IDX_UNSUPPORTED, "this build supports num_heads 32 or 64, head_dim 64 or 128, "
+                                 "block_size 32, 64 or 128");
   if (next_n > 4) return fail(IDX_UNSUPPORTED, "next_n must be 1..4");
   if (output_dtype != IDX_DTYPE_F32 && output_dtype != IDX_DTYPE_F16)
     return fail(IDX_UNSUPPORTED, "output_dtype must be IDX_DTYPE_F32 or IDX_DTYPE_F16");
@@ -198,7 +199,7 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
     return fail(IDX_INVALID_ARG,
                 "out_row_stride must be >= idx_padded_seq_len(max_seq_len) and a multiple of 4");
   const int64_t page_bytes = static_cast<int64_t>(block_size) * (head_dim + 4);
-  if (num_blocks > (INT64_C(1) << 31) / (page_bytes / 128) - 1)
+  if (num_blocks > (INT64_C(1) << 31) / (page_bytes / head_dim) - 1)
     return fail(IDX_INVALID_ARG, "num_blocks too large for 32-bit TMA row coordinates");
   if (!aligned(q, 16) || !aligned(kv_fused, 16) || !aligned(weights, 16) || !aligned(out, 16))
     return fail(IDX_INVALID_ARG, "q, kv_fused, weights and out must be 16-byte aligned");
@@ -217,11 +218,12 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
     if (st != IDX_OK) return st;
   }
   CUtensorMap kv_map, q_map;
-  st = encode_rows128(&kv_map, kv_fused, static_cast<uint64_t>(num_blocks) * (page_bytes / 128),
-                      128, static_cast<uint32_t>(block_size));
+  st = encode_rows(&kv_map, kv_fused,
+                   static_cast<uint64_t>(num_blocks) * (page_bytes / head_dim),
+                   static_cast<uint32_t>(head_dim), static_cast<uint32_t>(block_size));
   if (st != IDX_OK) return st;
-  st = encode_rows128(&q_map, q, static_cast<uint64_t>(batch) * next_n * num_heads, 128,
-                      static_cast<uint32_t>(next_n * num_heads));
+  st = encode_rows(&q_map, q, static_cast<uint64_t>(batch) * next_n * num_heads,
+                   static_cast<uint32_t>(head_dim), static_cast<uint32_t>(next_n * num_heads));
   if (st != IDX_OK) return st;
   idx::LogitsArgs a{};
   a.kv = kv_fused;
@@ -238,6 +240,7 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.num_heads = num_heads;
+  a.head_dim = head_dim;
   a.batch = batch;
   const cudaError_t e = idx::launch_logits_fp8(
       next_n, output_dtype == IDX_DTYPE_F16 ? idx::LogitsOut::kF16 : idx::LogitsOut::kF32, kv_map,
@@ -263,16 +266,16 @@ IDX_EXPORT int idx_indexer_threshold_select(
       bt_row_stride < bt_width || block_size <= 0 || num_heads <= 0 || head_dim <= 0 ||
       next_n <= 0)
     return fail(IDX_INVALID_ARG, "negative or inconsistent size or stride");
-  if ((num_heads != 32 && num_heads != 64) || head_dim != 128 ||
+  if ((num_heads != 32 && num_heads != 64) || (head_dim != 64 && head_dim != 128) ||
       (block_size != 32 && block_size != 64 && block_size != 128))
-    return fail(IDX_UNSUPPORTED,
-                "this build supports num_heads 32 or 64, head_dim 128, block_size 32, 64 or 128");
+    return fail(IDX_UNSUPPORTED, "this build supports num_heads 32 or 64, head_dim 64 or 128, "
+                                 "block_size 32, 64 or 128");
   if (next_n > 4) return fail(IDX_UNSUPPORTED, "next_n must be 1..4");
   if (batch > idx::kMaxBatch) return fail(IDX_UNSUPPORTED, "batch above 4096");
   if (top_k < 1 || capacity < 0 || static_cast<int64_t>(top_k) + capacity > (INT32_MAX / 2))
     return fail(IDX_INVALID_ARG, "top_k >= 1 and capacity >= 0 required");
   const int64_t page_bytes = static_cast<int64_t>(block_size) * (head_dim + 4);
-  if (num_blocks > (INT64_C(1) << 31) / (page_bytes / 128) - 1)
+  if (num_blocks > (INT64_C(1) << 31) / (page_bytes / head_dim) - 1)
     return fail(IDX_INVALID_ARG, "num_blocks too large for 32-bit TMA row coordinates");
   if (!aligned(q, 16) || !aligned(kv_fused, 16) || !aligned(weights, 16))
     return fail(IDX_INVALID_ARG, "q, kv_fused and weights must be 16-byte aligned");
@@ -303,11 +306,12 @@ IDX_EXPORT int idx_indexer_threshold_select(
     if (st != IDX_OK) return st;
   }
   CUtensorMap kv_map, q_map;
-  st = encode_rows128(&kv_map, kv_fused, static_cast<uint64_t>(num_blocks) * (page_bytes / 128),
-                      128, static_cast<uint32_t>(block_size));
+  st = encode_rows(&kv_map, kv_fused,
+                   static_cast<uint64_t>(num_blocks) * (page_bytes / head_dim),
+                   static_cast<uint32_t>(head_dim), static_cast<uint32_t>(block_size));
   if (st != IDX_OK) return st;
-  st = encode_rows128(&q_map, q, static_cast<uint64_t>(batch) * next_n * num_heads, 128,
-                      static_cast<uint32_t>(next_n * num_heads));
+  st = encode_rows(&q_map, q, static_cast<uint64_t>(batch) * next_n * num_heads,
+                   static_cast<uint32_t>(head_dim), static_cast<uint32_t>(next_n * num_heads));
   if (st != IDX_OK) return st;
   idx::LogitsArgs a{};
   a.kv = kv_fused;
@@ -320,6 +324,7 @@ IDX_EXPORT int idx_indexer_threshold_select(
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.num_heads = num_heads;
+  a.head_dim = head_dim;
   a.batch = batch;
   a.thresholds = thresholds;
   a.counters = counters;
@@ -343,6 +348,7 @@ IDX_EXPORT int idx_indexer_threshold_select(
   r.num_blocks = num_blocks;
   r.block_size = block_size;
   r.num_heads = num_heads;
+  r.head_dim = head_dim;
   r.batch = batch;
   r.out = scratch;
   r.out_stride = scratch_row_stride;

@@ -49,6 +49,7 @@ struct LogitsArgs {
   int32_t batch;
   int32_t block_size;           // tokens per page: 32, 64 or 128
   int32_t num_heads;            // 32 or 64
+  int32_t head_dim;             // 128 or 64
   // Rescoring (nullable): the counts of a finished fused pass ([rows][2], 8-byte aligned); only
   // requests with a row that does not fit (by top_k and capacity below) are scored.
   const int32_t *fit_counters;
@@ -67,6 +68,12 @@ enum class LogitsOut { kF32, kF16, kSelect };
 cudaError_t launch_logits_fp8(int next_n, LogitsOut mode, const CUtensorMap &kv_map,
                               const CUtensorMap &q_map, const LogitsArgs &args, int num_ctas,
                               cudaStream_t stream);
+
+// The head_dim 64 instantiations (a separate translation unit) and their status bits.
+cudaError_t launch_logits_d64(int next_n, LogitsOut mode, const CUtensorMap &kv_map,
+                              const CUtensorMap &q_map, const LogitsArgs &args, int num_ctas,
+                              cudaStream_t stream);
+cudaError_t logits_d64_status(int32_t *value, bool clear);
 
 // Launches the standalone schedule kernel.
 cudaError_t launch_schedule(const int32_t *seq_lens, int64_t stride, int batch, int num_ctas,

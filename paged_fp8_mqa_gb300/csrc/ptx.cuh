@@ -241,6 +241,28 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for rows of 64 bytes stored with the 64-byte swizzle: 8-row atoms 512 bytes apart,
+// layout type 4 = 64-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1u) << 16;
+  d |= static_cast<uint64_t>(512u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(4u) << 61;
+  return d;
+}
+
+// The descriptor for K-major rows of ROW_BYTES = 128 or 64 bytes (one swizzle atom wide).
+template <int ROW_BYTES>
+__device__ __forceinline__ uint64_t smem_desc_rows(uint32_t saddr) {
+  static_assert(ROW_BYTES == 128 || ROW_BYTES == 64, "128- or 64-byte swizzled rows");
+  if constexpr (ROW_BYTES == 128)
+    return smem_desc_sw128(saddr);
+  else
+    return smem_desc_sw64(saddr);
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f8f6f4 with A, B = E4M3 (format 0), both
 // K-major, D = float32: D format (bits 4-5) = 1, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t m, uint32_t n) {

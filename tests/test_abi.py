@@ -71,7 +71,8 @@ def _logits_args(**over):
     (dict(num_sms=-3), idx.IDX_INVALID_ARG),
     (dict(num_heads=48), idx.IDX_UNSUPPORTED),
     (dict(num_heads=16), idx.IDX_UNSUPPORTED),
-    (dict(head_dim=64), idx.IDX_UNSUPPORTED),
+    (dict(head_dim=96), idx.IDX_UNSUPPORTED),
+    (dict(head_dim=256), idx.IDX_UNSUPPORTED),
     (dict(block_size=48), idx.IDX_UNSUPPORTED),
     (dict(block_size=256), idx.IDX_UNSUPPORTED),
     (dict(next_n=5), idx.IDX_UNSUPPORTED),

@@ -67,10 +67,10 @@ def compare(w, logits, thr, top_k, capacity, num_sms=0, t=None):
     return repaired
 
 
-def _small(seed, next_n, lens, block_size=64, max_seq_len=None, num_heads=64):
+def _small(seed, next_n, lens, block_size=64, max_seq_len=None, num_heads=64, head_dim=128):
     m = max_seq_len or max(max(lens), 1)
     return synth.make_workload("edge", seed, len(lens), next_n, m, "fixed", values=list(lens),
-                               block_size=block_size, num_heads=num_heads)
+                               block_size=block_size, num_heads=num_heads, head_dim=head_dim)
 
 
 def _threshold_variants(lc, re, top_k, seed):
@@ -241,6 +241,17 @@ def test_fused_empty_and_short_requests(next_n):
 @pytest.mark.parametrize("next_n", [1, 2, 4])
 def test_fused_32_heads(next_n):
     w = _small(570 + next_n, next_n, [4000, 3, 0, 900, 7000], num_heads=32)
+    t = to_device(w)
+    logits, _ = gpu_logits(w, fill=0.0, tensors=t)
+    lc = logits.cpu().numpy()
+    for thr in _threshold_variants(lc, w.row_ends().numpy(), 64, seed=next_n).values():
+        compare(w, logits, thr, 64, 63, t=t)
+
+
+@pytest.mark.parametrize("next_n,heads", [(1, 64), (4, 64), (2, 32)])
+def test_fused_head_dim_64(next_n, heads):
+    w = _small(580 + next_n + heads, next_n, [4000, 3, 0, 900, 7000], num_heads=heads,
+               head_dim=64)
     t = to_device(w)
     logits, _ = gpu_logits(w, fill=0.0, tensors=t)
     lc = logits.cpu().numpy()

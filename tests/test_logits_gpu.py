@@ -170,6 +170,43 @@ def test_32_heads_long_runs_and_float16():
     _check_float16(w, out, ref, tol)
 
 
+DIM64 = [
+    (1, 64, 64, [5000, 1, 0, 777, 129, 64, 65]),
+    (2, 64, 32, [3000, 0, 2, 31, 33, 9000]),
+    (3, 64, 128, [2500, 3, 2, 0, 127, 129, 6000]),
+    (4, 64, 64, [4000, 4, 3, 100, 0, 8191, 8193]),
+    (2, 32, 64, [3000, 1, 0, 200, 7000]),
+    (4, 32, 128, [2000, 4, 0, 129, 5000]),
+]
+
+
+@pytest.mark.parametrize("next_n,heads,block_size,lens", DIM64,
+                         ids=[f"n{n}-h{h}-bs{b}" for n, h, b, _ in DIM64])
+def test_head_dim_64(next_n, heads, block_size, lens):
+    """head_dim = 64: rows of 64 bytes, 64-byte swizzle, two K = 32 MMAs per tile."""
+    w = _small(340 + next_n + heads, next_n, lens, num_heads=heads, head_dim=64,
+               block_size=block_size)
+    ref, tol = _oracle(w)
+    got, row_ends = gpu_logits(w)
+    check_logits(w, got, ref, tol)
+    assert (row_ends.cpu() == w.row_ends()).all()
+
+
+def test_head_dim_64_long_runs_and_float16():
+    g = torch.Generator().manual_seed(64)
+    lens = torch.randint(1, 900, (120,), generator=g).tolist()
+    w = _small(350, 3, lens, head_dim=64)
+    ref, tol = _oracle(w)
+    got, _ = gpu_logits(w, num_sms=1)
+    check_logits(w, got, ref, tol)
+    t = to_device(w)
+    out = torch.full((w.rows, idx.idx_padded_seq_len(w.max_seq_len)), float("nan"),
+                     dtype=torch.float16, device="cuda")
+    idx.logits_fp8(t["q"], t["kv"], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len, out=out)
+    torch.cuda.synchronize()
+    _check_float16(w, out, ref, tol)
+
+
 def test_stale_schedule_terminates():
     """A schedule computed for other lengths gives wrong coverage but no hang, no fault and no
     read past any request's pages."""
