@@ -5,7 +5,8 @@ ctypes.  Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
 may import this package; the product path never does, and the two share no code.
 
 Sources restated (see ``oracle.c`` for the passage each function follows):
-  * "flashinfer.attn_scores" -- fp8_paged_mqa_logits (formula, Note, Parameters, helpers).
+  * "flashinfer.attn_scores" -- fp8_paged_mqa_logits (formula, Note, Parameters, helpers) and
+    fp4_paged_mqa_logits (formula, Parameters q, q_sf, kv_fused).
   * "flashinfer.sdsa.indexer_threshold_select" -- description and Parameters.
 """
 from __future__ import annotations
@@ -74,6 +75,14 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
     lib.oracle_paged_logits.argtypes = [P, P, c.c_int64, c.c_int, P, P, c.c_int64, c.c_int64, P,
                                         c.c_int64, c.c_int, c.c_int, c.c_int, c.c_int, P,
                                         c.c_int64, c.c_int64, P, c.c_int]
+    lib.oracle_e2m1_to_double.restype = c.c_double
+    lib.oracle_e2m1_to_double.argtypes = [c.c_uint8]
+    lib.oracle_ue8m0_to_double.restype = c.c_double
+    lib.oracle_ue8m0_to_double.argtypes = [c.c_uint8]
+    lib.oracle_paged_logits_mxfp4.restype = c.c_int
+    lib.oracle_paged_logits_mxfp4.argtypes = [P, P, P, c.c_int64, c.c_int, P, P, c.c_int64,
+                                              c.c_int64, P, c.c_int64, c.c_int, c.c_int, c.c_int,
+                                              c.c_int, P, c.c_int64, c.c_int64, P, c.c_int]
     lib.oracle_total_order_cmp.restype = c.c_int
     lib.oracle_total_order_cmp.argtypes = [c.c_float, c.c_float]
     lib.oracle_topk.restype = c.c_int
@@ -155,6 +164,48 @@ def paged_logits(q_u8, kv_fused_u8, weights, block_tables, seq_lens, max_seq_len
                                  cols, cols, _ptr(tol) if with_tol else None, nthreads)
     if st != OK:
         raise OracleError(f"oracle_paged_logits returned {st}")
+    return out, tol
+
+
+def e2m1_to_double(nibble: int, lib=None) -> float:
+    return float((lib or load()).oracle_e2m1_to_double(nibble))
+
+
+def ue8m0_to_double(e: int, lib=None) -> float:
+    return float((lib or load()).oracle_ue8m0_to_double(e))
+
+
+def paged_logits_mxfp4(q_u8, q_sf_u8, kv_fused_u8, weights, block_tables, seq_lens,
+                       max_seq_len: int, *, block_size: int, out_cols: int | None = None,
+                       fill=np.nan, with_tol: bool = True, nthreads: int = 0, lib=None):
+    """Float64 MXFP4 logits and tolerance magnitudes.
+
+    q_u8: uint8 [B, next_n, H, D/2] (packed E2M1); q_sf_u8: uint8 [B, next_n, H, D/32] (UE8M0);
+    kv_fused_u8: uint8 [num_blocks, ...] whose rows are block_size*(D/2 + D/32) bytes; weights:
+    float32 [B*next_n, H]; block_tables int32 [B, W]; seq_lens int32 [B].
+    Returns (logits, tol), float64 [B*next_n, out_cols], entries outside extents = ``fill``.
+    """
+    lib = lib or load()
+    q = _np(q_u8)
+    qsf = _np(q_sf_u8)
+    kv = _np(kv_fused_u8)
+    w = _np(weights).astype(np.float32, copy=False)
+    bt = _np(block_tables).astype(np.int32, copy=False)
+    sl = _np(seq_lens).astype(np.int32, copy=False)
+    B, n, H, half = q.shape
+    D = 2 * half
+    assert qsf.shape == (B, n, H, D // 32), "q_sf shape"
+    num_blocks = kv.shape[0]
+    assert kv.reshape(num_blocks, -1).shape[1] == block_size * (D // 2 + D // 32), "block size"
+    cols = out_cols if out_cols is not None else padded_seq_len(max_seq_len, lib)
+    out = np.full((B * n, cols), fill, dtype=np.float64)
+    tol = np.full((B * n, cols), fill, dtype=np.float64) if with_tol else None
+    st = lib.oracle_paged_logits_mxfp4(_ptr(q), _ptr(qsf), _ptr(kv), num_blocks, block_size,
+                                       _ptr(w), _ptr(bt), bt.shape[1], bt.shape[1], _ptr(sl), 1,
+                                       B, n, H, D, _ptr(out), cols, cols,
+                                       _ptr(tol) if with_tol else None, nthreads)
+    if st != OK:
+        raise OracleError(f"oracle_paged_logits_mxfp4 returned {st}")
     return out, tol
 
 

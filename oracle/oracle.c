@@ -10,6 +10,8 @@
  *   [scores]  "flashinfer.attn_scores" -- fp8_paged_mqa_logits: the formula block, the Note on
  *             per-slot extents, and the Parameters list (q, kv_fused, weights, block_tables,
  *             seq_lens, out).
+ *   [fp4]     "flashinfer.attn_scores" -- fp4_paged_mqa_logits: the formula block and the
+ *             Parameters list (q, q_sf, kv_fused with its byte-offset drawing, sf_vec_size).
  *   [select]  "flashinfer.sdsa.indexer_threshold_select" -- the description (candidate / tie
  *             classification, fit rule, repair) and the Parameters list (row_ends,
  *             thresholds, counters, candidates, arrivals, ranges).
@@ -208,6 +210,149 @@ int oracle_paged_logits(const uint8_t *q, const uint8_t *kv_fused, int64_t num_b
                 }
                 out[r * out_row_stride + p] = scale * weighted;
                 if (tol) tol[r * out_row_stride + p] = fabs(scale) * magnitude;
+            }
+        }
+        free(kd);
+    }
+    free(qd);
+    return status;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* MXFP4 paged MQA logits                                                                      */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * OCP microscaling FP4 element, E2M1 ([fp4] Parameters: q, "Two FP4 (E2M1) values packed per
+ * byte"): 1 sign bit, 2 exponent bits with bias 1, 1 mantissa bit; exponent field 0 encodes the
+ * subnormal m/2; there are no infinities and no NaN.  Magnitudes: 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+ */
+double oracle_e2m1_to_double(uint8_t nibble) {
+    const int sign = (nibble >> 3) & 1;
+    const int exponent = (nibble >> 1) & 3;
+    const int mantissa = nibble & 1;
+    const double magnitude = exponent == 0 ? 0.5 * mantissa
+                                           : ldexp(1.0 + 0.5 * mantissa, exponent - 1);
+    return sign ? -magnitude : magnitude;
+}
+
+/* A UE8M0 scale factor ([fp4] Parameters: q_sf, "the raw float32 exponent byte"): 2^(e - 127);
+ * the all-ones byte is NaN in the OCP microscaling formats. */
+double oracle_ue8m0_to_double(uint8_t e) { return e == 0xFF ? NAN : ldexp(1.0, (int)e - 127); }
+
+/*
+ * logits[b*next_n + t, p] = sum_h w[b*next_n + t, h] * relu(q[b,t,h,:] . k[p,:])
+ * ([fp4] formula block), with every element dequantized: element d of a head_dim-long row is
+ * e2m1(its nibble) * ue8m0(the row's scale byte d / 32) (sf_vec_size = 32).  There is no
+ * per-position factor: the block scales are part of the values ([fp4] description).
+ *
+ * Layouts ([fp4] Parameters): a row of head_dim elements is head_dim/2 bytes, byte j holding
+ * element 2j in its low nibble and element 2j+1 in its high nibble; q is [batch, next_n,
+ * num_heads, head_dim/2] bytes; q_sf is [batch, next_n, num_heads, head_dim/32] bytes (the
+ * little-endian bytes of the pages' int32 view: byte k scales elements [32k, 32k + 32)); a
+ * kv_fused block is block_size*(head_dim/2 + head_dim/32) bytes: the packed rows token-major
+ * (token i at i*head_dim/2), then head_dim/32 scale bytes per token (token i's at
+ * block_size*head_dim/2 + (head_dim/32)*i).  Extents, paging and the untouched entries are as
+ * in oracle_paged_logits; tol = sum_h |w relu(s_h)|.
+ *
+ * Each product is exact in float64 (2 significant bits times 2 times a power of two); the
+ * head sums are exact unless a row's scales span more than ~45 binades.
+ */
+int oracle_paged_logits_mxfp4(const uint8_t *q, const uint8_t *q_sf, const uint8_t *kv_fused,
+                              int64_t num_blocks, int block_size, const float *weights,
+                              const int32_t *block_tables, int64_t bt_row_stride,
+                              int64_t bt_width, const int32_t *seq_lens, int64_t seq_lens_stride,
+                              int batch, int next_n, int num_heads, int head_dim, double *out,
+                              int64_t out_row_stride, int64_t out_cols, double *tol,
+                              int nthreads) {
+    if (!q || !q_sf || !kv_fused || !weights || !block_tables || !seq_lens || !out)
+        return ORACLE_BAD_ARG;
+    if (block_size <= 0 || batch < 0 || next_n <= 0 || num_heads <= 0 || head_dim <= 0 ||
+        head_dim % 32 != 0)
+        return ORACLE_BAD_ARG;
+    const int row_bytes = head_dim / 2, groups = head_dim / 32;
+    const int64_t block_bytes = (int64_t)block_size * (row_bytes + groups);
+    const int64_t scale_region = (int64_t)block_size * row_bytes;
+    const int64_t rows = (int64_t)batch * next_n;
+    const int64_t chunk = 256;
+    int64_t max_len = 0;
+    for (int b = 0; b < batch; ++b)
+        if (seq_lens[(int64_t)b * seq_lens_stride] > max_len)
+            max_len = seq_lens[(int64_t)b * seq_lens_stride];
+    const int64_t chunks_per_row = (max_len + chunk - 1) / chunk;
+    int status = ORACLE_OK;
+
+    /* q dequantized once: row (r, h) element d. */
+    double *qd = (double *)malloc(sizeof(double) * (size_t)(rows > 0 ? rows : 1) * num_heads *
+                                  head_dim);
+    if (!qd) return ORACLE_NO_MEMORY;
+    for (int64_t rh = 0; rh < rows * num_heads; ++rh)
+        for (int d = 0; d < head_dim; ++d) {
+            const uint8_t byte = q[rh * row_bytes + d / 2];
+            const uint8_t nibble = (d % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+            qd[rh * head_dim + d] =
+                oracle_e2m1_to_double(nibble) * oracle_ue8m0_to_double(q_sf[rh * groups + d / 32]);
+        }
+
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel
+#endif
+    {
+        double *kd = (double *)malloc(sizeof(double) * (size_t)head_dim);
+        int64_t item;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 4)
+#endif
+        for (item = 0; item < rows * chunks_per_row; ++item) {
+            const int64_t r = item / chunks_per_row;
+            const int64_t b = r / next_n;
+            const int64_t t = r % next_n;
+            const int64_t seq_len = seq_lens[b * seq_lens_stride];
+            const int64_t row_end = oracle_row_end(seq_len, next_n, t);
+            const int64_t p_begin = (item % chunks_per_row) * chunk;
+            int64_t p_end = p_begin + chunk;
+            if (p_end > row_end) p_end = row_end;
+            if (!kd) {
+                status = ORACLE_NO_MEMORY;
+                continue;
+            }
+            if (seq_len == 0) continue;
+            for (int64_t p = p_begin; p < p_end; ++p) {
+                const int64_t j = p / block_size;
+                const int64_t i = p % block_size;
+                if (j >= bt_width) {
+                    status = ORACLE_BAD_PAGE;
+                    break;
+                }
+                const int64_t pg = block_tables[b * bt_row_stride + j];
+                if (pg < 0 || pg >= num_blocks) {
+                    status = ORACLE_BAD_PAGE;
+                    break;
+                }
+                if (p >= out_cols) {
+                    status = ORACLE_BAD_COLUMN;
+                    break;
+                }
+                const uint8_t *block = kv_fused + pg * block_bytes;
+                for (int d = 0; d < head_dim; ++d) {
+                    const uint8_t byte = block[i * row_bytes + d / 2];
+                    const uint8_t nibble = (d % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+                    kd[d] = oracle_e2m1_to_double(nibble) *
+                            oracle_ue8m0_to_double(block[scale_region + i * groups + d / 32]);
+                }
+                double weighted = 0.0, magnitude = 0.0;
+                for (int h = 0; h < num_heads; ++h) {
+                    const double *qh = qd + (r * num_heads + h) * head_dim;
+                    double s = 0.0;
+                    for (int d = 0; d < head_dim; ++d) s += qh[d] * kd[d];
+                    const double relu = s > 0.0 ? s : 0.0;
+                    const double wh = (double)weights[r * num_heads + h];
+                    weighted += wh * relu;
+                    magnitude += fabs(wh * relu);
+                }
+                out[r * out_row_stride + p] = weighted;
+                if (tol) tol[r * out_row_stride + p] = magnitude;
             }
         }
         free(kd);

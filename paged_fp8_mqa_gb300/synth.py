@@ -15,7 +15,7 @@ Layouts follow "flashinfer.attn_scores", fp8_paged_mqa_logits, Parameters:
 
 Draw order, all from one CPU ``torch.Generator`` seeded with the workload's seed:
 seq_lens, (zero-length request choice), page permutation, q, k, (outlier-row mask), kv scales,
-weights, and later threshold noise and (forced-repair row choice).
+weights, and later threshold noise and (forced-repair row choice), or the MXFP4 q and k.
 """
 from __future__ import annotations
 
@@ -141,6 +141,57 @@ def make_workload(name: str, seed: int, batch: int, next_n: int, max_seq_len: in
                     seq_lens=seq_lens, block_tables=block_tables, kv_fused=kv_fused,
                     q=q8.contiguous(), weights=weights.contiguous(), top_k=top_k,
                     capacity=capacity, gen=g, spec=dict(spec, seed=seed))
+
+
+# ---- MXFP4 inputs ("flashinfer.attn_scores", fp4_paged_mqa_logits, Parameters q, q_sf,
+# kv_fused) -----------------------------------------------------------------------------------
+
+# The E2M1 magnitudes by code 0..7 (OCP Microscaling Formats, FP4 E2M1); code | 8 negates.
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def quantize_mxfp4(x: torch.Tensor):
+    """Packs float32 rows [..., D] (D a multiple of 32) as MXFP4: per 32 consecutive elements a
+    UE8M0 scale byte e (the group's values are x / 2^(e - 127)), the smallest power of two for
+    which the group's largest magnitude is at most 6, and per element the E2M1 code of the
+    nearest magnitude (ties to the smaller), packed two per byte, element 2j in the low nibble of
+    byte j.  Returns (values uint8 [..., D/2], scales uint8 [..., D/32])."""
+    *lead, D = x.shape
+    g = x.reshape(*lead, D // 32, 32).to(torch.float64)
+    amax = g.abs().amax(-1)
+    e = torch.ceil(torch.log2(torch.clamp(amax, min=2.0 ** -127) / 6.0)).clamp(-127, 127)
+    y = g / torch.exp2(e)[..., None]
+    mags = torch.tensor(E2M1_MAGNITUDES, dtype=torch.float64)
+    code = (y.abs()[..., None] - mags).abs().argmin(-1)  # first (smaller) on ties
+    code = code | ((y < 0) & (code > 0)).to(torch.int64) << 3
+    code = code.reshape(*lead, D).to(torch.uint8)
+    packed = code[..., 0::2] | (code[..., 1::2] << 4)
+    return packed.contiguous(), (e + 127).to(torch.uint8).contiguous()
+
+
+@dataclass
+class Mxfp4Inputs:
+    q: torch.Tensor          # uint8 [batch, next_n, H, D/2]: packed E2M1
+    q_sf: torch.Tensor       # uint8 [batch, next_n, H, D/32]: UE8M0
+    kv_fused: torch.Tensor   # uint8 [num_blocks, block_size*(D/2 + D/32)]
+
+
+def make_mxfp4(w: Workload, *, spread_tokens: int = 0) -> Mxfp4Inputs:
+    """MXFP4 q and KV pool for workload ``w`` (same lengths, pages, weights), drawn next from its
+    generator: N(0,1) values, quantized.  ``spread_tokens`` KV tokens get one group scaled by
+    2^-12 (their block scales then span more than 8 binades)."""
+    g = w.gen
+    B, n, H, D, BS = w.batch, w.next_n, w.num_heads, w.head_dim, w.block_size
+    pool = w.num_blocks
+    q = torch.randn(B, n, H, D, generator=g)
+    k = torch.randn(pool, BS, D, generator=g)
+    if spread_tokens:
+        idx = torch.randperm(pool * BS, generator=g)[:spread_tokens]
+        k.view(pool * BS, D)[idx, :32] *= 2.0 ** -12
+    qv, qs = quantize_mxfp4(q)
+    kv, ks = quantize_mxfp4(k)
+    kv_fused = torch.cat([kv.flatten(1), ks.flatten(1)], dim=1).contiguous()
+    return Mxfp4Inputs(q=qv, q_sf=qs, kv_fused=kv_fused)
 
 
 # The five workloads of the indexer, by what they are.

@@ -415,9 +415,107 @@ def check_schedule_invariants(lib):
         assert (sizes >= 0).all() and sizes.max() - sizes.min() <= 1, sizes
 
 
+# --------------------------------------------------------------------------------------------
+# MXFP4 ("flashinfer.attn_scores", fp4_paged_mqa_logits)
+# --------------------------------------------------------------------------------------------
+
+# The FP4 E2M1 element values by code (OCP Microscaling Formats specification v1.0, the E2M1
+# table): codes 0-7 are +0, 0.5, 1, 1.5, 2, 3, 4, 6; codes 8-15 the same with the sign set.
+OCP_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def check_e2m1_codes(lib):
+    got = [lib.oracle_e2m1_to_double(c) for c in range(16)]
+    assert got[:8] == OCP_E2M1, got[:8]
+    assert got[8:] == [-v for v in OCP_E2M1], got[8:]
+    assert math.copysign(1.0, got[8]) < 0  # code 8 is -0
+
+
+def check_ue8m0_vs_torch(lib):
+    """All 256 scale bytes against torch's float8_e8m0fnu decode (2^(e - 127), 0xFF NaN)."""
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e8m0fnu)
+    ref = ref.to(torch.float64).tolist()
+    for e in range(256):
+        got = lib.oracle_ue8m0_to_double(e)
+        assert (math.isnan(got) and math.isnan(ref[e])) or got == ref[e], (e, got, ref[e])
+
+
+def _mx_single(lib, q_vals, q_sf, block, block_size, head_dim, seq_len, weights):
+    """One request, one head, one page: the oracle's MXFP4 logits row."""
+    q = np.asarray(q_vals, dtype=np.uint8).reshape(1, 1, 1, head_dim // 2)
+    qsf = np.asarray(q_sf, dtype=np.uint8).reshape(1, 1, 1, head_dim // 32)
+    kv = np.asarray(block, dtype=np.uint8).reshape(1, -1)
+    bt = np.zeros((1, 1), dtype=np.int32)
+    sl = np.array([seq_len], dtype=np.int32)
+    w = np.asarray(weights, dtype=np.float32).reshape(1, 1)
+    out, _ = oracle.paged_logits_mxfp4(q, qsf, kv, w, bt, sl, seq_len, block_size=block_size,
+                                       lib=lib)
+    return out[0]
+
+
+def check_mxfp4_layout_worked_block(lib):
+    """The pages' drawing for block_size 32, head_dim 128: token i's 64 packed bytes at i*64,
+    its 4 scale bytes at 2048 + 4*i (byte k for elements [32k, 32k+32)); byte j holds element 2j
+    in the low nibble and 2j+1 in the high nibble.  A block written byte by byte at those offsets
+    with one nonzero element per token must give w * q_d * k_d * 2^(e - 127) at each token."""
+    ex = GOLDEN["mxfp4_block"]
+    BS, D = ex["block_size"], ex["head_dim"]
+    assert ex["values_bytes"] == BS * D // 2 and ex["scale_offset_token_1"] == BS * D // 2 + 4
+    for d0 in (0, 1, 37, 127):
+        q = np.zeros(D // 2, dtype=np.uint8)
+        q[d0 // 2] = 2 << (4 * (d0 % 2))          # q element d0 = code 2 = 1.0
+        q_sf = [127] * (D // 32)                   # 2^0
+        block = np.zeros(BS * (D // 2 + D // 32), dtype=np.uint8)
+        expect = []
+        for i in range(BS):
+            code = 1 + i % 7                       # 0.5 .. 6
+            e = 120 + i % 9                        # 2^-7 .. 2^1
+            block[i * 64 + d0 // 2] = code << (4 * (d0 % 2))
+            block[2048 + 4 * i + d0 // 32] = e
+            expect.append(OCP_E2M1[code] * 2.0 ** (e - 127) * 0.75)
+        got = _mx_single(lib, q, q_sf, block, BS, D, BS, [0.75])
+        assert np.array_equal(got[:BS], np.array(expect)), (d0, got[:4], expect[:4])
+
+
+def check_mxfp4_matches_fp8(lib):
+    """With every scale byte 127 (2^0) the MXFP4 logits equal the FP8 oracle's (per-token scale
+    1.0) on the same element values, which e4m3 represents exactly; scaling all of a K token's
+    scale bytes by 2^e equals a per-token scale of 2^e there, and all of a q head's by 2^a a
+    weight scaled by 2^a (a positive power of two commutes with the ReLU).  Both sums are
+    exact, so the results agree bit for bit."""
+    g = torch.Generator().manual_seed(404)
+    B, n, H, D, BS = 2, 2, 4, 64, 32
+    lens = [70, 33]
+    w = synth.make_workload("mx", 21, B, n, 96, "fixed", values=lens, num_heads=H, head_dim=D,
+                            block_size=BS)
+    pool = w.num_blocks
+    qc = torch.randint(0, 16, (B, n, H, D), generator=g)
+    kc = torch.randint(0, 16, (pool, BS, D), generator=g)
+    table = torch.tensor(OCP_E2M1 + [-v for v in OCP_E2M1], dtype=torch.float32)
+    pack = lambda c: (c[..., 0::2] | (c[..., 1::2] << 4)).to(torch.uint8)
+    kexp = torch.randint(-3, 4, (pool, BS), generator=g)
+    qexp = torch.randint(-2, 3, (B, n, H), generator=g)
+    qm = pack(qc)
+    qsf = (127 + qexp)[..., None].expand(B, n, H, D // 32).to(torch.uint8).contiguous()
+    ksf = (127 + kexp)[..., None].expand(pool, BS, D // 32).to(torch.uint8)
+    kv4 = torch.cat([pack(kc).flatten(1), ksf.flatten(1)], dim=1).contiguous()
+    out4, _ = oracle.paged_logits_mxfp4(qm, qsf, kv4, w.weights, w.block_tables, w.seq_lens,
+                                        w.max_seq_len, block_size=BS, lib=lib)
+    q8 = table[qc].to(torch.float8_e4m3fn).view(torch.uint8)
+    k8 = table[kc].to(torch.float8_e4m3fn).view(torch.uint8)
+    scale = torch.exp2(kexp.to(torch.float32))
+    kv8 = torch.cat([k8.flatten(1), scale.view(torch.uint8).flatten(1)], dim=1).contiguous()
+    w8 = (w.weights * torch.exp2(qexp.to(torch.float32)).reshape(B * n, H)).contiguous()
+    out8, _ = oracle.paged_logits(q8.contiguous(), kv8, w8, w.block_tables, w.seq_lens,
+                                  w.max_seq_len, block_size=BS, lib=lib)
+    assert np.array_equal(np.nan_to_num(out4, nan=-7.0), np.nan_to_num(out8, nan=-7.0))
+
+
 ALL_CHECKS = [
     check_e4m3_all_codes, check_f32_le, check_helpers_worked_examples, check_layout_worked_block,
     check_dense_matmul, check_relu_per_head, check_scale_linear, check_paging_metamorphic,
     check_extents, check_total_order, check_topk_distinct, check_topk_ties, check_slots_worked,
     check_classify_closed_forms, check_fit_rule_gives_topk, check_schedule_invariants,
+    check_e2m1_codes, check_ue8m0_vs_torch, check_mxfp4_layout_worked_block,
+    check_mxfp4_matches_fp8,
 ]

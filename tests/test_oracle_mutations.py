@@ -57,6 +57,23 @@ MUTANTS = [
      "const int64_t flat = (int64_t)c * (total / num_ctas);"),
     ("schedule_floor_tiles", "total += (len + tile_tokens - 1) / tile_tokens;",
      "total += len / tile_tokens;"),
+    ("e2m1_bias", ": ldexp(1.0 + 0.5 * mantissa, exponent - 1);",
+     ": ldexp(1.0 + 0.5 * mantissa, exponent - 2);"),
+    ("e2m1_subnormal", "exponent == 0 ? 0.5 * mantissa", "exponent == 0 ? 1.0 * mantissa"),
+    ("ue8m0_bias", "ldexp(1.0, (int)e - 127)", "ldexp(1.0, (int)e - 126)"),
+    ("mx_q_nibbles_swapped",
+     "const uint8_t byte = q[rh * row_bytes + d / 2];\n            const uint8_t nibble = (d % 2 == 0) ? (byte & 0xF) : (byte >> 4);",
+     "const uint8_t byte = q[rh * row_bytes + d / 2];\n            const uint8_t nibble = (d % 2 == 1) ? (byte & 0xF) : (byte >> 4);"),
+    ("mx_k_nibbles_swapped",
+     "const uint8_t byte = block[i * row_bytes + d / 2];\n                    const uint8_t nibble = (d % 2 == 0) ? (byte & 0xF) : (byte >> 4);",
+     "const uint8_t byte = block[i * row_bytes + d / 2];\n                    const uint8_t nibble = (d % 2 == 1) ? (byte & 0xF) : (byte >> 4);"),
+    ("mx_k_scale_group16", "oracle_ue8m0_to_double(block[scale_region + i * groups + d / 32])",
+     "oracle_ue8m0_to_double(block[scale_region + i * groups + (d / 16) % groups])"),
+    ("mx_k_scales_interleaved", "oracle_ue8m0_to_double(block[scale_region + i * groups + d / 32])",
+     "oracle_ue8m0_to_double(block[scale_region + (d / 32) * block_size + i])"),
+    ("mx_q_scale_dropped",
+     "oracle_e2m1_to_double(nibble) * oracle_ue8m0_to_double(q_sf[rh * groups + d / 32]);",
+     "oracle_e2m1_to_double(nibble);"),
 ]
 
 
