@@ -5,7 +5,8 @@
  *   1. paged FP8 MQA logits   ("flashinfer.attn_scores", fp8_paged_mqa_logits)
  *   2. threshold top-k select  ("flashinfer.sdsa.indexer_threshold_select"), reading stage 1's
  *      logits
- * and both fused into one pass that writes no logits (idx_indexer_threshold_select), plus the
+ * and both fused into one pass that writes no logits (idx_indexer_threshold_select), the MXFP4
+ * variant of stage 1 (idx_logits_mxfp4), plus the
  * persistent work split of stage 1 ("flashinfer.attn_scores", Scheduling and Setup) and the two
  * integer helpers named there.
  *
@@ -46,6 +47,8 @@ extern "C" {
 /* Device-side status bits (idx_device_status). */
 #define IDX_DEV_WAIT_TIMEOUT 1 /* a pipeline wait gave up after its time limit */
 #define IDX_DEV_BAD_PAGE 2     /* a needed block-table entry was outside [0, num_blocks) */
+#define IDX_DEV_INEXACT_SCALE 4 /* (MXFP4) a row's block scales span more than 8 binades, or a
+                                   scale byte is the NaN code 0xFF: its staging rounded */
 
 /* Description of the most recent error on the calling thread ("" if none). */
 const char *idx_last_error(void);
@@ -146,6 +149,47 @@ int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t num_blocks
                    int32_t head_dim, int32_t max_seq_len, const int32_t *schedule,
                    int32_t num_sms, int32_t output_dtype, void *out, int64_t out_row_stride,
                    int32_t *row_ends_out, void *stream);
+
+/*
+ * idx_logits_mxfp4 ("flashinfer.attn_scores", fp4_paged_mqa_logits: formula block, Parameters
+ * q, q_sf, kv_fused, sf_vec_size = 32):
+ *
+ *   out[(b*next_n + t) * out_row_stride + p] = sum_h weights[b*next_n + t, h] * relu(q . k)
+ *
+ * with every element of q[b,t,h,:] and k[p,:] an E2M1 value times its 32-element group's UE8M0
+ * scale 2^(e - 127), and no per-position factor.  Extents, zero-length requests, block_tables,
+ * seq_lens, batch, next_n, num_heads, head_dim, block_size, max_seq_len, num_sms,
+ * output_dtype, out, out_row_stride and row_ends_out are as for idx_logits_fp8 (output_dtype:
+ * IDX_DTYPE_F32 or IDX_DTYPE_F16; the pages' bfloat16 default is not offered).
+ *
+ *   q            device uint8 [batch, next_n, num_heads, head_dim/2], 16-byte aligned: two
+ *                E2M1 codes per byte, element 2j in the low nibble of byte j
+ *   q_sf         device uint8 [batch, next_n, num_heads, head_dim/32]: byte k scales elements
+ *                [32k, 32k + 32) (the little-endian bytes of the pages' int32 view)
+ *   kv_fused     device uint8 [num_blocks][block_size*(head_dim/2 + head_dim/32)], 16-byte
+ *                aligned: per block the packed rows token-major (token i at i*head_dim/2), then
+ *                head_dim/32 scale bytes per token (token i's at block_size*head_dim/2 +
+ *                (head_dim/32)*i)
+ *   weights      device float32 [batch*next_n, num_heads]
+ *   workspace    device, 256-byte aligned, at least idx_mxfp4_workspace_bytes(...) bytes
+ *
+ * Three launches: q (with its weights) and every KV page the batch references are staged in the
+ * FP8 layouts inside the workspace, each row's largest block scale moved into the head's weight
+ * or the token's float32 scale (exact: a positive power of two commutes with the ReLU), and
+ * idx_logits_fp8 runs on them.  The staged values are exact while a row's block scales span at
+ * most 8 binades; a row that spans more (or holds the NaN scale byte 0xFF) is rounded and raises
+ * IDX_DEV_INEXACT_SCALE.
+ */
+int64_t idx_mxfp4_workspace_bytes(int64_t num_blocks, int32_t block_size, int32_t batch,
+                                  int32_t next_n, int32_t num_heads, int32_t head_dim);
+int idx_logits_mxfp4(const uint8_t *q, const uint8_t *q_sf, const uint8_t *kv_fused,
+                     int64_t num_blocks, int32_t block_size, const float *weights,
+                     const int32_t *block_tables, int64_t bt_row_stride, int32_t bt_width,
+                     const int32_t *seq_lens, int64_t seq_lens_stride, int32_t batch,
+                     int32_t next_n, int32_t num_heads, int32_t head_dim, int32_t max_seq_len,
+                     int32_t num_sms, int32_t output_dtype, void *out, int64_t out_row_stride,
+                     int32_t *row_ends_out, void *workspace, int64_t workspace_bytes,
+                     void *stream);
 
 /*
  * idx_threshold_select ("flashinfer.sdsa.indexer_threshold_select": description; Parameters

@@ -27,6 +27,7 @@ IDX_DTYPE_F32 = 0
 IDX_DTYPE_F16 = 1
 IDX_DEV_WAIT_TIMEOUT = 1
 IDX_DEV_BAD_PAGE = 2
+IDX_DEV_INEXACT_SCALE = 4
 
 TILE_TOKENS = 128  # KV positions per work unit of the persistent logits kernel
 
@@ -75,6 +76,14 @@ def lib() -> ctypes.CDLL:
         P, P, c.c_int64, c.c_int32, P, P, c.c_int64, c.c_int32, P, c.c_int64, c.c_int32,
         c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32, P, P, P, c.c_int32, c.c_int32, P,
         P, P, c.c_int64, P]
+    L.idx_mxfp4_workspace_bytes.restype = c.c_int64
+    L.idx_mxfp4_workspace_bytes.argtypes = [c.c_int64, c.c_int32, c.c_int32, c.c_int32,
+                                            c.c_int32, c.c_int32]
+    L.idx_logits_mxfp4.restype = c.c_int
+    L.idx_logits_mxfp4.argtypes = [P, P, P, c.c_int64, c.c_int32, P, P, c.c_int64, c.c_int32, P,
+                                   c.c_int64, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
+                                   c.c_int32, c.c_int32, c.c_int32, P, c.c_int64, P, P,
+                                   c.c_int64, P]
     L.idx_device_status.restype = c.c_int
     L.idx_device_status.argtypes = [P, c.c_int32]
     _lib = L
@@ -160,6 +169,23 @@ def idx_indexer_threshold_select(q, kv_fused, num_blocks, block_size, weights, b
         scratch_row_stride, stream)
 
 
+def idx_mxfp4_workspace_bytes(num_blocks, block_size, batch, next_n, num_heads,
+                              head_dim) -> int:
+    return int(lib().idx_mxfp4_workspace_bytes(num_blocks, block_size, batch, next_n, num_heads,
+                                               head_dim))
+
+
+def idx_logits_mxfp4(q, q_sf, kv_fused, num_blocks, block_size, weights, block_tables,
+                     bt_row_stride, bt_width, seq_lens, seq_lens_stride, batch, next_n,
+                     num_heads, head_dim, max_seq_len, num_sms, output_dtype, out,
+                     out_row_stride, row_ends_out, workspace, workspace_bytes, stream) -> int:
+    return lib().idx_logits_mxfp4(q, q_sf, kv_fused, num_blocks, block_size, weights,
+                                  block_tables, bt_row_stride, bt_width, seq_lens,
+                                  seq_lens_stride, batch, next_n, num_heads, head_dim,
+                                  max_seq_len, num_sms, output_dtype, out, out_row_stride,
+                                  row_ends_out, workspace, workspace_bytes, stream)
+
+
 def idx_device_status(clear: bool = False) -> int:
     out = ctypes.c_int32(0)
     _check(lib().idx_device_status(ctypes.byref(out), int(clear)))
@@ -235,6 +261,55 @@ def logits_fp8(q, kv_fused, weights, block_tables, seq_lens, max_seq_len: int, *
                           _ptr(seq_lens), seq_lens.stride(0), B, n, H, D, max_seq_len,
                           _ptr(schedule_meta), num_sms, dtype_code, _ptr(out), out.stride(0),
                           _ptr(row_ends_out), _stream(stream)))
+    return out[:B * n, :max_seq_len]
+
+
+def logits_mxfp4(q, q_sf, kv_fused, weights, block_tables, seq_lens, max_seq_len: int, *,
+                 out=None, output_dtype=None, workspace=None, num_sms: int = 0,
+                 row_ends_out=None, stream=None):
+    """MXFP4 paged MQA logits.  q: uint8 [B, next_n, H, D/2] (packed E2M1); q_sf: uint8
+    [B, next_n, H, D/32] or its int32 view [B, next_n, H] (UE8M0); kv_fused: uint8 whose leading
+    dim is the block count, block_size*(D/2 + D/32) bytes per block; weights float32
+    [B*next_n, H]; block_tables, seq_lens as for ``logits_fp8``.  output_dtype: torch.float32
+    (default here; the pages default to bfloat16, which is not offered) or torch.float16.
+    ``workspace`` (uint8, at least idx_mxfp4_workspace_bytes) is allocated if not given."""
+    import torch
+    _need(q, torch.uint8, "q", 4)
+    _need(q_sf, (torch.uint8, torch.int32), "q_sf")
+    _need(kv_fused, torch.uint8, "kv_fused")
+    _need(weights, torch.float32, "weights", 2)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, n, H, half = q.shape
+    D = 2 * half
+    for t, name in ((q, "q"), (q_sf, "q_sf"), (weights, "weights"), (kv_fused, "kv_fused")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q_sf.dtype == torch.int32:
+        q_sf = q_sf.view(torch.uint8)
+    if q_sf.numel() != B * n * H * (D // 32):
+        raise ValueError("q_sf must hold head_dim/32 scale bytes per (b, t, h)")
+    if block_tables.stride(1) != 1:
+        raise ValueError("block_tables rows must be contiguous (stride(1) == 1)")
+    num_blocks = kv_fused.shape[0]
+    block_size = kv_fused.numel() // num_blocks // (D // 2 + D // 32) if num_blocks else 0
+    if out is None:
+        out = torch.empty(B * n, idx_padded_seq_len(max_seq_len),
+                          dtype=output_dtype or torch.float32, device=q.device)
+    elif output_dtype is not None and out.dtype != output_dtype:
+        raise ValueError(f"out is {out.dtype} but output_dtype is {output_dtype}")
+    _need(out, (torch.float32, torch.float16), "out", 2)
+    need = idx_mxfp4_workspace_bytes(num_blocks, block_size, B, n, H, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _need(workspace, torch.uint8, "workspace")
+    dtype_code = IDX_DTYPE_F16 if out.dtype == torch.float16 else IDX_DTYPE_F32
+    _check(idx_logits_mxfp4(_ptr(q), _ptr(q_sf), _ptr(kv_fused), num_blocks, block_size,
+                            _ptr(weights), _ptr(block_tables), block_tables.stride(0),
+                            block_tables.shape[1], _ptr(seq_lens), seq_lens.stride(0), B, n, H, D,
+                            max_seq_len, num_sms, dtype_code, _ptr(out), out.stride(0),
+                            _ptr(row_ends_out), _ptr(workspace), workspace.numel(),
+                            _stream(stream)))
     return out[:B * n, :max_seq_len]
 
 

@@ -249,6 +249,84 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
   return IDX_OK;
 }
 
+IDX_EXPORT int64_t idx_mxfp4_workspace_bytes(int64_t num_blocks, int32_t block_size,
+                                              int32_t batch, int32_t next_n, int32_t num_heads,
+                                              int32_t head_dim) {
+  if (num_blocks < 0 || block_size <= 0 || batch < 0 || next_n <= 0 || num_heads <= 0 ||
+      head_dim <= 0)
+    return -1;
+  const auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
+  const int64_t rows_heads = static_cast<int64_t>(batch) * next_n * num_heads;
+  return up(num_blocks * block_size * (head_dim + 4)) + up(rows_heads * head_dim) +
+         up(rows_heads * 4);
+}
+
+IDX_EXPORT int idx_logits_mxfp4(const uint8_t *q, const uint8_t *q_sf, const uint8_t *kv_fused,
+                                int64_t num_blocks, int32_t block_size, const float *weights,
+                                const int32_t *block_tables, int64_t bt_row_stride,
+                                int32_t bt_width, const int32_t *seq_lens,
+                                int64_t seq_lens_stride, int32_t batch, int32_t next_n,
+                                int32_t num_heads, int32_t head_dim, int32_t max_seq_len,
+                                int32_t num_sms, int32_t output_dtype, void *out,
+                                int64_t out_row_stride, int32_t *row_ends_out, void *workspace,
+                                int64_t workspace_bytes, void *stream) {
+  g_error.clear();
+  if (q == nullptr || q_sf == nullptr || kv_fused == nullptr || weights == nullptr ||
+      block_tables == nullptr || seq_lens == nullptr || out == nullptr || workspace == nullptr)
+    return fail(IDX_INVALID_ARG,
+                "q, q_sf, kv_fused, weights, block_tables, seq_lens, out, workspace: NULL");
+  if (batch < 0 || max_seq_len < 0 || num_blocks < 1 || bt_width < 0 || seq_lens_stride < 1 ||
+      bt_row_stride < bt_width || block_size <= 0 || num_heads <= 0 || head_dim <= 0 ||
+      next_n <= 0)
+    return fail(IDX_INVALID_ARG, "negative or inconsistent size or stride");
+  if ((num_heads != 32 && num_heads != 64) || (head_dim != 64 && head_dim != 128) ||
+      (block_size != 32 && block_size != 64 && block_size != 128))
+    return fail(IDX_UNSUPPORTED, "this build supports num_heads 32 or 64, head_dim 64 or 128, "
+                                 "block_size 32, 64 or 128");
+  if (next_n > 4) return fail(IDX_UNSUPPORTED, "next_n must be 1..4");
+  if (batch > idx::kMaxBatch) return fail(IDX_UNSUPPORTED, "batch above 4096");
+  const int64_t need = idx_mxfp4_workspace_bytes(num_blocks, block_size, batch, next_n,
+                                                 num_heads, head_dim);
+  if (workspace_bytes < need)
+    return fail(IDX_INVALID_ARG, "workspace_bytes < idx_mxfp4_workspace_bytes(...) = " +
+                                     std::to_string(need));
+  if (!aligned(q, 16) || !aligned(kv_fused, 16) || !aligned(workspace, 256) ||
+      !aligned(weights, 4))
+    return fail(IDX_INVALID_ARG, "q and kv_fused must be 16-byte aligned, workspace 256-byte");
+  if (batch == 0) return IDX_OK;
+  const auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
+  const int64_t rows_heads = static_cast<int64_t>(batch) * next_n * num_heads;
+  uint8_t *kv8 = static_cast<uint8_t *>(workspace);
+  uint8_t *q8 = kv8 + up(num_blocks * block_size * (head_dim + 4));
+  float *w8 = reinterpret_cast<float *>(q8 + up(rows_heads * head_dim));
+  idx::Mxfp4Stage st{};
+  st.q4 = q;
+  st.q_sf = q_sf;
+  st.weights = weights;
+  st.kv4 = kv_fused;
+  st.block_tables = block_tables;
+  st.bt_stride = bt_row_stride;
+  st.seq_lens = seq_lens;
+  st.sl_stride = seq_lens_stride;
+  st.q8 = q8;
+  st.w8 = w8;
+  st.kv8 = kv8;
+  st.num_blocks = num_blocks;
+  st.rows_heads = static_cast<int32_t>(rows_heads);
+  st.block_size = block_size;
+  st.head_dim = head_dim;
+  st.batch = batch;
+  st.max_pages = static_cast<int32_t>((static_cast<int64_t>(max_seq_len) + block_size - 1) /
+                                      block_size);
+  const cudaError_t e = idx::launch_mxfp4_stage(st, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "MXFP4 staging launch");
+  // The staged tensors are in the FP8 layouts: the FP8 logits path computes the logits.
+  return idx_logits_fp8(q8, kv8, num_blocks, block_size, w8, block_tables, bt_row_stride,
+                        bt_width, seq_lens, seq_lens_stride, batch, next_n, num_heads, head_dim,
+                        max_seq_len, nullptr, num_sms, output_dtype, out, out_row_stride,
+                        row_ends_out, stream);
+}
+
 IDX_EXPORT int idx_indexer_threshold_select(
     const uint8_t *q, const uint8_t *kv_fused, int64_t num_blocks, int32_t block_size,
     const float *weights, const int32_t *block_tables, int64_t bt_row_stride, int32_t bt_width,
@@ -467,10 +545,11 @@ IDX_EXPORT int idx_threshold_select_static(const float *logits, int64_t logits_r
 IDX_EXPORT int idx_device_status(int32_t *status_out, int32_t clear) {
   g_error.clear();
   if (status_out == nullptr) return fail(IDX_INVALID_ARG, "status_out is NULL");
-  int32_t a = 0, b = 0;
+  int32_t a = 0, b = 0, c = 0;
   cudaError_t e = idx::logits_status(&a, clear != 0);
   if (e == cudaSuccess) e = idx::select_status(&b, clear != 0);
+  if (e == cudaSuccess) e = idx::mxfp4_status(&c, clear != 0);
   if (e != cudaSuccess) return cuda_fail(e, "status copy");
-  *status_out = a | b;
+  *status_out = a | b | c;
   return IDX_OK;
 }

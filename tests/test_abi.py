@@ -154,6 +154,39 @@ def test_fused_accepts_missing_repair_buffers_without_arrivals(lib):
     assert idx.idx_indexer_threshold_select(*a.values()) == idx.IDX_OK, idx.idx_last_error()
 
 
+def test_mxfp4_workspace_size(lib):
+    up = lambda x: (x + 255) // 256 * 256
+    for nb, bs, b, n, h, d in ((10, 64, 2, 1, 64, 128), (7, 32, 3, 4, 32, 64), (1, 128, 0, 2, 64, 64)):
+        want = up(nb * bs * (d + 4)) + up(b * n * h * d) + up(b * n * h * 4)
+        assert idx.idx_mxfp4_workspace_bytes(nb, bs, b, n, h, d) == want
+    assert idx.idx_mxfp4_workspace_bytes(-1, 64, 1, 1, 64, 128) == -1
+
+
+def _mxfp4_args(**over):
+    a = dict(q=FAKE, q_sf=FAKE, kv_fused=FAKE, num_blocks=10, block_size=64, weights=FAKE,
+             block_tables=FAKE, bt_row_stride=16, bt_width=16, seq_lens=FAKE,
+             seq_lens_stride=1, batch=2, next_n=1, num_heads=64, head_dim=128, max_seq_len=1024,
+             num_sms=4, output_dtype=idx.IDX_DTYPE_F32, out=FAKE, out_row_stride=1024,
+             row_ends_out=None, workspace=FAKE, workspace_bytes=1 << 30, stream=None)
+    a.update(over)
+    return a
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q_sf=None), idx.IDX_INVALID_ARG),
+    (dict(workspace=None), idx.IDX_INVALID_ARG),
+    (dict(workspace_bytes=1000), idx.IDX_INVALID_ARG),
+    (dict(workspace=P((1 << 20) + 16)), idx.IDX_INVALID_ARG),
+    (dict(head_dim=96), idx.IDX_UNSUPPORTED),
+    (dict(num_heads=16), idx.IDX_UNSUPPORTED),
+    (dict(next_n=5), idx.IDX_UNSUPPORTED),
+    (dict(batch=-1), idx.IDX_INVALID_ARG),
+])
+def test_mxfp4_rejects_bad_arguments(lib, over, code):
+    a = _mxfp4_args(**over)
+    assert idx.idx_logits_mxfp4(*a.values()) == code, idx.idx_last_error()
+
+
 def test_schedule_rejects_bad_arguments(lib):
     assert idx.idx_schedule(None, 1, 4, 1, 8, FAKE, None) == idx.IDX_INVALID_ARG
     assert idx.idx_schedule(FAKE, 0, 4, 1, 8, FAKE, None) == idx.IDX_INVALID_ARG
