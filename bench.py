@@ -293,6 +293,54 @@ def time_fused(w, t, steps, warmup, stream) -> dict:
                     "(launched every step, empty when nothing needs a repair)"}
 
 
+def time_mxfp4(w: synth.Workload, dev, steps: int, warmup: int, stream, peaks: dict) -> dict:
+    """The MXFP4 variant on the same lengths, pages and weights (q and K drawn anew and
+    quantized): staging + FP8 logits per step, three MXFP4 pools in rotation (each below L2 on
+    its own, together above it).  Roofline: the MXFP4 bytes of every valid position (D/2 + D/32
+    per token), the logits written, q, q_sf and w."""
+    m = synth.make_mxfp4(w)
+    pools = [m.kv_fused.to(dev)]
+    for _ in range(POOL_COPIES - 1):
+        pools.append(pools[0].clone())
+    q, qsf = m.q.to(dev), m.q_sf.to(dev)
+    wt, bt, sl = w.weights.to(dev), w.block_tables.to(dev), w.seq_lens.to(dev)
+    ws = torch.empty(idx.idx_mxfp4_workspace_bytes(w.num_blocks, w.block_size, w.batch,
+                                                   w.next_n, w.num_heads, w.head_dim),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty(w.rows, idx.idx_padded_seq_len(w.max_seq_len), device=dev)
+
+    def step(i):
+        idx.logits_mxfp4(q, qsf, pools[i % POOL_COPIES], wt, bt, sl, w.max_seq_len, out=out,
+                         workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(2_000_000)
+        e0.record(stream)
+        for i in range(steps):
+            step(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    D = w.head_dim
+    P = int(w.seq_lens.to(torch.int64).sum())
+    scores = w.valid_scores()
+    nbytes = P * (D // 2 + D // 32) + 4 * scores + m.q.numel() + m.q_sf.numel() + 4 * wt.numel()
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    return {"value": scores / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_launch": ms,
+            "launches_per_step": 3, "algorithmic_bytes": nbytes,
+            "hbm_gbs": nbytes / (ms * 1e-3) / 1e9, "roofline_time_ms": t_hbm * 1e3,
+            "roofline_frac": t_hbm * 1e3 / ms,
+            "note": "q and every referenced KV page staged in the FP8 layouts (written and read "
+                    "back), then the FP8 logits kernel; a first correct path, not the roofline "
+                    "design (which converts on chip)"}
+
+
 def time_launch_events(w, t, steps, stream):
     """Diagnostic: the same launches each bracketed by its own pair of events (which keeps the
     device from overlapping one launch's start with the previous one's end)."""
@@ -558,6 +606,9 @@ def main() -> None:
                             "hbm_gbs": a2["bytes"] / (m2 * 1e-3) / 1e9,
                             "tflops": a2["flops"] / (m2 * 1e-3) / 1e12}
         del t2
+        # The MXFP4 variant on the decode workload's shape.
+        secondary["mxfp4"] = time_mxfp4(w, dev, max(3, min(300, args.steps)), args.warmup,
+                                        stream, peaks)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

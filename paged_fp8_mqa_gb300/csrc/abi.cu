@@ -13,6 +13,7 @@
 
 #include "../../include/idx.h"
 #include "internal.h"
+#include "mxfp4.h"
 
 #define IDX_EXPORT extern "C" __attribute__((visibility("default")))
 

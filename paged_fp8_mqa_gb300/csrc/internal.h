@@ -119,33 +119,8 @@ cudaError_t launch_fused_repair(const FusedRepairArgs &args, cudaStream_t stream
 // (at most IDX_STATIC_SELECT_MAX_ROWS rows; the caller checks).
 cudaError_t launch_threshold_select_static(SelectArgs args, cudaStream_t stream);
 
-// MXFP4 staging: q rows (and their weights) and the KV pages the batch references converted to
-// the FP8 layouts, with each row's largest block scale moved into the weight / per-token scale.
-struct Mxfp4Stage {
-  const uint8_t *q4;       // [batch * next_n * num_heads][head_dim / 2] packed E2M1
-  const uint8_t *q_sf;     // [batch * next_n * num_heads][head_dim / 32] UE8M0
-  const float *weights;    // [batch * next_n][num_heads]
-  const uint8_t *kv4;      // [num_blocks][block_size * (head_dim / 2 + head_dim / 32)]
-  const int32_t *block_tables;
-  int64_t bt_stride;
-  const int32_t *seq_lens;
-  int64_t sl_stride;
-  uint8_t *q8;             // staged q, [batch * next_n * num_heads][head_dim] e4m3
-  float *w8;               // staged weights
-  uint8_t *kv8;            // staged pool, [num_blocks][block_size * (head_dim + 4)]
-  int64_t num_blocks;
-  int32_t rows_heads;      // batch * next_n * num_heads
-  int32_t block_size;
-  int32_t head_dim;        // 64 or 128
-  int32_t batch;
-  int32_t max_pages;       // ceil(max_seq_len / block_size)
-};
-
-cudaError_t launch_mxfp4_stage(const Mxfp4Stage &stage, cudaStream_t stream);
-
 // Device-side status words of each translation unit (IDX_DEV_* bits).
 cudaError_t logits_status(int32_t *value, bool clear);
 cudaError_t select_status(int32_t *value, bool clear);
-cudaError_t mxfp4_status(int32_t *value, bool clear);
 
 }  // namespace idx

@@ -24,6 +24,7 @@
 
 #include "../../include/idx.h"
 #include "internal.h"
+#include "mxfp4.h"
 #include "ptx.cuh"
 
 namespace idx {
