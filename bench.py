@@ -449,20 +449,23 @@ def barrier():
         torch.distributed.barrier()
 
 
-def reduce_max(x: float) -> float:
+def _reduce(x: float, op) -> float:
+    """All-reduce of one float over the replicas (on the GPU under NCCL, on the host under
+    gloo); x itself without a process group."""
     if torch.distributed.is_available() and torch.distributed.is_initialized():
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=op)
         return float(t.item())
     return x
+
+
+def reduce_max(x: float) -> float:
+    return _reduce(x, torch.distributed.ReduceOp.MAX)
 
 
 def reduce_sum(x: float) -> float:
-    if torch.distributed.is_available() and torch.distributed.is_initialized():
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
-        return float(t.item())
-    return x
+    return _reduce(x, torch.distributed.ReduceOp.SUM)
 
 
 def make(name: str) -> synth.Workload:
