@@ -221,7 +221,7 @@ int idx_logits_mxfp4(const uint8_t *q, const uint8_t *q_sf, const uint8_t *kv_fu
  *   candidates        device int32 [rows][top_k + capacity][2]
  *   top_k             >= 1 (the number of tie slots)
  *   capacity          >= 0 candidate slots; >= top_k - 1 when arrivals is given
- *   max_context       the most keys a row sees; sizes the grid (one CTA per 8192 keys)
+ *   max_context       the most keys a row sees; sizes the grid (one CTA per 16384 keys)
  *   arrivals          NULL (no repair), or device int32 [rows], zeroed once; every call
  *                     leaves it zeroed
  *   ranges            device int32 [2][rows]; required when arrivals is given, else ignored
