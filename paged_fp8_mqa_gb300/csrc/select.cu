@@ -4,9 +4,9 @@
 //
 // Grid: (ceil(max_context / kChunk), rows).  CTA (c, r) sweeps keys [c*kChunk, (c+1)*kChunk)
 // of row r below row_ends[r]: s > thr is a candidate, "neither above nor below" (== or NaN) a
-// tie.  Slots are reserved with one atomicAdd per warp and per kind (warp-aggregated), the
-// n-th candidate going to slot top_k + n (n < capacity), the n-th tie to top_k - 1 - n
-// (n < top_k), each as (key index, raw float32 bits).
+// tie.  Slots are reserved with one atomicAdd per warp and per kind for all the warp's 512 keys
+// (a warp scan of the counts), the n-th candidate going to slot top_k + n (n < capacity), the
+// n-th tie to top_k - 1 - n (n < top_k), each as (key index, raw float32 bits).
 //
 // With `arrivals`, the last CTA of a row to finish (an atomicAdd ticket, no waiting) decides
 // whether the row fits; if not, it repairs it alone: an MSB-first radix select over
@@ -22,6 +22,10 @@
 // to two sweeps (an 11-bit histogram of the row finds the bin holding v; a second sweep stores
 // the keys of higher bins as candidates and gathers the bin into the buffer), and if that bin is
 // too large, to four 8-bit passes over the row and a final in-order sweep.
+//
+// k_fused_repair is the last launch of the fused score + select: one CTA per row, which writes
+// the slot range of a row that fits and repairs one that does not, with the same code, from the
+// row's rescored logits.
 
 #include <cuda_runtime.h>
 
