@@ -137,6 +137,16 @@ def row_end(seq_len: int, next_n: int, t: int, lib=None) -> int:
     return int((lib or load()).oracle_row_end(seq_len, next_n, t))
 
 
+def row_ends(seq_lens, next_n: int, lib=None) -> np.ndarray:
+    """int32 [batch*next_n]: oracle_row_end of every (request, draft slot), row b*next_n + t
+    ("flashinfer.attn_scores", fp8_paged_mqa_logits, Note and Returns: slot t of request b
+    sees positions 0 .. seq_lens[b] - next_n + t)."""
+    lib = lib or load()
+    sl = _np(seq_lens).astype(np.int64, copy=False).reshape(-1)
+    return np.array([lib.oracle_row_end(int(L), next_n, t) for L in sl for t in range(next_n)],
+                    dtype=np.int32)
+
+
 def paged_logits(q_u8, kv_fused_u8, weights, block_tables, seq_lens, max_seq_len: int,
                  *, block_size: int, out_cols: int | None = None, fill=np.nan,
                  with_tol: bool = True, nthreads: int = 0, lib=None):

@@ -1,6 +1,7 @@
 // internal.h -- host-side interface between the C ABI layer and the kernel translation units.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -27,6 +28,27 @@ cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, s
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
+
+// A kernel attribute (the opt-in to more than 48 KiB of dynamic shared memory) belongs to the
+// current device's context, so each launcher sets it once per device: `set` runs on the first
+// call made with each device current (devices past the first 64 run it on every call).
+class PerDeviceOnce {
+ public:
+  template <typename F>
+  cudaError_t run(F &&set) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t{1} << dev) : 0;
+    if (bit != 0 && (done_.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = set();
+    if (e == cudaSuccess && bit != 0) done_.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  std::atomic<uint64_t> done_{0};
+};
 
 // Largest batch (requests per call) the kernels accept: the logits kernel keeps every
 // request's length in shared memory.

@@ -927,14 +927,13 @@ cudaError_t launch_nn(const CUtensorMap &kv_map, const CUtensorMap &q_map, const
                       int num_ctas, cudaStream_t stream) {
   using C = Cfg<NN, H, D>;
   const uint32_t smem = C::smem_bytes(args.batch);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_logits_fp8<NN, H, D, OutT, BS_SHIFT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::smem_bytes(kMaxBatch));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce configured;
+  const cudaError_t e = configured.run([] {
+    return cudaFuncSetAttribute(k_logits_fp8<NN, H, D, OutT, BS_SHIFT>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::smem_bytes(kMaxBatch));
+  });
+  if (e != cudaSuccess) return e;
   return launch_dependent(k_logits_fp8<NN, H, D, OutT, BS_SHIFT>, dim3(num_ctas), dim3(C::THREADS),
                           smem, stream, kv_map, q_map, args);
 }

@@ -37,14 +37,13 @@ __global__ void __launch_bounds__(kThreads)
 
 cudaError_t launch_schedule(const int32_t *seq_lens, int64_t stride, int batch, int num_ctas,
                             int32_t *schedule, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(
+  static PerDeviceOnce configured;
+  const cudaError_t e = configured.run([] {
+    return cudaFuncSetAttribute(
         k_schedule, cudaFuncAttributeMaxDynamicSharedMemorySize,
         static_cast<int>(sizeof(long long) * (kThreads / 32 + kMaxBatch) + 4 * kMaxBatch));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  });
+  if (e != cudaSuccess) return e;
   const size_t smem = sizeof(long long) * (kThreads / 32 + batch) + 4 * static_cast<size_t>(batch);
   return launch_dependent(k_schedule, dim3(1), dim3(kThreads), smem, stream, seq_lens, stride, batch,
                           num_ctas, schedule);

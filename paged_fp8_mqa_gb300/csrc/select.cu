@@ -741,24 +741,22 @@ __global__ void __launch_bounds__(kThreads) k_fused_repair(const FusedRepairArgs
 cudaError_t launch_threshold_select(const SelectArgs &args, cudaStream_t stream) {
   const int per_row = args.max_context > 0 ? (args.max_context + kChunk - 1) / kChunk : 1;
   const dim3 grid(per_row, args.rows);
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        k_threshold_select, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelectSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce configured;
+  const cudaError_t e = configured.run([] {
+    return cudaFuncSetAttribute(k_threshold_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSelectSmem);
+  });
+  if (e != cudaSuccess) return e;
   return launch_dependent(k_threshold_select, grid, dim3(kThreads), kSelectSmem, stream, args);
 }
 
 cudaError_t launch_fused_repair(const FusedRepairArgs &args, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        k_fused_repair, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelectSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce configured;
+  const cudaError_t e = configured.run([] {
+    return cudaFuncSetAttribute(k_fused_repair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSelectSmem);
+  });
+  if (e != cudaSuccess) return e;
   return launch_dependent(k_fused_repair, dim3(args.batch, args.next_n), dim3(kThreads),
                           kSelectSmem, stream, args);
 }

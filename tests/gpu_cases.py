@@ -20,6 +20,17 @@ def dev():
     return torch.device("cuda:0")
 
 
+def expected_row_ends(w: synth.Workload) -> np.ndarray:
+    """int32 [rows]: the oracle's extent of every row (row b*next_n + t sees positions
+    0 .. seq_lens[b] - next_n + t).  Every GPU test takes its expected extents from here."""
+    return oracle.row_ends(w.seq_lens, w.next_n)
+
+
+def expected_scores(w: synth.Workload) -> int:
+    """Number of (row, position) pairs inside the oracle's extents."""
+    return int(expected_row_ends(w).astype(np.int64).sum())
+
+
 def to_device(w: synth.Workload):
     d = dev()
     return dict(q=w.q.to(d), kv=w.kv_fused.to(d), weights=w.weights.to(d),
@@ -54,12 +65,15 @@ def check_logits(w: synth.Workload, got_t: torch.Tensor, ref: np.ndarray, tol: n
     """Element-wise check of every in-extent score; zero-length requests' rows untouched;
     columns at or past seq_lens[b] untouched (this build writes only p < seq_lens[b])."""
     got = got_t.cpu().double().numpy()
-    re = w.row_ends().numpy()
+    re = expected_row_ends(w)
     worst = 0.0
     n_checked = 0
     for r in range(w.rows):
         L = int(w.seq_lens[r // w.next_n])
         e = int(re[r])
+        # The oracle leaves exactly the columns outside the row's extent unset (NaN).
+        assert np.isfinite(ref[r, :e]).all() and np.isnan(ref[r, e:]).all(), \
+            f"row {r}: the oracle's logits disagree with its own extent {e}"
         if e:
             err = np.abs(got[r, :e] - ref[r, :e])
             lim = REL * tol[r, :e] + ABS

@@ -11,7 +11,7 @@ import torch
 import oracle
 import paged_fp8_mqa_gb300 as idx
 from paged_fp8_mqa_gb300 import synth
-from gpu_cases import (check_selection, gpu_logits, gpu_select, kth_values, selected_from_slots,
+from gpu_cases import (expected_row_ends, expected_scores, check_selection, gpu_logits, gpu_select, kth_values, selected_from_slots,
                        to_device)
 
 pytestmark = pytest.mark.gpu
@@ -54,7 +54,7 @@ def compare(w, logits, thr, top_k, capacity, num_sms=0, t=None):
     """Fused vs two-stage on the same thresholds; returns the number of repaired rows."""
     t = t or to_device(w)
     lc = logits.cpu().numpy()
-    re = w.row_ends().numpy()
+    re = expected_row_ends(w)
     row_ends = torch.from_numpy(re).to(torch.int32).cuda()
     two = gpu_select(logits, row_ends, thr, top_k, capacity, w.max_seq_len)
     fused = gpu_fused(w, t, thr, top_k, capacity, num_sms=num_sms)
@@ -103,7 +103,7 @@ def test_fused_matches_two_stage(next_n, block_size, lens, top_k, capacity):
     t = to_device(w)
     logits, _ = gpu_logits(w, fill=0.0, tensors=t)
     lc = logits.cpu().numpy()
-    re = w.row_ends().numpy()
+    re = expected_row_ends(w)
     for name, thr in _threshold_variants(lc, re, top_k, seed=next_n).items():
         repaired = compare(w, logits, thr, top_k, capacity, t=t)
         if name == "inf":
@@ -115,7 +115,7 @@ def test_fused_full_workloads(name):
     w = synth.WORKLOADS[name]()
     t = to_device(w)
     logits, _ = gpu_logits(w, fill=0.0, tensors=t)
-    re = w.row_ends().numpy()
+    re = expected_row_ends(w)
     kth = torch.from_numpy(kth_values(logits.cpu().double().numpy(), re, w.top_k))
     thr = (synth.thresholds_below_kth(w, kth) if name == "long_select"
            else synth.thresholds_scaled_kth(w, kth))
@@ -136,7 +136,7 @@ def test_fused_runs_over_several_tile_lists(num_sms):
     t = to_device(w)
     logits, _ = gpu_logits(w, fill=0.0, tensors=t)
     lc = logits.cpu().numpy()
-    variants = _threshold_variants(lc, w.row_ends().numpy(), 32, seed=num_sms)
+    variants = _threshold_variants(lc, expected_row_ends(w), 32, seed=num_sms)
     for thr in (variants["kth"], variants["mixed"]):
         compare(w, logits, thr, 32, 40, num_sms=num_sms, t=t)
 
@@ -148,7 +148,7 @@ def test_fused_without_arrivals_counts_only():
     t = to_device(w)
     logits, _ = gpu_logits(w, fill=0.0, tensors=t)
     lc = logits.cpu().numpy()
-    re = w.row_ends().numpy()
+    re = expected_row_ends(w)
     top_k, capacity = 128, 200
     for thr in _threshold_variants(lc, re, top_k, seed=9).values():
         res = gpu_fused(w, t, thr, top_k, capacity, repair=False)
@@ -177,7 +177,7 @@ def test_fused_graph_replay_and_repeat():
     t = to_device(w)
     logits, _ = gpu_logits(w, fill=0.0, tensors=t)
     lc = logits.cpu().numpy()
-    re = w.row_ends().numpy()
+    re = expected_row_ends(w)
     top_k, capacity = 100, 120
     thr0 = _threshold_variants(lc, re, top_k, seed=4)["mixed"].cuda()
     d = t["q"].device
@@ -233,7 +233,7 @@ def test_fused_empty_and_short_requests(next_n):
         thr = torch.full((w.rows,), math.inf)
         compare(w, logits, thr, 16, 15, t=t)
         fused = gpu_fused(w, t, thr, 16, 15)
-        re = w.row_ends().numpy()
+        re = expected_row_ends(w)
         for r in range(w.rows):
             assert fused["ranges"][1, r] - fused["ranges"][0, r] == min(int(re[r]), 16)
 
@@ -244,7 +244,7 @@ def test_fused_32_heads(next_n):
     t = to_device(w)
     logits, _ = gpu_logits(w, fill=0.0, tensors=t)
     lc = logits.cpu().numpy()
-    for thr in _threshold_variants(lc, w.row_ends().numpy(), 64, seed=next_n).values():
+    for thr in _threshold_variants(lc, expected_row_ends(w), 64, seed=next_n).values():
         compare(w, logits, thr, 64, 63, t=t)
 
 
@@ -255,5 +255,5 @@ def test_fused_head_dim_64(next_n, heads):
     t = to_device(w)
     logits, _ = gpu_logits(w, fill=0.0, tensors=t)
     lc = logits.cpu().numpy()
-    for thr in _threshold_variants(lc, w.row_ends().numpy(), 64, seed=next_n).values():
+    for thr in _threshold_variants(lc, expected_row_ends(w), 64, seed=next_n).values():
         compare(w, logits, thr, 64, 63, t=t)

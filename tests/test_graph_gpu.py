@@ -6,7 +6,7 @@ import torch
 
 import paged_fp8_mqa_gb300 as idx
 from paged_fp8_mqa_gb300 import synth
-from gpu_cases import (check_logits, check_selection, kth_values, oracle_logits_cached,
+from gpu_cases import (expected_row_ends, expected_scores, check_logits, check_selection, kth_values, oracle_logits_cached,
                        selected_from_slots)
 
 pytestmark = pytest.mark.gpu
@@ -18,7 +18,7 @@ def test_serving_indexer_graph_replay():
     q, kv, wt = w.q.to(d), w.kv_fused.to(d), w.weights.to(d)
     bt, sl = w.block_tables.to(d), w.seq_lens.to(d)
     rows, pad = w.rows, idx.idx_padded_seq_len(w.max_seq_len)
-    kth = torch.from_numpy(kth_values(ref, w.row_ends().numpy(), w.top_k))
+    kth = torch.from_numpy(kth_values(ref, expected_row_ends(w), w.top_k))
     thr0 = synth.thresholds_scaled_kth(w, kth)
     out = torch.zeros(rows, pad, device=d)
     row_ends = torch.zeros(rows, dtype=torch.int32, device=d)
@@ -52,24 +52,24 @@ def test_serving_indexer_graph_replay():
             import oracle
             ref, tol = oracle.paged_logits(w.q, w.kv_fused, w.weights, w.block_tables,
                                            w.seq_lens, w.max_seq_len, block_size=w.block_size)
-            kth = torch.from_numpy(kth_values(ref, w.row_ends().numpy(), w.top_k))
+            kth = torch.from_numpy(kth_values(ref, expected_row_ends(w), w.top_k))
             thr0 = synth.thresholds_scaled_kth(w, kth)
         thr.copy_(thr0.to(d))
         out.zero_()
         graph.replay()
         torch.cuda.synchronize()
-        assert (row_ends.cpu() == w.row_ends()).all()
+        assert (row_ends.cpu().numpy() == expected_row_ends(w)).all()
         check_logits(w, out, ref, tol, untouched_fill_nan=False)
         res = {"thresholds": thr.cpu().numpy(), "counters": counters.cpu().numpy(),
                "candidates": cand.cpu().numpy(), "arrivals": arrivals.cpu().numpy(),
                "ranges": ranges.cpu().numpy()}
-        check_selection(out.cpu().numpy(), w.row_ends().numpy(), w.top_k, w.capacity, res,
+        check_selection(out.cpu().numpy(), expected_row_ends(w), w.top_k, w.capacity, res,
                         thr0.numpy())
         # Eager run on the same inputs gives bit-identical logits and the same selection.
         graph_logits = out.clone()
         def selection():
             c, rg, lc = cand.cpu().numpy(), ranges.cpu().numpy(), out.cpu().numpy()
-            k = np.minimum(w.row_ends().numpy(), w.top_k)
+            k = np.minimum(expected_row_ends(w), w.top_k)
             return [selected_from_slots(lc[r], c[r], rg[0, r], rg[1, r], int(k[r])).tolist()
                     for r in range(rows)]
         graph_sel = selection()

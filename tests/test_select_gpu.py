@@ -8,7 +8,7 @@ import torch
 import oracle
 import paged_fp8_mqa_gb300 as idx
 from paged_fp8_mqa_gb300 import synth
-from gpu_cases import (check_selection, gpu_logits, gpu_select, kth_values, oracle_logits_cached,
+from gpu_cases import (expected_row_ends, expected_scores, check_selection, gpu_logits, gpu_select, kth_values, oracle_logits_cached,
                        selected_from_slots)
 
 pytestmark = pytest.mark.gpu
@@ -24,7 +24,7 @@ def _clean_status():
 def _logits_and_thresholds(name):
     w, ref, _ = oracle_logits_cached(name)
     got, row_ends = gpu_logits(w, fill=0.0)
-    re = w.row_ends().numpy()
+    re = expected_row_ends(w)
     kth = torch.from_numpy(kth_values(ref, re, w.top_k))
     if name == "long_select":
         thr = synth.thresholds_below_kth(w, kth)
@@ -38,7 +38,7 @@ def test_full_workload_selection(name):
     w, logits, row_ends, thr = _logits_and_thresholds(name)
     res = gpu_select(logits, row_ends, thr.cuda(), w.top_k, w.capacity, w.max_seq_len)
     lc = logits.cpu().numpy()
-    repaired = check_selection(lc, w.row_ends().numpy(), w.top_k, w.capacity, res, thr.numpy())
+    repaired = check_selection(lc, expected_row_ends(w), w.top_k, w.capacity, res, thr.numpy())
     if name == "long_select":
         assert repaired >= 10  # the ten rows forced to +inf at least
 
@@ -46,7 +46,7 @@ def test_full_workload_selection(name):
 def test_any_threshold_gives_the_same_selection():
     w, logits, row_ends, thr = _logits_and_thresholds("long_select")
     lc = logits.cpu().numpy()
-    re = w.row_ends().numpy()
+    re = expected_row_ends(w)
     sets = []
     g = torch.Generator().manual_seed(5)
     variants = [thr, torch.full_like(thr, math.inf), torch.full_like(thr, -math.inf),
@@ -115,7 +115,7 @@ def test_classification_only_slots():
     at the slot positions the select's Parameters give, each holding its key and score bits."""
     w, logits, row_ends, thr = _logits_and_thresholds("serving")
     lc = logits.cpu().numpy()
-    re = w.row_ends().numpy()
+    re = expected_row_ends(w)
     res = gpu_select(logits, row_ends, thr.cuda(), w.top_k, w.capacity, w.max_seq_len,
                      repair=False)
     nc, nt, _ = oracle.select_classify(lc, re, thr.numpy(), w.top_k, w.capacity)
@@ -155,7 +155,7 @@ def test_arrivals_stay_zero_across_calls():
         c = cand.cpu().numpy()
         rg = ranges.cpu().numpy()
         lc = logits.cpu().numpy()
-        k = np.minimum(w.row_ends().numpy(), w.top_k)
+        k = np.minimum(expected_row_ends(w), w.top_k)
         sel = [selected_from_slots(lc[r], c[r], rg[0, r], rg[1, r], int(k[r])).tolist()
                for r in range(rows)]
         first = first or sel

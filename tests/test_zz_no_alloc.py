@@ -17,7 +17,7 @@ import torch
 
 import paged_fp8_mqa_gb300 as idx
 from paged_fp8_mqa_gb300 import synth
-from gpu_cases import (check_selection, gpu_logits, gpu_select, kth_values, oracle_logits_cached,
+from gpu_cases import (expected_row_ends, expected_scores, check_selection, gpu_logits, gpu_select, kth_values, oracle_logits_cached,
                        selected_from_slots)
 
 pytestmark = pytest.mark.gpu
@@ -56,7 +56,7 @@ def test_static_select_matches_workspace_select_on_two_calls():
     for name in ("long_select", "serving"):  # two calls in a row, different row counts
         w, ref, _ = oracle_logits_cached(name)
         logits, row_ends = gpu_logits(w, fill=0.0)
-        re = w.row_ends().numpy()
+        re = expected_row_ends(w)
         kth = torch.from_numpy(kth_values(ref, re, w.top_k))
         thr = (synth.thresholds_below_kth(w, kth) if name == "long_select"
                else synth.thresholds_scaled_kth(w, kth))
