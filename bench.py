@@ -48,6 +48,60 @@ def load_peaks() -> dict:
             "source": "fallback"}
 
 
+def load_fp8_peak() -> dict | None:
+    """The dense e4m3 tensor peak measured on the GB300s (``--measure-fp8-peak``,
+    committed under profiles/), or None."""
+    path = os.path.join(ROOT, "profiles", "fp8_peak.json")
+    if not os.path.exists(path):
+        return None
+    return json.load(open(path))
+
+
+def measure_fp8_peak(dev, seconds: float = 4.0) -> dict:
+    """Dense e4m3 x e4m3 -> bf16 GEMM throughput of the library GEMM (torch._scaled_mm,
+    8192^3, 2*N^3 flops): best of 10 single calls (burst) and the mean over a loop of about
+    `seconds` (sustained, under the power cap), with the clocks sampled meanwhile."""
+    n = 8192
+    g = torch.Generator(device=dev).manual_seed(0)
+    a = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+    one = torch.ones((), device=dev, dtype=torch.float32)
+
+    def mm():
+        return torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16,
+                                use_fast_accum=True)
+
+    for _ in range(5):
+        mm()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mm()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    iters = max(10, int(seconds * 1e3 / best))
+    e0.record()
+    for _ in range(iters):
+        mm()
+    e1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    sustained = e0.elapsed_time(e1) / iters
+    flops = 2.0 * n ** 3
+    return {"fp8_tflops": flops / (best * 1e-3) / 1e12,
+            "fp8_tflops_sustained": flops / (sustained * 1e-3) / 1e12,
+            "how": "torch._scaled_mm e4m3 x e4m3 -> bf16, 8192^3 (2*N^3 flops), use_fast_accum; "
+                   f"best of 10 (burst) and the mean of {iters} back-to-back calls (sustained)",
+            "gpu": torch.cuda.get_device_name(dev), "torch": torch.__version__,
+            "clocks_sustained": clocks}
+
+
 def algorithmic(w: synth.Workload) -> dict:
     """Per-launch algorithmic work: KV values + scales of every valid position (132 B each),
     the logits written (4 B per valid score), q and w; MMA flops 2*64*128 per score."""
@@ -293,6 +347,37 @@ def time_fused(w, t, steps, warmup, stream) -> dict:
                     "(launched every step, empty when nothing needs a repair)"}
 
 
+def time_selecting(name: str, dev, steps: int, warmup: int, stream, peaks: dict) -> dict:
+    """A workload with a top-k (long_select or serving), timed like the headline: the two-stage
+    step (counter and threshold reset, logits, threshold select with its repair) over K
+    back-to-back steps; the select launch alone; the fused score + select step with the
+    workload's thresholds; and both steps again with thresholds at which every row fits."""
+    w = make(name)
+    t = device_inputs(w, dev)
+    t["select"] = selection_inputs(w, t, dev)
+    alg = algorithmic(w)
+    two, _ = time_device(w, t, steps, warmup, stream)
+    single = time_launch_events(w, t, min(steps, 100), stream)
+    sel = time_select(w, t, stream, min(steps, 200))
+    fused = time_fused(w, t, steps, warmup, stream)
+    s = t["select"]
+    saved, s["thr0"] = s["thr0"], s["thr_fit"]
+    two_fit, _ = time_device(w, t, steps, warmup, stream)
+    fused_fit = time_fused(w, t, steps, warmup, stream)
+    s["thr0"] = saved
+    t_roof = alg["kv_bytes"] / (peaks["hbm_gbs"] * 1e9) * 1e3
+    return {"value": alg["scores"] / (two * 1e-3) / 1e9, "unit": UNIT,
+            "config": workload_config(w), "ms_per_step": two,
+            "single_step_ms": single, "select_ms_per_launch": sel["ms_per_launch"],
+            "fused_ms_per_step": fused["ms_per_step"],
+            "all_rows_fit": {"ms_per_step": two_fit, "fused_ms_per_step": fused_fit["ms_per_step"],
+                             "thresholds": "each row's K'-th largest score"},
+            "kv_roofline_time_ms": t_roof, "kv_roofline_frac": t_roof / two,
+            "note": "step = counter/threshold reset + logits + select (2 kernels, plus 2 small "
+                    "torch fills); fused = the same outputs through idx_indexer_threshold_select "
+                    "(3 kernels)"}
+
+
 def time_mxfp4(w: synth.Workload, dev, steps: int, warmup: int, stream, peaks: dict) -> dict:
     """The MXFP4 variant on the same lengths, pages and weights (q and K drawn anew and
     quantized): staging + FP8 logits per step, three MXFP4 pools in rotation (each below L2 on
@@ -527,7 +612,12 @@ def main() -> None:
     ap.add_argument("--workload", default="decode", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--measure-fp8-peak", action="store_true",
+                    help="print the dense e4m3 GEMM peak of this GPU as one JSON line and exit")
     args = ap.parse_args()
+    if args.measure_fp8_peak:
+        print(json.dumps(measure_fp8_peak(torch.device("cuda", 0))), flush=True)
+        return
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -579,7 +669,11 @@ def main() -> None:
     e2e_value = reduce_sum(alg["scores"] / (e2e_ms * 1e-3) / 1e9)
 
     hbm_ach = alg["bytes"] / (mean_ms * 1e-3) / 1e9
-    fp8_peak = 2.0 * peaks["bf16_tflops"]  # fp8 dense = 2x bf16 (nominal 4.5 / 2.25 PFLOP/s)
+    fp8 = load_fp8_peak()
+    if fp8 is not None:
+        fp8_peak, fp8_source = fp8["fp8_tflops"], "measured e4m3 GEMM burst (profiles/fp8_peak.json)"
+    else:
+        fp8_peak, fp8_source = 2.0 * peaks["bf16_tflops"], peaks["source"] + " bf16 x 2 (nominal ratio)"
     t_hbm = alg["bytes"] / (peaks["hbm_gbs"] * 1e9)
     t_mma = alg["flops"] / (fp8_peak * 1e12)
     bound = "hbm" if t_hbm >= t_mma else "tensor"
@@ -588,12 +682,20 @@ def main() -> None:
             "peak": peaks["hbm_gbs"] if bound == "hbm" else fp8_peak,
             "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
             "traffic": measured_traffic(args.workload),
-            "peak_source": peaks["source"] + (" (fp8 = 2 x bf16)" if bound == "tensor" else ""),
+            "peak_source": (peaks["source"] + " copy bandwidth (MEASURED_PEAKS.json)")
+            if bound == "hbm" else fp8_source,
+            "fp8_peak_tflops": fp8_peak, "fp8_peak_source": fp8_source,
             "algorithmic_bytes": alg["bytes"], "kv_bytes": alg["kv_bytes"],
             "flops": alg["flops"],
             "roofline_time_ms": max(t_hbm, t_mma) * 1e3,
             "roofline_frac": max(t_hbm, t_mma) * 1e3 / mean_ms}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    # The survey's definition: KV bytes only (132 B per position) against the FP8 MMA time;
+    # and the same for a launch timed on its own (no overlap with a neighbouring launch).
+    t_kv = max(alg["kv_bytes"] / (peaks["hbm_gbs"] * 1e9), t_mma) * 1e3
+    roof["kv_roofline_time_ms"] = t_kv
+    roof["frac_kv"] = t_kv / mean_ms
+    roof["frac_kv_single_launch"] = t_kv / event_ms
 
     secondary = {}
     if not args.no_secondary and args.workload == "decode":
@@ -602,13 +704,22 @@ def main() -> None:
         t2 = device_inputs(w2, dev)
         m2, _ = time_device(w2, t2, max(3, min(500, args.steps)), args.warmup, stream)
         a2 = algorithmic(w2)
+        e2 = time_launch_events(w2, t2, min(args.steps, 200), stream)
         r2 = max(a2["bytes"] / (peaks["hbm_gbs"] * 1e9), a2["flops"] / (fp8_peak * 1e12)) * 1e3
+        k2 = max(a2["kv_bytes"] / (peaks["hbm_gbs"] * 1e9), a2["flops"] / (fp8_peak * 1e12)) * 1e3
         secondary["mtp"] = {"value": a2["scores"] / (m2 * 1e-3) / 1e9, "unit": UNIT,
-                            "ms_per_launch": m2, "roofline_time_ms": r2,
-                            "roofline_frac": r2 / m2,
+                            "ms_per_launch": m2, "single_launch_ms": e2,
+                            "roofline_time_ms": r2, "roofline_frac": r2 / m2,
+                            "kv_roofline_time_ms": k2, "frac_kv": k2 / m2,
+                            "bound_kv": "hbm" if a2["kv_bytes"] / (peaks["hbm_gbs"] * 1e9) >=
+                            a2["flops"] / (fp8_peak * 1e12) else "tensor",
                             "hbm_gbs": a2["bytes"] / (m2 * 1e-3) / 1e9,
                             "tflops": a2["flops"] / (m2 * 1e-3) / 1e12}
         del t2
+        # The workloads with a top-k: long context (8 x 131072, next_n 2) and the serving mix.
+        for name in ("long_select", "serving"):
+            secondary[name] = time_selecting(name, dev, max(3, min(200, args.steps)),
+                                             args.warmup, stream, peaks)
         # The MXFP4 variant on the decode workload's shape.
         secondary["mxfp4"] = time_mxfp4(w, dev, max(3, min(300, args.steps)), args.warmup,
                                         stream, peaks)

@@ -13,7 +13,8 @@
  * Conventions shared by every entry point
  *   - Pointers marked "device" are caller-owned device memory; the library never allocates,
  *     frees or synchronises, so every call can be captured in a CUDA graph once it has run
- *     eagerly one time (that first call loads the kernels).  `stream` is a cudaStream_t
+ *     eagerly one time (that first call loads the kernels); this header makes no statement
+ *     either way about capturing idx_threshold_select_static.  `stream` is a cudaStream_t
  *     (NULL = the legacy default stream).
  *   - Return value: IDX_OK, or an error code; idx_last_error() then describes it.  On any
  *     error other than IDX_CUDA nothing has been launched.
@@ -310,6 +311,19 @@ int idx_indexer_threshold_select(const uint8_t *q, const uint8_t *kv_fused, int6
                                  int32_t *candidates, int32_t top_k, int32_t capacity,
                                  int32_t *arrivals, int32_t *ranges, float *scratch,
                                  int64_t scratch_row_stride, void *stream);
+
+/*
+ * idx_debug_withhold_first_tile -- fault injection for testing the time-limited pipeline waits
+ * (the pages have no counterpart).  From the next logits launch on (idx_logits_fp8,
+ * idx_logits_mxfp4, and the scoring passes of idx_indexer_threshold_select), the CTA of index
+ * `cta` of the persistent grid issues none of the copies of the first tile of its run, so the
+ * waits on that tile run out after their limit (one second): that CTA's roles give up, it drains
+ * every copy it did issue, frees its tensor memory and exits, and IDX_DEV_WAIT_TIMEOUT is raised
+ * (idx_device_status).  The launch's output is then incomplete.  `cta` = -1 switches it off (the
+ * default).  Synchronous; for tests only, never for production use.
+ * Returns IDX_INVALID_ARG for cta outside -1 .. 1023.
+ */
+int idx_debug_withhold_first_tile(int32_t cta);
 
 /*
  * Reads (and, if clear != 0, resets) the OR of the device-side status bits (IDX_DEV_*) that

@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
                                    c.c_int64, P]
     L.idx_device_status.restype = c.c_int
     L.idx_device_status.argtypes = [P, c.c_int32]
+    L.idx_debug_withhold_first_tile.restype = c.c_int
+    L.idx_debug_withhold_first_tile.argtypes = [c.c_int32]
     _lib = L
     return L
 
@@ -184,6 +186,10 @@ def idx_logits_mxfp4(q, q_sf, kv_fused, num_blocks, block_size, weights, block_t
                                   seq_lens_stride, batch, next_n, num_heads, head_dim,
                                   max_seq_len, num_sms, output_dtype, out, out_row_stride,
                                   row_ends_out, workspace, workspace_bytes, stream)
+
+
+def idx_debug_withhold_first_tile(cta: int) -> None:
+    _check(lib().idx_debug_withhold_first_tile(int(cta)))
 
 
 def idx_device_status(clear: bool = False) -> int:

@@ -543,6 +543,14 @@ IDX_EXPORT int idx_threshold_select_static(const float *logits, int64_t logits_r
   return IDX_OK;
 }
 
+IDX_EXPORT int idx_debug_withhold_first_tile(int32_t cta) {
+  g_error.clear();
+  if (cta < -1 || cta >= 1024) return fail(IDX_INVALID_ARG, "cta must be -1 .. 1023");
+  const cudaError_t e = idx::logits_withhold(cta);
+  if (e != cudaSuccess) return cuda_fail(e, "fault-injection flag copy");
+  return IDX_OK;
+}
+
 IDX_EXPORT int idx_device_status(int32_t *status_out, int32_t clear) {
   g_error.clear();
   if (status_out == nullptr) return fail(IDX_INVALID_ARG, "status_out is NULL");

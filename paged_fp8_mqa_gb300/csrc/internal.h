@@ -96,6 +96,7 @@ cudaError_t launch_logits_d64(int next_n, LogitsOut mode, const CUtensorMap &kv_
                               const CUtensorMap &q_map, const LogitsArgs &args, int num_ctas,
                               cudaStream_t stream);
 cudaError_t logits_d64_status(int32_t *value, bool clear);
+cudaError_t logits_d64_withhold(int32_t cta);
 
 // Launches the standalone schedule kernel.
 cudaError_t launch_schedule(const int32_t *seq_lens, int64_t stride, int batch, int num_ctas,
@@ -143,6 +144,9 @@ cudaError_t launch_threshold_select_static(SelectArgs args, cudaStream_t stream)
 
 // Device-side status words of each translation unit (IDX_DEV_* bits).
 cudaError_t logits_status(int32_t *value, bool clear);
+// (testing only) The logits CTA that withholds its first tile's copies (-1: none), in both
+// logits translation units.
+cudaError_t logits_withhold(int32_t cta);
 cudaError_t select_status(int32_t *value, bool clear);
 
 }  // namespace idx

@@ -18,4 +18,6 @@ cudaError_t launch_logits_d64(int next_n, LogitsOut mode, const CUtensorMap &kv_
 
 cudaError_t logits_d64_status(int32_t *value, bool clear) { return read_unit_status(value, clear); }
 
+cudaError_t logits_d64_withhold(int32_t cta) { return set_unit_withhold(cta); }
+
 }  // namespace idx

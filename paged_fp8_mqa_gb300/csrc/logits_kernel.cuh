@@ -67,6 +67,10 @@ namespace {
 
 // Device-side status bits (IDX_DEV_*) of the kernels of the including translation unit.
 __device__ int g_logits_status;
+// Fault injection for testing the time-limited waits (idx_debug_withhold_first_tile): the CTA
+// with this index issues none of its first tile's copies, so the waits on that tile run out.
+// -1 (the default): off.
+__device__ int g_withhold_cta = -1;
 
 constexpr int kEpiWarpBase = 2;                  // epilogue warps 2, 3, ...
 constexpr int kMaxList = 256;                     // tiles per tile list
@@ -587,6 +591,8 @@ __global__ void __launch_bounds__(Cfg<NN, H, D>::THREADS, 1)
       if (lane == 0 && ok) {
         const uint64_t pol_stream = l2_policy_evict_first();
         const uint64_t pol_keep = l2_policy_evict_last();
+        // (testing only) The first tile whose copies are never issued, or -1.
+        const int withhold = g_withhold_cta == static_cast<int>(blockIdx.x) ? 0 : -1;
         const auto produce = [&](auto page_tokens) {
           constexpr int BS = decltype(page_tokens)::value;
           constexpr uint32_t kValue = BS * D, kScale = BS * 4;
@@ -608,16 +614,18 @@ __global__ void __launch_bounds__(Cfg<NN, H, D>::THREADS, 1)
             }
             const uint32_t pages = (r.z >= 0 ? 1u : 0u) + (r.w >= 0 ? 1u : 0u) +
                                    (hi.x >= 0 ? 1u : 0u) + (hi.y >= 0 ? 1u : 0u);
-            mbar_arrive_expect_tx(&full[stage], (kValue + kScale) * pages);
-            // The first ACC tiles' accumulators were never read: stand in for their readers.
-            if (kbase + i < C::ACC) mbar_arrive_count(&full[stage], C::TEAM_WARPS);
-            uint8_t *dst = s_kv + stage * C::STAGE_BYTES;
-            float *sdst = s_scale + ((kbase + i) % C::SCALE_SLOTS) * kTileTokens;
-            page(0, r.z, dst, sdst);
-            if (BS <= 64) page(1, r.w, dst, sdst);
-            if (BS == 32) {
-              page(2, hi.x, dst, sdst);
-              page(3, hi.y, dst, sdst);
+            if (kbase + i != withhold) {
+              mbar_arrive_expect_tx(&full[stage], (kValue + kScale) * pages);
+              // The first ACC tiles' accumulators were never read: stand in for their readers.
+              if (kbase + i < C::ACC) mbar_arrive_count(&full[stage], C::TEAM_WARPS);
+              uint8_t *dst = s_kv + stage * C::STAGE_BYTES;
+              float *sdst = s_scale + ((kbase + i) % C::SCALE_SLOTS) * kTileTokens;
+              page(0, r.z, dst, sdst);
+              if (BS <= 64) page(1, r.w, dst, sdst);
+              if (BS == 32) {
+                page(2, hi.x, dst, sdst);
+                page(3, hi.y, dst, sdst);
+              }
             }
             if (++stage == C::STAGES) {  // (before the q wait, so a timeout there still drains)
               stage = 0;
@@ -974,6 +982,11 @@ cudaError_t launch_shape(int next_n, LogitsOut mode, const CUtensorMap &kv_map,
       return launch_out<H, D, SelectOut>(next_n, kv_map, q_map, args, num_ctas, stream);
   }
   return cudaErrorInvalidValue;
+}
+
+// Sets this translation unit's fault-injection CTA (-1: off); synchronous.
+inline cudaError_t set_unit_withhold(int32_t cta) {
+  return cudaMemcpyToSymbol(g_withhold_cta, &cta, sizeof(int32_t));
 }
 
 // Reads (and, if `clear`, resets) this translation unit's status bits.
