@@ -44,6 +44,7 @@ extern "C" {
 /* Element types of idx_logits_fp8's output (the pages' output_dtype). */
 #define IDX_DTYPE_F32 0 /* float32 (the default on the pages) */
 #define IDX_DTYPE_F16 1 /* IEEE binary16 */
+#define IDX_DTYPE_BF16 2 /* bfloat16 (idx_logits_mxfp4 with head_dim 128 only; its pages' default) */
 
 /* Device-side status bits (idx_device_status). */
 #define IDX_DEV_WAIT_TIMEOUT 1 /* a pipeline wait gave up after its time limit */

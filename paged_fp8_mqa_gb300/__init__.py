@@ -25,6 +25,7 @@ IDX_CUDA = 3
 IDX_CONTRACT = 4
 IDX_DTYPE_F32 = 0
 IDX_DTYPE_F16 = 1
+IDX_DTYPE_BF16 = 2
 IDX_DEV_WAIT_TIMEOUT = 1
 IDX_DEV_BAD_PAGE = 2
 IDX_DEV_INEXACT_SCALE = 4
@@ -277,7 +278,8 @@ def logits_mxfp4(q, q_sf, kv_fused, weights, block_tables, seq_lens, max_seq_len
     [B, next_n, H, D/32] or its int32 view [B, next_n, H] (UE8M0); kv_fused: uint8 whose leading
     dim is the block count, block_size*(D/2 + D/32) bytes per block; weights float32
     [B*next_n, H]; block_tables, seq_lens as for ``logits_fp8``.  output_dtype: torch.float32
-    (default here; the pages default to bfloat16, which is not offered) or torch.float16.
+    (the default of this binding, the path checked against the oracle element by element),
+    torch.float16, or with head_dim 128 torch.bfloat16 (the pages' default for this variant).
     ``workspace`` (uint8, at least idx_mxfp4_workspace_bytes) is allocated if not given."""
     import torch
     _need(q, torch.uint8, "q", 4)
@@ -304,12 +306,13 @@ def logits_mxfp4(q, q_sf, kv_fused, weights, block_tables, seq_lens, max_seq_len
                           dtype=output_dtype or torch.float32, device=q.device)
     elif output_dtype is not None and out.dtype != output_dtype:
         raise ValueError(f"out is {out.dtype} but output_dtype is {output_dtype}")
-    _need(out, (torch.float32, torch.float16), "out", 2)
+    _need(out, (torch.float32, torch.float16, torch.bfloat16), "out", 2)
     need = idx_mxfp4_workspace_bytes(num_blocks, block_size, B, n, H, D)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     _need(workspace, torch.uint8, "workspace")
-    dtype_code = IDX_DTYPE_F16 if out.dtype == torch.float16 else IDX_DTYPE_F32
+    dtype_code = {torch.float16: IDX_DTYPE_F16, torch.bfloat16: IDX_DTYPE_BF16}.get(out.dtype,
+                                                                                  IDX_DTYPE_F32)
     _check(idx_logits_mxfp4(_ptr(q), _ptr(q_sf), _ptr(kv_fused), num_blocks, block_size,
                             _ptr(weights), _ptr(block_tables), block_tables.stride(0),
                             block_tables.shape[1], _ptr(seq_lens), seq_lens.stride(0), B, n, H, D,

@@ -258,8 +258,9 @@ IDX_EXPORT int64_t idx_mxfp4_workspace_bytes(int64_t num_blocks, int32_t block_s
     return -1;
   const auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
   const int64_t rows_heads = static_cast<int64_t>(batch) * next_n * num_heads;
-  return up(num_blocks * block_size * (head_dim + 4)) + up(rows_heads * head_dim) +
-         up(rows_heads * 4);
+  // head_dim 128: the KV pages are converted on chip, only q and the weights are staged.
+  const int64_t kv = head_dim == 128 ? 0 : up(num_blocks * block_size * (head_dim + 4));
+  return kv + up(rows_heads * head_dim) + up(rows_heads * 4);
 }
 
 IDX_EXPORT int idx_logits_mxfp4(const uint8_t *q, const uint8_t *q_sf, const uint8_t *kv_fused,
@@ -294,33 +295,82 @@ IDX_EXPORT int idx_logits_mxfp4(const uint8_t *q, const uint8_t *q_sf, const uin
   if (!aligned(q, 16) || !aligned(kv_fused, 16) || !aligned(workspace, 256) ||
       !aligned(weights, 4))
     return fail(IDX_INVALID_ARG, "q and kv_fused must be 16-byte aligned, workspace 256-byte");
+  const bool on_chip = head_dim == 128;  // the KV pages converted inside the logits kernel
+  if (output_dtype != IDX_DTYPE_F32 && output_dtype != IDX_DTYPE_F16 &&
+      !(on_chip && output_dtype == IDX_DTYPE_BF16))
+    return fail(IDX_UNSUPPORTED, "output_dtype must be IDX_DTYPE_F32, IDX_DTYPE_F16 or (head_dim "
+                                 "128) IDX_DTYPE_BF16");
+  if (out_row_stride < idx_padded_seq_len(max_seq_len) || out_row_stride % 4 != 0)
+    return fail(IDX_INVALID_ARG,
+                "out_row_stride must be >= idx_padded_seq_len(max_seq_len) and a multiple of 4");
+  if (!aligned(out, 16) || !aligned(block_tables, 4) || !aligned(seq_lens, 4) ||
+      (row_ends_out != nullptr && !aligned(row_ends_out, 4)))
+    return fail(IDX_INVALID_ARG, "out must be 16-byte aligned, int32 arguments 4-byte aligned");
+  const int64_t raw_page = static_cast<int64_t>(block_size) * (head_dim / 2 + head_dim / 32);
+  if (num_blocks > INT64_MAX / raw_page) return fail(IDX_INVALID_ARG, "num_blocks too large");
+  int32_t ctas = 0;
+  int st = resolve_sms(num_sms, &ctas);
+  if (st != IDX_OK) return st;
   if (batch == 0) return IDX_OK;
   const auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
   const int64_t rows_heads = static_cast<int64_t>(batch) * next_n * num_heads;
   uint8_t *kv8 = static_cast<uint8_t *>(workspace);
-  uint8_t *q8 = kv8 + up(num_blocks * block_size * (head_dim + 4));
+  uint8_t *q8 = kv8 + (on_chip ? 0 : up(num_blocks * block_size * (head_dim + 4)));
   float *w8 = reinterpret_cast<float *>(q8 + up(rows_heads * head_dim));
-  idx::Mxfp4Stage st{};
-  st.q4 = q;
-  st.q_sf = q_sf;
-  st.weights = weights;
-  st.kv4 = kv_fused;
-  st.block_tables = block_tables;
-  st.bt_stride = bt_row_stride;
-  st.seq_lens = seq_lens;
-  st.sl_stride = seq_lens_stride;
-  st.q8 = q8;
-  st.w8 = w8;
-  st.kv8 = kv8;
-  st.num_blocks = num_blocks;
-  st.rows_heads = static_cast<int32_t>(rows_heads);
-  st.block_size = block_size;
-  st.head_dim = head_dim;
-  st.batch = batch;
-  st.max_pages = static_cast<int32_t>((static_cast<int64_t>(max_seq_len) + block_size - 1) /
+  idx::Mxfp4Stage stg{};
+  stg.q4 = q;
+  stg.q_sf = q_sf;
+  stg.weights = weights;
+  stg.kv4 = kv_fused;
+  stg.block_tables = block_tables;
+  stg.bt_stride = bt_row_stride;
+  stg.seq_lens = seq_lens;
+  stg.sl_stride = seq_lens_stride;
+  stg.q8 = q8;
+  stg.w8 = w8;
+  stg.kv8 = kv8;
+  stg.num_blocks = num_blocks;
+  stg.rows_heads = static_cast<int32_t>(rows_heads);
+  stg.block_size = block_size;
+  stg.head_dim = head_dim;
+  stg.batch = batch;
+  stg.max_pages = static_cast<int32_t>((static_cast<int64_t>(max_seq_len) + block_size - 1) /
                                       block_size);
-  const cudaError_t e = idx::launch_mxfp4_stage(st, static_cast<cudaStream_t>(stream));
+  stg.stage_kv = !on_chip;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (on_chip && validate_requested()) {
+    st = validate_logits_contents(block_tables, bt_row_stride, bt_width, seq_lens,
+                                  seq_lens_stride, batch, max_seq_len, num_blocks, block_size, s);
+    if (st != IDX_OK) return st;
+  }
+  cudaError_t e = idx::launch_mxfp4_stage(stg, s);
   if (e != cudaSuccess) return cuda_fail(e, "MXFP4 staging launch");
+  if (on_chip) {
+    // q (staged) through TMA; the KV pages converted by the logits kernel's converter warps.
+    CUtensorMap q_map;
+    st = encode_rows(&q_map, q8, static_cast<uint64_t>(rows_heads), 128u,
+                     static_cast<uint32_t>(next_n * num_heads));
+    if (st != IDX_OK) return st;
+    idx::LogitsArgs a{};
+    a.kv = kv_fused;
+    a.weights = w8;
+    a.block_tables = block_tables;
+    a.bt_stride = bt_row_stride;
+    a.bt_width = bt_width;
+    a.seq_lens = seq_lens;
+    a.sl_stride = seq_lens_stride;
+    a.out = out;
+    a.out_stride = out_row_stride;
+    a.row_ends = row_ends_out;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.num_heads = num_heads;
+    a.head_dim = head_dim;
+    a.batch = batch;
+    e = idx::launch_logits_mxfp4(next_n, output_dtype, q_map, a, ctas, s);
+    if (e != cudaSuccess) return cuda_fail(e, "MXFP4 logits launch");
+    return IDX_OK;
+  }
   // The staged tensors are in the FP8 layouts: the FP8 logits path computes the logits.
   return idx_logits_fp8(q8, kv8, num_blocks, block_size, w8, block_tables, bt_row_stride,
                         bt_width, seq_lens, seq_lens_stride, batch, next_n, num_heads, head_dim,

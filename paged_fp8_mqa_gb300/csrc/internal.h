@@ -98,6 +98,14 @@ cudaError_t launch_logits_d64(int next_n, LogitsOut mode, const CUtensorMap &kv_
 cudaError_t logits_d64_status(int32_t *value, bool clear);
 cudaError_t logits_d64_withhold(int32_t cta);
 
+// The same kernel reading an MXFP4 KV pool (head_dim 128; a separate translation unit): q and
+// weights already staged in the FP8 layout (q_map over them), args.kv the MXFP4 pool.
+// output_dtype: IDX_DTYPE_F32, _F16 or _BF16.
+cudaError_t launch_logits_mxfp4(int next_n, int output_dtype, const CUtensorMap &q_map,
+                                const LogitsArgs &args, int num_ctas, cudaStream_t stream);
+cudaError_t logits_mx_status(int32_t *value, bool clear);
+cudaError_t logits_mx_withhold(int32_t cta);
+
 // Launches the standalone schedule kernel.
 cudaError_t launch_schedule(const int32_t *seq_lens, int64_t stride, int batch, int num_ctas,
                             int32_t *schedule, cudaStream_t stream);

@@ -23,14 +23,16 @@ cudaError_t launch_logits_fp8(int next_n, LogitsOut mode, const CUtensorMap &kv_
 cudaError_t logits_withhold(int32_t cta) {
   cudaError_t e = set_unit_withhold(cta);
   if (e == cudaSuccess) e = logits_d64_withhold(cta);
+  if (e == cudaSuccess) e = logits_mx_withhold(cta);
   return e;
 }
 
 cudaError_t logits_status(int32_t *value, bool clear) {
-  int32_t other = 0;
+  int32_t d64 = 0, mx = 0;
   cudaError_t e = read_unit_status(value, clear);
-  if (e == cudaSuccess) e = logits_d64_status(&other, clear);
-  if (e == cudaSuccess) *value |= other;
+  if (e == cudaSuccess) e = logits_d64_status(&d64, clear);
+  if (e == cudaSuccess) e = logits_mx_status(&mx, clear);
+  if (e == cudaSuccess) *value |= d64 | mx;
   return e;
 }
 

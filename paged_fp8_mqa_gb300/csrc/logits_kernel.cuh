@@ -50,6 +50,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -58,6 +59,7 @@
 
 #include "../../include/idx.h"
 #include "internal.h"
+#include "mx_convert.cuh"
 #include "ptx.cuh"
 #include "slots.cuh"
 #include "split.cuh"
@@ -81,9 +83,11 @@ constexpr int kOrdShift = 22;                     // bits 22-29: the request's o
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
 
 // next_n = NN draft slots of H heads each (H = 32 or 64), head_dim D (128 or 64): one e4m3 row
-// of q or K is one swizzle atom wide (128- or 64-byte swizzle).
-template <int NN, int H, int D>
+// of q or K is one swizzle atom wide (128- or 64-byte swizzle).  MX: the KV pool holds MXFP4
+// pages, which converter warps turn into the e4m3 tile in shared memory (D = 128 only).
+template <int NN, int H, int D, bool MX_ = false>
 struct Cfg {
+  static constexpr bool MX = MX_;
   static constexpr int N = NN * H;  // MMA N: query rows of one request
   static constexpr int R = H / 8;   // head pairs a thread holds per position and slot
   static constexpr uint32_t STAGE_BYTES = kTileTokens * D;  // a tile's values
@@ -96,9 +100,18 @@ struct Cfg {
   static constexpr int TEAMS = 2;                       // teams taking tiles in turn
   static constexpr int TEAM_WARPS = 4 * SPLIT;          // warps reading one tile
   static constexpr int EPI_WARPS = TEAMS * TEAM_WARPS;
-  static constexpr int THREADS = (kEpiWarpBase + EPI_WARPS) * 32;
+  // (MX) Converter warps.  A tile's conversion is 256 units (a token's half row: two 32-element
+  // groups); eight warps take one unit per thread, or two warps four each where the epilogue's
+  // 16 warps leave registers for only two more.
+  static constexpr int CONV_WARPS = MX ? (N >= 192 ? 2 : 8) : 0;
+  static constexpr int CONV_BASE = kEpiWarpBase + EPI_WARPS;  // first converter warp
+  static constexpr int THREADS = (kEpiWarpBase + EPI_WARPS + CONV_WARPS) * 32;
   static constexpr int SLOTS = (NN + SPLIT - 1) / SPLIT;  // draft slots per epilogue warp (max)
-  static constexpr int STAGES = N <= 128 ? 10 : (N == 192 ? 9 : 8);
+  // KV stages (e4m3 tiles the MMA reads).  MX: few, since the loads land in a ring of raw MXFP4
+  // tiles first (RAW_STAGES of RAW_BYTES: a tile's pages, packed rows then scale bytes each).
+  static constexpr int STAGES = MX ? 4 : (N <= 128 ? 10 : (N == 192 ? 9 : 8));
+  static constexpr uint32_t RAW_BYTES = MX ? kTileTokens * (D / 2 + D / 32) : 0;
+  static constexpr int RAW_STAGES = MX ? (N <= 128 ? 10 : (N == 192 ? 8 : 6)) : 0;
   static constexpr int ACC = N <= 128 ? 4 : 2;  // even: tile k's accumulator belongs to team k&1
   static constexpr int TMEM_COLS = (ACC * N <= 256) ? 256 : 512;
   static constexpr uint32_t Q_BYTES = N * D;
@@ -110,19 +123,22 @@ struct Cfg {
   // k + ACC's MMAs started, which needs tile k's epilogue to have released its accumulator, and
   // the epilogue reads its scale before that release.
   static constexpr int SCALE_SLOTS = STAGES + ACC;
-  static constexpr uint32_t OFF_SCALE = OFF_W + 2 * W_FLOATS * 4;
+  static constexpr uint32_t OFF_RAW = OFF_W + 2 * W_FLOATS * 4;
+  static constexpr uint32_t OFF_SCALE = OFF_RAW + RAW_STAGES * RAW_BYTES;
   static constexpr uint32_t OFF_LIST = OFF_SCALE + SCALE_SLOTS * kTileTokens * 4;
   static constexpr uint32_t OFF_PG2 = OFF_LIST + kMaxList * 16;  // pages 2, 3 (32-token pages)
   static constexpr uint32_t OFF_BAR = OFF_PG2 + kMaxList * 8;
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 1;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr uint32_t OFF_LEN = OFF_MISC + 64;
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 1 + 2 * RAW_STAGES;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;  // TMEM address, list length, table
+  static constexpr uint32_t OFF_LEN = OFF_MISC + 64 + 80;
   static constexpr uint32_t smem_bytes(int batch) {
     return OFF_LEN + 4u * static_cast<uint32_t>(batch) + 1024u;  // + alignment slack
   }
   static_assert(OFF_Q % 1024 == 0 && Q_BYTES % 1024 == 0, "swizzled tiles 1024-aligned");
-  static_assert(OFF_W % 16 == 0 && OFF_LIST % 16 == 0 && OFF_SCALE % 16 == 0,
+  static_assert(OFF_W % 16 == 0 && OFF_LIST % 16 == 0 && OFF_SCALE % 16 == 0 &&
+                    OFF_RAW % 16 == 0 && RAW_BYTES % 16 == 0,
                 "copy destinations 16-byte aligned");
+  static_assert(!MX || D == 128, "MXFP4 tiles: head_dim 128");
   static_assert(smem_bytes(kMaxBatch) <= 232448, "fits the 227 KiB per-CTA limit");
   static_assert(ACC * N <= TMEM_COLS && ACC % 2 == 0 && ACC <= STAGES, "accumulators");
 };
@@ -132,6 +148,7 @@ __device__ __forceinline__ void flag_error(int bits) { atomicOr(&g_logits_status
 // The output element: float32, or float16 rounded to nearest even (the pages' output_dtype).
 __device__ __forceinline__ void store_out(float *p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__half *p, float v) { *p = __float2half_rn(v); }
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
 
 // The fused score + select output ("flashinfer.sdsa.indexer_threshold_select": description):
 // instead of being stored, each score is classified against its row's threshold into the row's
@@ -392,11 +409,11 @@ __device__ __noinline__ ListResult build_list(ListCursor cur, int batch, const i
   return ListResult{cur, n};
 }
 
-template <int NN, int H, int D, typename OutT, int BS_SHIFT>
-__global__ void __launch_bounds__(Cfg<NN, H, D>::THREADS, 1)
+template <int NN, int H, int D, typename OutT, int BS_SHIFT, bool MX = false>
+__global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
     k_logits_fp8(const __grid_constant__ CUtensorMap kv_map,
                  const __grid_constant__ CUtensorMap q_map, const LogitsArgs a) {
-  using C = Cfg<NN, H, D>;
+  using C = Cfg<NN, H, D, MX>;
   constexpr bool kSelect = std::is_same<OutT, SelectOut>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -412,8 +429,12 @@ __global__ void __launch_bounds__(Cfg<NN, H, D>::THREADS, 1)
   uint64_t *q_full = done + C::STAGES;
   uint64_t *q_empty = q_full + 2;
   uint64_t *drain = q_empty + 2;
+  uint64_t *raw_full = drain + 1;                // (MX) a raw tile landed
+  uint64_t *raw_empty = raw_full + C::RAW_STAGES;  // (MX) a raw tile was converted
+  uint8_t *s_raw = smem + C::OFF_RAW;
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   int *s_count = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);  // current list length
+  uint2 *s_tab = reinterpret_cast<uint2 *>(smem + C::OFF_MISC + 64);  // (MX) 9 e4m3 tables
   int *s_len = reinterpret_cast<int *>(smem + C::OFF_LEN);
 
   const int tid = threadIdx.x;
@@ -525,8 +546,13 @@ __global__ void __launch_bounds__(Cfg<NN, H, D>::THREADS, 1)
       prefetch_tensor_map(&kv_map);
       prefetch_tensor_map(&q_map);
       for (int s = 0; s < C::STAGES; ++s) {
-        mbar_init(&full[s], 1 + C::TEAM_WARPS);  // producer + the accumulator's last readers
-        mbar_init(&done[s], 1);                   // the MMA's commit
+        // The producer (MX: the converter warps) + the accumulator's last readers.
+        mbar_init(&full[s], (C::MX ? C::CONV_WARPS : 1) + C::TEAM_WARPS);
+        mbar_init(&done[s], 1);  // the MMA's commit
+      }
+      for (int s = 0; s < C::RAW_STAGES; ++s) {
+        mbar_init(&raw_full[s], 1);
+        mbar_init(&raw_empty[s], C::CONV_WARPS);
       }
       for (int c = 0; c < 2; ++c) {
         mbar_init(&q_full[c], 1);
@@ -540,9 +566,17 @@ __global__ void __launch_bounds__(Cfg<NN, H, D>::THREADS, 1)
     tmem_relinquish();
   }
 
-  // Per-role pipeline state, kept across lists.
+  if constexpr (C::MX) {
+    const int ct = tid - C::CONV_BASE * 32;
+    if (ct >= 0 && ct < 9) s_tab[ct] = e2m1_table_entry(ct);  // read after the next barrier
+  }
+
+  // Per-role pipeline state, kept across lists.  (MX) The producer's stage / phase follow the
+  // raw ring; the converters' follow the KV stages, their rstage / rphase the raw ring.
   int stage = 0;
   uint32_t phase = 0;
+  int rstage = 0;
+  uint32_t rphase = 0;
   int qcount = 0, qb = 0;
   int kbase = 0;  // CTA-wide index of the current list's first tile
   bool ok = true;
@@ -605,31 +639,55 @@ __global__ void __launch_bounds__(Cfg<NN, H, D>::THREADS, 1)
             bulk_load(sdst + pg * BS, a.kv + static_cast<int64_t>(id) * kPage + kValue, kScale,
                       &full[stage], pol_stream);
           };
+          // (MX) A page is BS packed rows of D/2 bytes, then BS * D/32 scale bytes: one bulk
+          // copy into the raw tile, at page p's place.
+          constexpr uint32_t kRawPage = BS * (D / 2 + D / 32);
           for (int i = 0; i < n; ++i) {
             const int4 r = s_list[i];
             const int2 hi = BS == 32 ? s_pg2[i] : make_int2(-1, -1);
-            if (!mbar_wait(&done[stage], phase ^ 1, kWaitLimitNs)) {
-              ok = false;
-              break;
-            }
             const uint32_t pages = (r.z >= 0 ? 1u : 0u) + (r.w >= 0 ? 1u : 0u) +
                                    (hi.x >= 0 ? 1u : 0u) + (hi.y >= 0 ? 1u : 0u);
-            if (kbase + i != withhold) {
-              mbar_arrive_expect_tx(&full[stage], (kValue + kScale) * pages);
-              // The first ACC tiles' accumulators were never read: stand in for their readers.
-              if (kbase + i < C::ACC) mbar_arrive_count(&full[stage], C::TEAM_WARPS);
-              uint8_t *dst = s_kv + stage * C::STAGE_BYTES;
-              float *sdst = s_scale + ((kbase + i) % C::SCALE_SLOTS) * kTileTokens;
-              page(0, r.z, dst, sdst);
-              if (BS <= 64) page(1, r.w, dst, sdst);
-              if (BS == 32) {
-                page(2, hi.x, dst, sdst);
-                page(3, hi.y, dst, sdst);
+            if constexpr (C::MX) {
+              if (!mbar_wait(&raw_empty[stage], phase ^ 1, kWaitLimitNs)) {
+                ok = false;
+                break;
               }
-            }
-            if (++stage == C::STAGES) {  // (before the q wait, so a timeout there still drains)
-              stage = 0;
-              phase ^= 1;
+              if (kbase + i != withhold) {
+                mbar_arrive_expect_tx(&raw_full[stage], kRawPage * pages);
+                uint8_t *dst = s_raw + stage * C::RAW_BYTES;
+                const int ids[4] = {r.z, r.w, hi.x, hi.y};
+#pragma unroll
+                for (int pg = 0; pg < (kTileTokens / BS); ++pg)
+                  if (ids[pg] >= 0)
+                    bulk_load(dst + pg * kRawPage, a.kv + static_cast<int64_t>(ids[pg]) * kRawPage,
+                              kRawPage, &raw_full[stage], pol_stream);
+              }
+              if (++stage == C::RAW_STAGES) {
+                stage = 0;
+                phase ^= 1;
+              }
+            } else {
+              if (!mbar_wait(&done[stage], phase ^ 1, kWaitLimitNs)) {
+                ok = false;
+                break;
+              }
+              if (kbase + i != withhold) {
+                mbar_arrive_expect_tx(&full[stage], (kValue + kScale) * pages);
+                // The first ACC tiles' accumulators were never read: stand in for their readers.
+                if (kbase + i < C::ACC) mbar_arrive_count(&full[stage], C::TEAM_WARPS);
+                uint8_t *dst = s_kv + stage * C::STAGE_BYTES;
+                float *sdst = s_scale + ((kbase + i) % C::SCALE_SLOTS) * kTileTokens;
+                page(0, r.z, dst, sdst);
+                if (BS <= 64) page(1, r.w, dst, sdst);
+                if (BS == 32) {
+                  page(2, hi.x, dst, sdst);
+                  page(3, hi.y, dst, sdst);
+                }
+              }
+              if (++stage == C::STAGES) {  // (before the q wait, so a timeout there still drains)
+                stage = 0;
+                phase ^= 1;
+              }
             }
             // A new request's q and w go out after its first KV tile, whose latency is longer.
             if (r.x & kFirstFlag) {
@@ -701,6 +759,88 @@ __global__ void __launch_bounds__(Cfg<NN, H, D>::THREADS, 1)
         }
       }
       __syncwarp();
+    } else if (C::MX && warp >= C::CONV_BASE) {
+      // ============================== converters (MX) =========================================
+      // Unit u of a tile = token ct = u / 2, half hf = u % 2: the token's groups 2hf and 2hf + 1
+      // (64 elements) are converted from the raw packed row into the e4m3 row of the KV stage
+      // (128 bytes, stored with the 128-byte swizzle the TMA would have applied: 16-byte chunk c
+      // of row ct at chunk c ^ (ct % 8)), relative to the token's largest scale byte E (all four
+      // bytes are read); half 0 writes the token's float32 scale 2^(E - 127) into the tile's
+      // scale slot.  Rows of absent pages become zeros.  Then the raw tile is released and the
+      // stage marked full for the MMA (after a proxy fence: the tensor core reads shared memory
+      // through the async proxy).  The two groups of a unit are read in an order rotated by
+      // token (ct / 2), which spreads a quarter warp's reads over distinct banks.
+      if (ok) {
+        constexpr int BS = 1 << BS_SHIFT;
+        constexpr uint32_t kRawPage = BS * (D / 2 + D / 32);
+        constexpr int kConvThreads = C::CONV_WARPS * 32;
+        for (int i = 0; i < n; ++i) {
+          const int4 r = s_list[i];
+          if (!mbar_wait(&raw_full[rstage], rphase, kWaitLimitNs) ||
+              !mbar_wait(&done[stage], phase ^ 1, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          bool inexact = false;
+          for (int u = tid - C::CONV_BASE * 32; u < 2 * kTileTokens; u += kConvThreads) {
+            const int ct = u >> 1, hf = u & 1;
+            const int pg = ct >> BS_SHIFT, tt = ct & (BS - 1);
+            uint8_t *row = s_kv + stage * C::STAGE_BYTES + ct * 128;
+            const bool have = (static_cast<uint32_t>(r.x) >> (kMaskShift + pg)) & 1u;
+            if (have) {
+              const uint8_t *raw = s_raw + rstage * C::RAW_BYTES + pg * kRawPage;
+              const uint32_t sf = *reinterpret_cast<const uint32_t *>(raw + BS * (D / 2) + tt * 4);
+              int emax = 0;
+#pragma unroll
+              for (int g = 0; g < 4; ++g) emax = max(emax, static_cast<int>((sf >> (8 * g)) & 0xFFu));
+              if (((sf & 0xFFu) == 0xFFu || ((sf >> 8) & 0xFFu) == 0xFFu ||
+                   ((sf >> 16) & 0xFFu) == 0xFFu || (sf >> 24) == 0xFFu) &&
+                  r.y * kTileTokens + ct < s_len[r.x & 0xFFFF])
+                inexact = true;
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const int g = 2 * hf + ((j + (ct >> 1)) & 1);
+                const int rel = static_cast<int>((sf >> (8 * g)) & 0xFFu) - emax;
+                uint32_t out[8];
+                bool lost = false;
+                mx_group_to_e4m3(*reinterpret_cast<const uint4 *>(raw + tt * (D / 2) + 16 * g), rel,
+                                 s_tab[rel >= -8 ? -rel : 0], out, &lost);
+                if (lost && r.y * kTileTokens + ct < s_len[r.x & 0xFFFF]) inexact = true;
+                *reinterpret_cast<uint4 *>(row + (((2 * g) ^ (ct & 7)) << 4)) =
+                    make_uint4(out[0], out[1], out[2], out[3]);
+                *reinterpret_cast<uint4 *>(row + (((2 * g + 1) ^ (ct & 7)) << 4)) =
+                    make_uint4(out[4], out[5], out[6], out[7]);
+              }
+              if (hf == 0)
+                s_scale[((kbase + i) % C::SCALE_SLOTS) * kTileTokens + ct] = pow2f(emax - 127);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4 *>(row + (((4 * hf + j) ^ (ct & 7)) << 4)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+              if (hf == 0) s_scale[((kbase + i) % C::SCALE_SLOTS) * kTileTokens + ct] = 0.0f;
+            }
+          }
+          if (inexact) flag_error(IDX_DEV_INEXACT_SCALE);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&raw_empty[rstage]);
+            mbar_arrive(&full[stage]);
+            // The first ACC tiles' accumulators were never read: stand in for their readers.
+            if (warp == C::CONV_BASE && kbase + i < C::ACC)
+              mbar_arrive_count(&full[stage], C::TEAM_WARPS);
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (++rstage == C::RAW_STAGES) {
+            rstage = 0;
+            rphase ^= 1;
+          }
+        }
+      }
     } else {
       // ============================== epilogue ================================================
       const int team = (warp - kEpiWarpBase) / C::TEAM_WARPS;  // takes tiles k % TEAMS == team
@@ -908,11 +1048,14 @@ __global__ void __launch_bounds__(Cfg<NN, H, D>::THREADS, 1)
   if (__syncthreads_or(!ok)) {
     if (!ok) flag_error(IDX_DEV_WAIT_TIMEOUT);
     if (warp == 0 && lane == 0) {
-      const int tail = kbase < C::STAGES ? kbase : C::STAGES;
+      // The producer's copies land on full (MX: on raw_full, the raw ring's barriers).
+      constexpr int kRing = C::MX ? C::RAW_STAGES : C::STAGES;
+      uint64_t *landed = C::MX ? raw_full : full;
+      const int tail = kbase < kRing ? kbase : kRing;
       for (int d = 1; d <= tail; ++d) {
-        const int s = ((stage - d) % C::STAGES + C::STAGES) % C::STAGES;
+        const int s = ((stage - d) % kRing + kRing) % kRing;
         const uint32_t ph = (stage - d < 0) ? (phase ^ 1) : phase;
-        if (!mbar_wait(&full[s], ph, kWaitLimitNs)) flag_error(IDX_DEV_WAIT_TIMEOUT);
+        if (!mbar_wait(&landed[s], ph, kWaitLimitNs)) flag_error(IDX_DEV_WAIT_TIMEOUT);
       }
       if (qcount > 0 &&
           !mbar_wait(&q_full[(qcount - 1) & 1], ((qcount - 1) >> 1) & 1, kWaitLimitNs))
@@ -930,41 +1073,41 @@ __global__ void __launch_bounds__(Cfg<NN, H, D>::THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
-template <int NN, int H, int D, typename OutT, int BS_SHIFT>
+template <int NN, int H, int D, typename OutT, int BS_SHIFT, bool MX = false>
 cudaError_t launch_nn(const CUtensorMap &kv_map, const CUtensorMap &q_map, const LogitsArgs &args,
                       int num_ctas, cudaStream_t stream) {
-  using C = Cfg<NN, H, D>;
+  using C = Cfg<NN, H, D, MX>;
   const uint32_t smem = C::smem_bytes(args.batch);
   static PerDeviceOnce configured;
   const cudaError_t e = configured.run([] {
-    return cudaFuncSetAttribute(k_logits_fp8<NN, H, D, OutT, BS_SHIFT>,
+    return cudaFuncSetAttribute(k_logits_fp8<NN, H, D, OutT, BS_SHIFT, MX>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::smem_bytes(kMaxBatch));
   });
   if (e != cudaSuccess) return e;
-  return launch_dependent(k_logits_fp8<NN, H, D, OutT, BS_SHIFT>, dim3(num_ctas), dim3(C::THREADS),
-                          smem, stream, kv_map, q_map, args);
+  return launch_dependent(k_logits_fp8<NN, H, D, OutT, BS_SHIFT, MX>, dim3(num_ctas),
+                          dim3(C::THREADS), smem, stream, kv_map, q_map, args);
 }
 
-template <int H, int D, typename OutT, int BS_SHIFT>
+template <int H, int D, typename OutT, int BS_SHIFT, bool MX = false>
 cudaError_t launch_bs(int next_n, const CUtensorMap &kv_map, const CUtensorMap &q_map,
                       const LogitsArgs &args, int num_ctas, cudaStream_t stream) {
   switch (next_n) {
-    case 1: return launch_nn<1, H, D, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
-    case 2: return launch_nn<2, H, D, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
-    case 3: return launch_nn<3, H, D, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
-    case 4: return launch_nn<4, H, D, OutT, BS_SHIFT>(kv_map, q_map, args, num_ctas, stream);
+    case 1: return launch_nn<1, H, D, OutT, BS_SHIFT, MX>(kv_map, q_map, args, num_ctas, stream);
+    case 2: return launch_nn<2, H, D, OutT, BS_SHIFT, MX>(kv_map, q_map, args, num_ctas, stream);
+    case 3: return launch_nn<3, H, D, OutT, BS_SHIFT, MX>(kv_map, q_map, args, num_ctas, stream);
+    case 4: return launch_nn<4, H, D, OutT, BS_SHIFT, MX>(kv_map, q_map, args, num_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <int H, int D, typename OutT>
+template <int H, int D, typename OutT, bool MX = false>
 cudaError_t launch_out(int next_n, const CUtensorMap &kv_map, const CUtensorMap &q_map,
                        const LogitsArgs &args, int num_ctas, cudaStream_t stream) {
   switch (args.block_size) {
-    case 32: return launch_bs<H, D, OutT, 5>(next_n, kv_map, q_map, args, num_ctas, stream);
-    case 64: return launch_bs<H, D, OutT, 6>(next_n, kv_map, q_map, args, num_ctas, stream);
-    case 128: return launch_bs<H, D, OutT, 7>(next_n, kv_map, q_map, args, num_ctas, stream);
+    case 32: return launch_bs<H, D, OutT, 5, MX>(next_n, kv_map, q_map, args, num_ctas, stream);
+    case 64: return launch_bs<H, D, OutT, 6, MX>(next_n, kv_map, q_map, args, num_ctas, stream);
+    case 128: return launch_bs<H, D, OutT, 7, MX>(next_n, kv_map, q_map, args, num_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }

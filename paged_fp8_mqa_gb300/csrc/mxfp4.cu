@@ -24,6 +24,7 @@
 
 #include "../../include/idx.h"
 #include "internal.h"
+#include "mx_convert.cuh"
 #include "mxfp4.h"
 #include "ptx.cuh"
 
@@ -32,20 +33,6 @@ namespace idx {
 __device__ int g_mxfp4_status;
 
 namespace {
-
-// An E2M1 code (OCP microscaling FP4: sign, 2 exponent bits with bias 1, 1 mantissa bit) as a
-// float: built from its fields; exponent field 0 is the subnormal m/2.
-__device__ __forceinline__ float e2m1_value(uint32_t nibble) {
-  const uint32_t e = (nibble >> 1) & 3u, m = nibble & 1u;
-  const float mag = e != 0u ? __uint_as_float(((e + 126u) << 23) | (m << 22)) : 0.5f * m;
-  return (nibble & 8u) ? -mag : mag;
-}
-
-// 2^k for -149 <= k <= 127 (k = -127 .. -149 as float32 subnormals).
-__device__ __forceinline__ float pow2f(int k) {
-  return k >= -126 ? __uint_as_float(static_cast<uint32_t>(k + 127) << 23)
-                   : __uint_as_float(1u << (k + 149));
-}
 
 // Converts one row of head_dim elements (head_dim / 2 packed bytes, head_dim / 32 scale bytes)
 // into head_dim e4m3 bytes relative to the row's largest scale byte, which it returns.
@@ -65,29 +52,9 @@ __device__ __forceinline__ int stage_row(const uint8_t *packed, const uint8_t *s
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     const int rel = e[g] - emax;
-    const float f = pow2f(max(rel, -149));
-    const uint4 in = *reinterpret_cast<const uint4 *>(packed + 16 * g);  // 32 elements
-    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    const uint2 tab = rel >= -8 ? e2m1_table_entry(-rel) : make_uint2(0u, 0u);
     uint32_t out[8];
-    bool nonzero = false;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      nonzero = nonzero || (w[k] & 0x77777777u) != 0u;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const uint32_t bits = w[k] >> (16 * half);  // elements 8k+4h .. +3, low nibble first
-        uint32_t word = 0;
-#pragma unroll
-        for (int pr = 0; pr < 2; ++pr) {
-          const float2 v = make_float2(e2m1_value((bits >> (8 * pr)) & 0xFu) * f,
-                                       e2m1_value((bits >> (8 * pr + 4)) & 0xFu) * f);
-          const uint32_t two = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
-          word |= (two & 0xFFFFu) << (16 * pr);
-        }
-        out[2 * k + half] = word;
-      }
-    }
-    if (rel < -8 && nonzero) *inexact = true;
+    mx_group_to_e4m3(*reinterpret_cast<const uint4 *>(packed + 16 * g), rel, tab, out, inexact);
     uint4 *o = reinterpret_cast<uint4 *>(dst + 32 * g);
     o[0] = make_uint4(out[0], out[1], out[2], out[3]);
     o[1] = make_uint4(out[4], out[5], out[6], out[7]);
@@ -123,7 +90,11 @@ __global__ void __launch_bounds__(128) k_mxfp4_q(const Mxfp4Args a) {
   const int emax = stage_row<D>(a.q4 + static_cast<int64_t>(i) * (D / 2),
                                 a.q_sf + static_cast<int64_t>(i) * (D / 32),
                                 a.q8 + static_cast<int64_t>(i) * D, &inexact);
-  a.w8[i] = a.weights[i] * pow2f(emax - 127);
+  // The weight times the row's largest scale must stay a normal float32 for the product to be
+  // exact (a huge or tiny q scale byte could overflow or fall into the subnormals).
+  const float w = a.weights[i], w8 = w * pow2f(emax - 127), aw = fabsf(w8);
+  a.w8[i] = w8;
+  if (w != 0.0f && !(aw >= 1.17549435e-38f && aw <= 3.40282347e38f)) inexact = true;
   if (inexact) atomicOr(&g_mxfp4_status, IDX_DEV_INEXACT_SCALE);
 }
 
@@ -154,10 +125,11 @@ __global__ void k_mxfp4_kv(const Mxfp4Args a) {
 }
 
 template <int D>
-cudaError_t launch_stage(const Mxfp4Args &a, int max_pages, int batch, cudaStream_t stream) {
+cudaError_t launch_stage(const Mxfp4Args &a, int max_pages, int batch, bool stage_kv,
+                         cudaStream_t stream) {
   cudaError_t e = launch_dependent(k_mxfp4_q<D>, dim3((a.rows_heads + 127) / 128), dim3(128), 0,
                                    stream, a);
-  if (e != cudaSuccess || max_pages == 0) return e;
+  if (e != cudaSuccess || max_pages == 0 || !stage_kv) return e;
   return launch_dependent(k_mxfp4_kv<D>, dim3(max_pages, batch), dim3(a.block_size), 0, stream,
                           a);
 }
@@ -181,8 +153,8 @@ cudaError_t launch_mxfp4_stage(const Mxfp4Stage &s, cudaStream_t stream) {
   a.rows_heads = s.rows_heads;
   a.block_size = s.block_size;
   switch (s.head_dim) {
-    case 64: return launch_stage<64>(a, s.max_pages, s.batch, stream);
-    case 128: return launch_stage<128>(a, s.max_pages, s.batch, stream);
+    case 64: return launch_stage<64>(a, s.max_pages, s.batch, s.stage_kv, stream);
+    case 128: return launch_stage<128>(a, s.max_pages, s.batch, s.stage_kv, stream);
     default: return cudaErrorInvalidValue;
   }
 }

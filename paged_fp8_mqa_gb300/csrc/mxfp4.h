@@ -26,6 +26,8 @@ struct Mxfp4Stage {
   int32_t head_dim;        // 64 or 128
   int32_t batch;
   int32_t max_pages;       // ceil(max_seq_len / block_size)
+  bool stage_kv;           // false: q and the weights only (the logits kernel converts the KV
+                           // pages on chip); kv8 unused
 };
 
 cudaError_t launch_mxfp4_stage(const Mxfp4Stage &stage, cudaStream_t stream);

@@ -95,3 +95,43 @@ def test_mxfp4_wide_scale_spread_is_flagged():
         err = np.abs(g[r, :e] - ref[r, :e])
         close += int((err <= 2e-6 * tol[r, :e] + 1e-7).sum())
     assert close >= expected_scores(w) - 40  # only the spread tokens may differ
+
+
+def test_mxfp4_bfloat16_output():
+    """bfloat16 output (the pages' default for this variant; head_dim 128) equals the float32
+    result rounded to nearest even."""
+    w, m = _case(660, 2, [3000, 0, 700, 129], block_size=32)
+    got, _ = _gpu(w, m)
+    got_bf, _ = _gpu(w, m, dtype=torch.bfloat16)
+    re = expected_row_ends(w)
+    a, b = got.cpu(), got_bf.cpu()
+    for r in range(w.rows):
+        e = int(re[r])
+        assert torch.equal(a[r, :e].to(torch.bfloat16), b[r, :e]), f"row {r}"
+
+
+def test_mxfp4_bfloat16_refused_for_head_dim_64():
+    w, m = _case(661, 1, [300], head_dim=64)
+    with pytest.raises(idx.IdxError) as e:
+        _gpu(w, m, dtype=torch.bfloat16)
+    assert e.value.status == idx.IDX_UNSUPPORTED
+
+
+@pytest.mark.parametrize("byte", [254, 250, 1, 0])
+def test_mxfp4_extreme_q_scale_is_flagged(byte):
+    """A q row whose largest scale byte moves its weight out of float32's normal range (the
+    weight times 2^(E - 127) overflows or turns subnormal) raises IDX_DEV_INEXACT_SCALE; rows of
+    ordinary scales are unaffected."""
+    w, m = _case(670 + byte, 1, [600, 900])
+    q_sf = m.q_sf.clone()
+    q_sf[1, 0, 5, :] = byte  # request 1, head 5: every group at the extreme byte
+    weights = w.weights.clone()
+    weights[1, 5] = 3.0e38 if byte >= 250 else 1.0e-30
+    w2 = synth.Workload(**{**w.__dict__, "weights": weights})
+    m2 = synth.Mxfp4Inputs(q=m.q, q_sf=q_sf, kv_fused=m.kv_fused)
+    ref, tol = _oracle(w2, m2)
+    got, _ = _gpu(w2, m2)
+    assert idx.device_status(clear=True) & idx.IDX_DEV_INEXACT_SCALE
+    g = got.cpu().double().numpy()
+    e = int(expected_row_ends(w2)[0])  # request 0 is untouched by the extreme head
+    assert (np.abs(g[0, :e] - ref[0, :e]) <= 2e-6 * tol[0, :e] + 1e-7).all()

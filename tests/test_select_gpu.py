@@ -160,3 +160,39 @@ def test_arrivals_stay_zero_across_calls():
                for r in range(rows)]
         first = first or sel
         assert sel == first
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties"])
+def test_very_long_rows(kind):
+    """Rows of up to 270000 keys (17 sweeping CTAs each), repaired by each row's last CTA."""
+    rows, n = 3, 270000
+    x = _synthetic(rows, n, kind, seed=9)
+    row_ends = torch.tensor([n, 262145, 70000], dtype=torch.int32)
+    lc = x.numpy()
+    top_k, capacity = 2048, 4096
+    kth = kth_values(lc.astype(np.float64), row_ends.numpy(), top_k)
+    thr = torch.from_numpy(np.nan_to_num(kth, nan=0.0)).to(torch.float32)
+    for t in (thr, torch.full_like(thr, math.inf), thr - 1.0):
+        res = gpu_select(x.cuda(), row_ends.cuda(), t.cuda(), top_k, capacity, n)
+        check_selection(lc, row_ends.numpy(), top_k, capacity, res, t.numpy())
+
+
+@pytest.mark.parametrize("max_context", [32768, 100000, 262144])
+def test_row_lengths_around_chunks(max_context):
+    """Rows spread over 2 to 16 sweeping CTAs, with ragged ends around the chunks' borders,
+    thresholds that fit and that force the repair, and a row of many equal keys (the bin of the
+    K'-th value too full for the repair's shared-memory buffer)."""
+    g = torch.Generator().manual_seed(max_context)
+    ends = [max_context, max_context - 1, 32767, 32769, 65537, 5000, 1, 0]
+    ends = [min(e, max_context) for e in ends]
+    rows = len(ends)
+    x = torch.randn(rows, max_context, generator=g)
+    x[1, :] = torch.randint(-2, 3, (max_context,), generator=g).to(torch.float32)  # many ties
+    lc = x.numpy()
+    row_ends = torch.tensor(ends, dtype=torch.int32)
+    for top_k, capacity in ((2048, 4096), (300, 299)):
+        kth = kth_values(lc.astype(np.float64), row_ends.numpy(), top_k)
+        thr = torch.from_numpy(np.nan_to_num(kth, nan=0.0)).to(torch.float32)
+        for t in (thr, torch.full_like(thr, math.inf), thr - 0.5):
+            res = gpu_select(x.cuda(), row_ends.cuda(), t.cuda(), top_k, capacity, max_context)
+            check_selection(lc, row_ends.numpy(), top_k, capacity, res, t.numpy())
