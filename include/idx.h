@@ -126,8 +126,10 @@ int idx_schedule(const int32_t *seq_lens, int64_t seq_lens_stride, int32_t batch
  *   batch           0 .. 4096
  *   next_n          1 .. 4 (draft depth; slot t = next_n - 1 is the newest and sees the whole
  *                   sequence)
- *   num_heads, head_dim   this build supports 32 or 64 heads of 64 or 128 (IDX_UNSUPPORTED
- *                   else); kv_fused blocks are then block_size*(head_dim+4) bytes
+ *   num_heads, head_dim   this build supports 8, 16, 32 or 64 heads of 64 or 128
+ *                   (IDX_UNSUPPORTED else; the pages' restrictions num_heads % 4 == 0 and
+ *                   next_n * num_heads in [8, 256] hold for all of them); kv_fused blocks are
+ *                   then block_size*(head_dim+4) bytes
  *   block_size      32, 64 or 128 tokens per block (IDX_UNSUPPORTED else)
  *   max_seq_len     >= every seq_lens[b]
  *   schedule        device int32 [num_sms+1][2] from idx_schedule with the same seq_lens and
@@ -162,7 +164,8 @@ int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t num_blocks
  * scale 2^(e - 127), and no per-position factor.  Extents, zero-length requests, block_tables,
  * seq_lens, batch, next_n, num_heads, head_dim, block_size, max_seq_len, num_sms,
  * output_dtype, out, out_row_stride and row_ends_out are as for idx_logits_fp8 (output_dtype:
- * IDX_DTYPE_F32 or IDX_DTYPE_F16; the pages' bfloat16 default is not offered).
+ * IDX_DTYPE_F32, IDX_DTYPE_F16, or IDX_DTYPE_BF16 -- the pages' default for this variant -- with
+ * head_dim 128 and 32 or 64 heads).
  *
  *   q            device uint8 [batch, next_n, num_heads, head_dim/2], 16-byte aligned: two
  *                E2M1 codes per byte, element 2j in the low nibble of byte j
@@ -175,12 +178,16 @@ int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t num_blocks
  *   weights      device float32 [batch*next_n, num_heads]
  *   workspace    device, 256-byte aligned, at least idx_mxfp4_workspace_bytes(...) bytes
  *
- * Three launches: q (with its weights) and every KV page the batch references are staged in the
- * FP8 layouts inside the workspace, each row's largest block scale moved into the head's weight
- * or the token's float32 scale (exact: a positive power of two commutes with the ReLU), and
- * idx_logits_fp8 runs on them.  The staged values are exact while a row's block scales span at
- * most 8 binades; a row that spans more (or holds the NaN scale byte 0xFF) is rounded and raises
- * IDX_DEV_INEXACT_SCALE.
+ * Each row's largest block scale 2^(E - 127) leaves the row (exact: a positive power of two
+ * commutes with the ReLU): a q head's multiplies the head's weight, a K token's becomes the
+ * token's float32 scale, and what remains of each element is an e4m3 value.  With head_dim 128
+ * and 32 or 64 heads, two launches: q and the weights are staged in the FP8 layout inside the
+ * workspace, then the logits kernel loads the MXFP4 pages themselves and converts each tile to
+ * e4m3 in shared memory (no staged KV pool).  Otherwise three: every KV page the batch
+ * references is also staged in the workspace and idx_logits_fp8 runs on the staged tensors.
+ * Either way the conversion is exact while a row's block scales span at most 8 binades; a row
+ * that spans more (or holds the NaN scale byte 0xFF), or a q row whose weight times 2^(E - 127)
+ * leaves float32's normal range, is rounded and raises IDX_DEV_INEXACT_SCALE.
  */
 int64_t idx_mxfp4_workspace_bytes(int64_t num_blocks, int32_t block_size, int32_t batch,
                                   int32_t next_n, int32_t num_heads, int32_t head_dim);

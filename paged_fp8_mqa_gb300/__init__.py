@@ -236,7 +236,7 @@ def schedule(seq_lens, next_n: int = 1, num_sms: int = 0, out=None, stream=None)
 def logits_fp8(q, kv_fused, weights, block_tables, seq_lens, max_seq_len: int, *, out=None,
                schedule_meta=None, num_sms: int = 0, row_ends_out=None, stream=None,
                output_dtype=None):
-    """Paged FP8 MQA logits.  q: e4m3 (or its uint8 view) [B, next_n, H, D] with H = 32 or 64
+    """Paged FP8 MQA logits.  q: e4m3 (or its uint8 view) [B, next_n, H, D] with H = 8, 16, 32 or 64
     and D = 64 or 128; kv_fused: uint8 whose leading dim is the block count and whose per-block
     bytes are block_size*(D+4) (block_size 32, 64 or 128); weights: float32 [B*next_n, H]; block_tables: int32 [B, W] with unit column stride; seq_lens: int32
     [B] (any stride).  output_dtype: torch.float32 (default) or torch.float16; an `out` buffer

@@ -188,10 +188,11 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
       bt_row_stride < bt_width || block_size <= 0 || num_heads <= 0 || head_dim <= 0 ||
       next_n <= 0)
     return fail(IDX_INVALID_ARG, "negative or inconsistent size or stride");
-  if ((num_heads != 32 && num_heads != 64) || (head_dim != 64 && head_dim != 128) ||
+  if ((num_heads != 8 && num_heads != 16 && num_heads != 32 && num_heads != 64) ||
+      (head_dim != 64 && head_dim != 128) ||
       (block_size != 32 && block_size != 64 && block_size != 128))
-    return fail(IDX_UNSUPPORTED, "this build supports num_heads 32 or 64, head_dim 64 or 128, "
-                                 "block_size 32, 64 or 128");
+    return fail(IDX_UNSUPPORTED, "this build supports num_heads 8, 16, 32 or 64, head_dim 64 or "
+                                 "128, block_size 32, 64 or 128");
   if (next_n > 4) return fail(IDX_UNSUPPORTED, "next_n must be 1..4");
   if (output_dtype != IDX_DTYPE_F32 && output_dtype != IDX_DTYPE_F16)
     return fail(IDX_UNSUPPORTED, "output_dtype must be IDX_DTYPE_F32 or IDX_DTYPE_F16");
@@ -223,8 +224,10 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
                    static_cast<uint64_t>(num_blocks) * (page_bytes / head_dim),
                    static_cast<uint32_t>(head_dim), static_cast<uint32_t>(block_size));
   if (st != IDX_OK) return st;
+  // The kernel loads a request's q rows rounded up to a multiple of 16 (the MMA's N).
   st = encode_rows(&q_map, q, static_cast<uint64_t>(batch) * next_n * num_heads,
-                   static_cast<uint32_t>(head_dim), static_cast<uint32_t>(next_n * num_heads));
+                   static_cast<uint32_t>(head_dim),
+                   static_cast<uint32_t>((next_n * num_heads + 15) / 16 * 16));
   if (st != IDX_OK) return st;
   idx::LogitsArgs a{};
   a.kv = kv_fused;
@@ -258,8 +261,10 @@ IDX_EXPORT int64_t idx_mxfp4_workspace_bytes(int64_t num_blocks, int32_t block_s
     return -1;
   const auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
   const int64_t rows_heads = static_cast<int64_t>(batch) * next_n * num_heads;
-  // head_dim 128: the KV pages are converted on chip, only q and the weights are staged.
-  const int64_t kv = head_dim == 128 ? 0 : up(num_blocks * block_size * (head_dim + 4));
+  // head_dim 128 with 32 or 64 heads: the KV pages are converted on chip, only q and the
+  // weights are staged.
+  const bool on_chip = head_dim == 128 && (num_heads == 32 || num_heads == 64);
+  const int64_t kv = on_chip ? 0 : up(num_blocks * block_size * (head_dim + 4));
   return kv + up(rows_heads * head_dim) + up(rows_heads * 4);
 }
 
@@ -281,10 +286,11 @@ IDX_EXPORT int idx_logits_mxfp4(const uint8_t *q, const uint8_t *q_sf, const uin
       bt_row_stride < bt_width || block_size <= 0 || num_heads <= 0 || head_dim <= 0 ||
       next_n <= 0)
     return fail(IDX_INVALID_ARG, "negative or inconsistent size or stride");
-  if ((num_heads != 32 && num_heads != 64) || (head_dim != 64 && head_dim != 128) ||
+  if ((num_heads != 8 && num_heads != 16 && num_heads != 32 && num_heads != 64) ||
+      (head_dim != 64 && head_dim != 128) ||
       (block_size != 32 && block_size != 64 && block_size != 128))
-    return fail(IDX_UNSUPPORTED, "this build supports num_heads 32 or 64, head_dim 64 or 128, "
-                                 "block_size 32, 64 or 128");
+    return fail(IDX_UNSUPPORTED, "this build supports num_heads 8, 16, 32 or 64, head_dim 64 or "
+                                 "128, block_size 32, 64 or 128");
   if (next_n > 4) return fail(IDX_UNSUPPORTED, "next_n must be 1..4");
   if (batch > idx::kMaxBatch) return fail(IDX_UNSUPPORTED, "batch above 4096");
   const int64_t need = idx_mxfp4_workspace_bytes(num_blocks, block_size, batch, next_n,
@@ -295,11 +301,13 @@ IDX_EXPORT int idx_logits_mxfp4(const uint8_t *q, const uint8_t *q_sf, const uin
   if (!aligned(q, 16) || !aligned(kv_fused, 16) || !aligned(workspace, 256) ||
       !aligned(weights, 4))
     return fail(IDX_INVALID_ARG, "q and kv_fused must be 16-byte aligned, workspace 256-byte");
-  const bool on_chip = head_dim == 128;  // the KV pages converted inside the logits kernel
+  // The KV pages converted inside the logits kernel (head_dim 128, 32 or 64 heads); otherwise
+  // staged in the workspace for the FP8 kernel.
+  const bool on_chip = head_dim == 128 && (num_heads == 32 || num_heads == 64);
   if (output_dtype != IDX_DTYPE_F32 && output_dtype != IDX_DTYPE_F16 &&
       !(on_chip && output_dtype == IDX_DTYPE_BF16))
     return fail(IDX_UNSUPPORTED, "output_dtype must be IDX_DTYPE_F32, IDX_DTYPE_F16 or (head_dim "
-                                 "128) IDX_DTYPE_BF16");
+                                 "128, 32 or 64 heads) IDX_DTYPE_BF16");
   if (out_row_stride < idx_padded_seq_len(max_seq_len) || out_row_stride % 4 != 0)
     return fail(IDX_INVALID_ARG,
                 "out_row_stride must be >= idx_padded_seq_len(max_seq_len) and a multiple of 4");

@@ -98,6 +98,18 @@ cudaError_t launch_logits_d64(int next_n, LogitsOut mode, const CUtensorMap &kv_
 cudaError_t logits_d64_status(int32_t *value, bool clear);
 cudaError_t logits_d64_withhold(int32_t cta);
 
+// The 8- and 16-head instantiations (translation units of their own; float32 / float16 output).
+cudaError_t launch_logits_h8(int next_n, LogitsOut mode, const CUtensorMap &kv_map,
+                             const CUtensorMap &q_map, const LogitsArgs &args, int num_ctas,
+                             cudaStream_t stream);
+cudaError_t launch_logits_h16(int next_n, LogitsOut mode, const CUtensorMap &kv_map,
+                              const CUtensorMap &q_map, const LogitsArgs &args, int num_ctas,
+                              cudaStream_t stream);
+cudaError_t logits_h8_status(int32_t *value, bool clear);
+cudaError_t logits_h16_status(int32_t *value, bool clear);
+cudaError_t logits_h8_withhold(int32_t cta);
+cudaError_t logits_h16_withhold(int32_t cta);
+
 // The same kernel reading an MXFP4 KV pool (head_dim 128; a separate translation unit): q and
 // weights already staged in the FP8 layout (q_map over them), args.kv the MXFP4 pool.
 // output_dtype: IDX_DTYPE_F32, _F16 or _BF16.

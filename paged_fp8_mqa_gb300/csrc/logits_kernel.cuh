@@ -88,8 +88,11 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitim
 template <int NN, int H, int D, bool MX_ = false>
 struct Cfg {
   static constexpr bool MX = MX_;
-  static constexpr int N = NN * H;  // MMA N: query rows of one request
-  static constexpr int R = H / 8;   // head pairs a thread holds per position and slot
+  static constexpr int N = NN * H;  // query rows of one request
+  // The MMA's N: N rounded up to a multiple of 16 (8 heads at next_n 1 or 3); the extra q rows
+  // (the next request's, or zeros past the end of q) give accumulator columns nobody reads.
+  static constexpr int NP = (N + 15) / 16 * 16;
+  static constexpr int R = H / 8;   // 8-column chunks a thread holds per position and slot
   static constexpr uint32_t STAGE_BYTES = kTileTokens * D;  // a tile's values
   // relu_scaled's exactness needs every score below 2^25 in magnitude: D * 448^2 < 2^25.
   static_assert(D == 128 || D == 64, "head_dim 128 or 64");
@@ -113,8 +116,8 @@ struct Cfg {
   static constexpr uint32_t RAW_BYTES = MX ? kTileTokens * (D / 2 + D / 32) : 0;
   static constexpr int RAW_STAGES = MX ? (N <= 128 ? 10 : (N == 192 ? 8 : 6)) : 0;
   static constexpr int ACC = N <= 128 ? 4 : 2;  // even: tile k's accumulator belongs to team k&1
-  static constexpr int TMEM_COLS = (ACC * N <= 256) ? 256 : 512;
-  static constexpr uint32_t Q_BYTES = N * D;
+  static constexpr int TMEM_COLS = (ACC * NP <= 256) ? 256 : 512;
+  static constexpr uint32_t Q_BYTES = NP * D;
   static constexpr uint32_t W_FLOATS = NN * H;
   static constexpr uint32_t OFF_KV = 0;
   static constexpr uint32_t OFF_Q = OFF_KV + STAGES * STAGE_BYTES;
@@ -140,7 +143,8 @@ struct Cfg {
                 "copy destinations 16-byte aligned");
   static_assert(!MX || D == 128, "MXFP4 tiles: head_dim 128");
   static_assert(smem_bytes(kMaxBatch) <= 232448, "fits the 227 KiB per-CTA limit");
-  static_assert(ACC * N <= TMEM_COLS && ACC % 2 == 0 && ACC <= STAGES, "accumulators");
+  static_assert(ACC * NP <= TMEM_COLS && ACC % 2 == 0 && ACC <= STAGES, "accumulators");
+  static_assert(H == 8 || H == 16 || H == 32 || H == 64, "8, 16, 32 or 64 heads");
 };
 
 __device__ __forceinline__ void flag_error(int bits) { atomicOr(&g_logits_status, bits); }
@@ -716,7 +720,7 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
       // adding the stage / buffer offset to their start-address field (addresses stay below
       // 256 KiB, so the 14-bit field never carries).
       if (lane == 0 && ok) {
-        constexpr uint32_t idesc = idesc_e4m3_f32(kTileTokens, C::N);
+        constexpr uint32_t idesc = idesc_e4m3_f32(kTileTokens, C::NP);
         const uint64_t a_desc0 = smem_desc_rows<D>(smem_addr(s_kv));
         const uint64_t b_desc0 = smem_desc_rows<D>(smem_addr(s_q));
         int acc = kbase % C::ACC;
@@ -739,7 +743,7 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
           tc_fence_after_sync();
           const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(stage * (C::STAGE_BYTES >> 4));
           const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(qb * (C::Q_BYTES >> 4));
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::N);
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::NP);
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk)  // K step of 32 bytes = 2 in the field
             mma_f8f6f4(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, kk > 0 ? 1u : 0u);
@@ -955,7 +959,7 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
                 if (store) store_out(dst + static_cast<int64_t>(t) * a.out_stride, logit);
               }
             };
-            const uint32_t col0 = static_cast<uint32_t>(e_acc * C::N);
+            const uint32_t col0 = static_cast<uint32_t>(e_acc * C::NP);
             const int nslots = min(C::SLOTS, NN - t_first);
             // The quadrant's two 16-lane windows hold positions (g, g + 8) and (g + 16, g + 24).
             // With the slot split (more warps, fewer registers each) they are read one after the
@@ -1130,6 +1134,20 @@ cudaError_t launch_shape(int next_n, LogitsOut mode, const CUtensorMap &kv_map,
 // Sets this translation unit's fault-injection CTA (-1: off); synchronous.
 inline cudaError_t set_unit_withhold(int32_t cta) {
   return cudaMemcpyToSymbol(g_withhold_cta, &cta, sizeof(int32_t));
+}
+
+// 8 or 16 heads: float32 and float16 output only (the fused select takes 32 or 64 heads).
+template <int H, int D>
+cudaError_t launch_shape_plain(int next_n, LogitsOut mode, const CUtensorMap &kv_map,
+                               const CUtensorMap &q_map, const LogitsArgs &args, int num_ctas,
+                               cudaStream_t stream) {
+  switch (mode) {
+    case LogitsOut::kF32:
+      return launch_out<H, D, float>(next_n, kv_map, q_map, args, num_ctas, stream);
+    case LogitsOut::kF16:
+      return launch_out<H, D, __half>(next_n, kv_map, q_map, args, num_ctas, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // Reads (and, if `clear`, resets) this translation unit's status bits.

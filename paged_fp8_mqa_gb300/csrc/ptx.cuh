@@ -334,14 +334,31 @@ __device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 
-// The 16x256b load of R 8-column chunks (R = 4 or 8): 4R registers per thread.
+__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_16x256b_x1(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+
+// The 16x256b load of R 8-column chunks (R = 1, 2, 4 or 8): 4R registers per thread.
 template <int R>
 __device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[4 * R]) {
-  static_assert(R == 4 || R == 8, "16x256b.x4 or .x8");
+  static_assert(R == 1 || R == 2 || R == 4 || R == 8, "16x256b.x1, .x2, .x4 or .x8");
   if constexpr (R == 8)
     tmem_ld_16x256b_x8(taddr, r);
-  else
+  else if constexpr (R == 4)
     tmem_ld_16x256b_x4(taddr, r);
+  else if constexpr (R == 2)
+    tmem_ld_16x256b_x2(taddr, r);
+  else
+    tmem_ld_16x256b_x1(taddr, r);
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {
@@ -350,6 +367,16 @@ __device__ __forceinline__ void tmem_ld_wait() {
 
 // An empty statement that "rewrites" the registers, placed after tmem_ld_wait(): the compiler
 // cannot move a use of a tcgen05.ld result above it, hence not above the wait either.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[4]) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]));
+}
+
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[8]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]));
+}
+
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[16]) {
   asm volatile(""
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),

@@ -70,7 +70,7 @@ def _logits_args(**over):
     (dict(q=P((1 << 20) + 4)), idx.IDX_INVALID_ARG),
     (dict(num_sms=-3), idx.IDX_INVALID_ARG),
     (dict(num_heads=48), idx.IDX_UNSUPPORTED),
-    (dict(num_heads=16), idx.IDX_UNSUPPORTED),
+    (dict(num_heads=12), idx.IDX_UNSUPPORTED),
     (dict(head_dim=96), idx.IDX_UNSUPPORTED),
     (dict(head_dim=256), idx.IDX_UNSUPPORTED),
     (dict(block_size=48), idx.IDX_UNSUPPORTED),
@@ -180,7 +180,7 @@ def _mxfp4_args(**over):
     (dict(workspace_bytes=1000), idx.IDX_INVALID_ARG),
     (dict(workspace=P((1 << 20) + 16)), idx.IDX_INVALID_ARG),
     (dict(head_dim=96), idx.IDX_UNSUPPORTED),
-    (dict(num_heads=16), idx.IDX_UNSUPPORTED),
+    (dict(num_heads=12), idx.IDX_UNSUPPORTED),
     (dict(next_n=5), idx.IDX_UNSUPPORTED),
     (dict(batch=-1), idx.IDX_INVALID_ARG),
 ])

@@ -324,3 +324,40 @@ def test_block_size_32_float16_output():
     idx.logits_fp8(t["q"], t["kv"], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len, out=out)
     torch.cuda.synchronize()
     _check_float16(w, out, ref, tol)
+
+
+@pytest.mark.parametrize("heads", [8, 16])
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("next_n", [1, 2, 3, 4])
+def test_few_heads(heads, head_dim, next_n):
+    """8 and 16 heads ("flashinfer.attn_scores", fp8_paged_mqa_logits: num_heads % 4 == 0,
+    next_n * num_heads in [8, 256]): the tensor core's N is next_n * heads rounded up to a
+    multiple of 16 (8 heads at next_n 1 or 3 read extra q rows, or zeros past the end of q, into
+    columns nobody reads).  Every page size, ragged lengths, the last request long."""
+    for block_size in (32, 64, 128):
+        w = _small(360 + heads + head_dim + next_n + block_size, next_n,
+                   [0, 1, 129, 64, 300, 2049], max_seq_len=2049, num_heads=heads,
+                   head_dim=head_dim, block_size=block_size)
+        ref, tol = _oracle(w)
+        got, row_ends = gpu_logits(w)
+        check_logits(w, got, ref, tol)
+        assert (row_ends.cpu().numpy() == expected_row_ends(w)).all()
+
+
+@pytest.mark.parametrize("heads", [8, 16])
+def test_few_heads_long_runs_and_float16(heads):
+    """Many short requests over one to three CTAs (several tile lists each), and float16
+    output equal to the float32 result rounded."""
+    g = torch.Generator().manual_seed(heads)
+    lens = torch.randint(0, 700, (160,), generator=g).tolist()
+    w = _small(380 + heads, 3, lens, max_seq_len=700, num_heads=heads)
+    ref, tol = _oracle(w)
+    for num_sms in (1, 3):
+        got, _ = gpu_logits(w, num_sms=num_sms)
+        check_logits(w, got, ref, tol)
+    t = to_device(w)
+    out = torch.full((w.rows, idx.idx_padded_seq_len(w.max_seq_len)), float("nan"),
+                     dtype=torch.float16, device="cuda")
+    idx.logits_fp8(t["q"], t["kv"], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len, out=out)
+    torch.cuda.synchronize()
+    _check_float16(w, out, ref, tol)
