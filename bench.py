@@ -168,7 +168,7 @@ class ClockSampler:
 
 # Sources compiled into the logits kernel: the committed traffic figures hold only for them.
 KERNEL_SOURCES = ("logits.cu", "logits_kernel.cuh", "ptx.cuh", "split.cuh", "slots.cuh",
-                  "internal.h")
+                  "internal.h", "mx_convert.cuh")
 
 
 def kernel_sources_digest() -> str:

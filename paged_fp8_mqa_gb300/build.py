@@ -16,8 +16,8 @@ HERE = Path(__file__).resolve().parent
 CSRC = HERE / "csrc"
 LIB = HERE / "libidx.so"
 BUILD = HERE.parent / "_build"
-SOURCES = ["logits.cu", "logits_d64.cu", "logits_h16.cu", "logits_h8.cu", "logits_mxfp4.cu",
-           "select.cu", "schedule.cu", "mxfp4.cu", "abi.cu"]
+SOURCES = ["logits.cu", "logits_d64.cu", "logits_d192.cu", "logits_h16.cu", "logits_h8.cu",
+           "logits_mxfp4.cu", "select.cu", "schedule.cu", "mxfp4.cu", "abi.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

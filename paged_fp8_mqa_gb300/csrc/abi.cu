@@ -73,6 +73,42 @@ int encode_rows(CUtensorMap *map, const void *base, uint64_t rows, uint32_t row_
   return IDX_OK;
 }
 
+// head_dim 192: the pool as [num_blocks][block_size tokens][3 K blocks][64 bytes] (page stride
+// block_size * 196 bytes: the tokens' values, then their scales) and q as [rows][3][64], each read
+// one K block at a time ([tokens or rows] x 64 bytes) with the 64-byte swizzle.
+int encode_kblocks_kv(CUtensorMap *map, const void *base, uint64_t num_blocks,
+                      uint32_t block_size) {
+  EncodeTiled fn = encode_tiled();
+  if (fn == nullptr) return fail(IDX_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[4] = {64, 3, block_size, num_blocks};
+  const cuuint64_t strides[3] = {64, 192, static_cast<cuuint64_t>(block_size) * 196};
+  const cuuint32_t box[4] = {64, 1, block_size, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(IDX_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
+  return IDX_OK;
+}
+
+int encode_kblocks_q(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+  EncodeTiled fn = encode_tiled();
+  if (fn == nullptr) return fail(IDX_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[3] = {64, 3, rows};
+  const cuuint64_t strides[2] = {64, 192};
+  const cuuint32_t box[3] = {64, 1, box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(IDX_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
+  return IDX_OK;
+}
+
 int resolve_sms(int32_t requested, int32_t *out) {
   if (requested < 0 || requested > 1024) return fail(IDX_INVALID_ARG, "num_sms must be 0..1024");
   if (requested > 0) {
@@ -189,10 +225,12 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
       next_n <= 0)
     return fail(IDX_INVALID_ARG, "negative or inconsistent size or stride");
   if ((num_heads != 8 && num_heads != 16 && num_heads != 32 && num_heads != 64) ||
-      (head_dim != 64 && head_dim != 128) ||
-      (block_size != 32 && block_size != 64 && block_size != 128))
-    return fail(IDX_UNSUPPORTED, "this build supports num_heads 8, 16, 32 or 64, head_dim 64 or "
-                                 "128, block_size 32, 64 or 128");
+      (head_dim != 64 && head_dim != 128 && head_dim != 192) ||
+      (block_size != 32 && block_size != 64 && block_size != 128) ||
+      (head_dim == 192 && num_heads != 32 && num_heads != 64))
+    return fail(IDX_UNSUPPORTED, "this build supports num_heads 8, 16, 32 or 64 with head_dim 64 "
+                                 "or 128, and 32 or 64 heads with head_dim 192; block_size 32, 64 "
+                                 "or 128");
   if (next_n > 4) return fail(IDX_UNSUPPORTED, "next_n must be 1..4");
   if (output_dtype != IDX_DTYPE_F32 && output_dtype != IDX_DTYPE_F16)
     return fail(IDX_UNSUPPORTED, "output_dtype must be IDX_DTYPE_F32 or IDX_DTYPE_F16");
@@ -201,8 +239,10 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
     return fail(IDX_INVALID_ARG,
                 "out_row_stride must be >= idx_padded_seq_len(max_seq_len) and a multiple of 4");
   const int64_t page_bytes = static_cast<int64_t>(block_size) * (head_dim + 4);
-  if (num_blocks > (INT64_C(1) << 31) / (page_bytes / head_dim) - 1)
+  if (head_dim != 192 && num_blocks > (INT64_C(1) << 31) / (page_bytes / head_dim) - 1)
     return fail(IDX_INVALID_ARG, "num_blocks too large for 32-bit TMA row coordinates");
+  if (head_dim == 192 && num_blocks >= (INT64_C(1) << 31))
+    return fail(IDX_INVALID_ARG, "num_blocks too large for 32-bit TMA coordinates");
   if (!aligned(q, 16) || !aligned(kv_fused, 16) || !aligned(weights, 16) || !aligned(out, 16))
     return fail(IDX_INVALID_ARG, "q, kv_fused, weights and out must be 16-byte aligned");
   if (!aligned(block_tables, 4) || !aligned(seq_lens, 4) ||
@@ -220,14 +260,21 @@ IDX_EXPORT int idx_logits_fp8(const uint8_t *q, const uint8_t *kv_fused, int64_t
     if (st != IDX_OK) return st;
   }
   CUtensorMap kv_map, q_map;
-  st = encode_rows(&kv_map, kv_fused,
-                   static_cast<uint64_t>(num_blocks) * (page_bytes / head_dim),
-                   static_cast<uint32_t>(head_dim), static_cast<uint32_t>(block_size));
-  if (st != IDX_OK) return st;
   // The kernel loads a request's q rows rounded up to a multiple of 16 (the MMA's N).
-  st = encode_rows(&q_map, q, static_cast<uint64_t>(batch) * next_n * num_heads,
-                   static_cast<uint32_t>(head_dim),
-                   static_cast<uint32_t>((next_n * num_heads + 15) / 16 * 16));
+  const uint32_t q_box = static_cast<uint32_t>((next_n * num_heads + 15) / 16 * 16);
+  const uint64_t q_rows = static_cast<uint64_t>(batch) * next_n * num_heads;
+  if (head_dim == 192) {
+    st = encode_kblocks_kv(&kv_map, kv_fused, static_cast<uint64_t>(num_blocks),
+                           static_cast<uint32_t>(block_size));
+    if (st != IDX_OK) return st;
+    st = encode_kblocks_q(&q_map, q, q_rows, q_box);
+  } else {
+    st = encode_rows(&kv_map, kv_fused,
+                     static_cast<uint64_t>(num_blocks) * (page_bytes / head_dim),
+                     static_cast<uint32_t>(head_dim), static_cast<uint32_t>(block_size));
+    if (st != IDX_OK) return st;
+    st = encode_rows(&q_map, q, q_rows, static_cast<uint32_t>(head_dim), q_box);
+  }
   if (st != IDX_OK) return st;
   idx::LogitsArgs a{};
   a.kv = kv_fused;

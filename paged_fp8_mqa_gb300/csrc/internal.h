@@ -110,6 +110,15 @@ cudaError_t logits_h16_status(int32_t *value, bool clear);
 cudaError_t logits_h8_withhold(int32_t cta);
 cudaError_t logits_h16_withhold(int32_t cta);
 
+// The head_dim 192 instantiations (32 or 64 heads; float32 / float16 output).  kv_map views the
+// pool as [num_blocks][block_size][3][64] bytes (page stride block_size * 196), q_map as
+// [rows][3][64]; both with the 64-byte swizzle and boxes of one K block.
+cudaError_t launch_logits_d192(int next_n, LogitsOut mode, const CUtensorMap &kv_map,
+                               const CUtensorMap &q_map, const LogitsArgs &args, int num_ctas,
+                               cudaStream_t stream);
+cudaError_t logits_d192_status(int32_t *value, bool clear);
+cudaError_t logits_d192_withhold(int32_t cta);
+
 // The same kernel reading an MXFP4 KV pool (head_dim 128; a separate translation unit): q and
 // weights already staged in the FP8 layout (q_map over them), args.kv the MXFP4 pool.
 // output_dtype: IDX_DTYPE_F32, _F16 or _BF16.

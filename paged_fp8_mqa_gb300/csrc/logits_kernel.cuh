@@ -94,8 +94,13 @@ struct Cfg {
   static constexpr int NP = (N + 15) / 16 * 16;
   static constexpr int R = H / 8;   // 8-column chunks a thread holds per position and slot
   static constexpr uint32_t STAGE_BYTES = kTileTokens * D;  // a tile's values
-  // relu_scaled's exactness needs every score below 2^25 in magnitude: D * 448^2 < 2^25.
-  static_assert(D == 128 || D == 64, "head_dim 128 or 64");
+  // head_dim 192: rows of 192 bytes are three 64-byte K blocks, each a [rows x 64] tile with the
+  // 64-byte swizzle (KB blocks per tile, KBLOCK bytes apart); 64 and 128 are one block of the
+  // 64- or 128-byte swizzle.
+  static constexpr int KB = D == 192 ? 3 : 1;
+  static constexpr uint32_t KBLOCK = kTileTokens * (D / KB);
+  // relu_scaled's exactness needs every score below 2^26 in magnitude: D * 448^2 < 2^26.
+  static_assert(D == 128 || D == 64 || D == 192, "head_dim 64, 128 or 192");
   // Epilogue: two teams take alternate tiles.  A team has SPLIT warps per TMEM lane quadrant;
   // with N >= 192 the two warps of a quadrant share a tile's draft slots, which gives each
   // scheduler four epilogue warps to hide the arithmetic's latency with.
@@ -112,7 +117,10 @@ struct Cfg {
   static constexpr int SLOTS = (NN + SPLIT - 1) / SPLIT;  // draft slots per epilogue warp (max)
   // KV stages (e4m3 tiles the MMA reads).  MX: few, since the loads land in a ring of raw MXFP4
   // tiles first (RAW_STAGES of RAW_BYTES: a tile's pages, packed rows then scale bytes each).
-  static constexpr int STAGES = MX ? 4 : (N <= 128 ? 10 : (N == 192 ? 9 : 8));
+  static constexpr int STAGES =
+      MX ? 4
+         : D == 192 ? (N <= 64 ? 7 : (N <= 128 ? 6 : (N == 192 ? 5 : 4)))
+                    : (N <= 128 ? 10 : (N == 192 ? 9 : 8));
   static constexpr uint32_t RAW_BYTES = MX ? kTileTokens * (D / 2 + D / 32) : 0;
   static constexpr int RAW_STAGES = MX ? (N <= 128 ? 10 : (N == 192 ? 8 : 6)) : 0;
   static constexpr int ACC = N <= 128 ? 4 : 2;  // even: tile k's accumulator belongs to team k&1
@@ -184,11 +192,12 @@ __device__ __forceinline__ void finish_cands(PendingCands &pc, int2 *candidates,
   pc.mask = 0u;
 }
 
-// relu(s) * 2^-25 on the FMA pipe: a saturating multiply clamps to [0, 1] (NaN to 0), and
-// every score satisfies |s| <= 128 * 448^2 < 2^25, so the product is exact.
+// relu(s) * 2^-26 on the FMA pipe: a saturating multiply clamps to [0, 1] (NaN to 0), and
+// every score satisfies |s| <= 192 * 448^2 < 2^26, so the product is exact (and a nonzero score,
+// a multiple of 2^-18, stays a normal float).
 __device__ __forceinline__ float relu_scaled(float s) {
   float r;
-  asm("mul.rn.sat.f32 %0, %1, 0f33000000;" : "=f"(r) : "f"(s));  // 0f33000000 = 2^-25
+  asm("mul.rn.sat.f32 %0, %1, 0f32800000;" : "=f"(r) : "f"(s));  // 0f32800000 = 2^-26
   return r;
 }
 
@@ -196,8 +205,8 @@ __device__ __forceinline__ float relu_scaled(float s) {
 // g + 8 of its window): sums over this thread's 2R heads {8r + 2c, 8r + 2c + 1 : r < R} (of
 // H = 8R) of w_h * max(s_h, 0) in float32, the head pair of each r in one packed FMA.  Even r
 // take the ReLU as max(s, 0) on the ALU pipe, odd r as relu_scaled on the FMA pipe, which
-// balances the two pipes; the latter's sums are 2^-25 times what max(s, 0) would have produced
-// (a power-of-two scaling commutes with every rounding), so the final 2^25 rescale makes the
+// balances the two pipes; the latter's sums are 2^-26 times what max(s, 0) would have produced
+// (a power-of-two scaling commutes with every rounding), so the final 2^26 rescale makes the
 // result identical to an all-max(s, 0) evaluation of the same summation order.
 template <int R>
 __device__ __forceinline__ float2 quad_partials(const uint32_t (&v)[4 * R],
@@ -215,7 +224,7 @@ __device__ __forceinline__ float2 quad_partials(const uint32_t (&v)[4 * R],
       u1 = __ffma2_rn(w[r], make_float2(fmaxf(b0, 0.0f), fmaxf(b1, 0.0f)), u1);
     }
   }
-  constexpr float kUnscale = 33554432.0f;  // 2^25
+  constexpr float kUnscale = 67108864.0f;  // 2^26
   return make_float2((u0.x + u0.y) + (s0.x + s0.y) * kUnscale,
                      (u1.x + u1.y) + (s1.x + s1.y) * kUnscale);
 }
@@ -635,11 +644,21 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
           constexpr int BS = decltype(page_tokens)::value;
           constexpr uint32_t kValue = BS * D, kScale = BS * 4;
           constexpr int64_t kPage = BS * (D + 4);
-          constexpr int kRows = static_cast<int>(kPage / D);  // rows of D bytes per page
-          static_assert(kPage % D == 0, "a page is a whole number of D-byte rows");
+          // Rows of D bytes per page (head_dim 64, 128; the pool viewed as such rows).
+          constexpr int kRows = C::KB == 1 ? static_cast<int>(kPage / D) : 0;
+          static_assert(C::KB != 1 || kPage % D == 0, "a page is a whole number of D-byte rows");
           const auto page = [&](int pg, int id, uint8_t *dst, float *sdst) {
             if (id < 0) return;
-            tma_load_2d(dst + pg * kValue, &kv_map, &full[stage], 0, id * kRows, pol_stream);
+            if constexpr (C::KB == 1) {
+              tma_load_2d(dst + pg * kValue, &kv_map, &full[stage], 0, id * kRows, pol_stream);
+            } else {
+              // The pool as [page][token][K block][64 bytes]: block j of the page's tokens
+              // lands in K block j of the tile, at the page's rows.
+#pragma unroll
+              for (int j = 0; j < C::KB; ++j)
+                tma_load_4d(dst + j * C::KBLOCK + pg * BS * (D / C::KB), &kv_map, &full[stage],
+                            0, j, 0, id, pol_stream);
+            }
             bulk_load(sdst + pg * BS, a.kv + static_cast<int64_t>(id) * kPage + kValue, kScale,
                       &full[stage], pol_stream);
           };
@@ -702,7 +721,14 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
                 break;
               }
               mbar_arrive_expect_tx(&q_full[buf], C::Q_BYTES + C::W_FLOATS * 4);
-              tma_load_2d(s_q + buf * C::Q_BYTES, &q_map, &q_full[buf], 0, b * C::N, pol_keep);
+              if constexpr (C::KB == 1) {
+                tma_load_2d(s_q + buf * C::Q_BYTES, &q_map, &q_full[buf], 0, b * C::N, pol_keep);
+              } else {
+#pragma unroll
+                for (int j = 0; j < C::KB; ++j)
+                  tma_load_3d(s_q + buf * C::Q_BYTES + j * C::NP * (D / C::KB), &q_map,
+                              &q_full[buf], 0, j, b * C::N, pol_keep);
+              }
               bulk_load(s_w + buf * C::W_FLOATS,
                         a.weights + static_cast<int64_t>(b) * C::W_FLOATS, C::W_FLOATS * 4,
                         &q_full[buf], pol_keep);
@@ -721,8 +747,8 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
       // 256 KiB, so the 14-bit field never carries).
       if (lane == 0 && ok) {
         constexpr uint32_t idesc = idesc_e4m3_f32(kTileTokens, C::NP);
-        const uint64_t a_desc0 = smem_desc_rows<D>(smem_addr(s_kv));
-        const uint64_t b_desc0 = smem_desc_rows<D>(smem_addr(s_q));
+        const uint64_t a_desc0 = smem_desc_rows<D / C::KB>(smem_addr(s_kv));
+        const uint64_t b_desc0 = smem_desc_rows<D / C::KB>(smem_addr(s_q));
         int acc = kbase % C::ACC;
         int4 r_next = s_list[0];
         for (int i = 0; i < n; ++i) {
@@ -745,8 +771,13 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
           const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(qb * (C::Q_BYTES >> 4));
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::NP);
 #pragma unroll
-          for (int kk = 0; kk < D / 32; ++kk)  // K step of 32 bytes = 2 in the field
-            mma_f8f6f4(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+          for (int j = 0; j < C::KB; ++j)
+#pragma unroll
+            for (int kk = 0; kk < D / C::KB / 32; ++kk) {  // K step of 32 bytes = 2 in the field
+              const uint64_t ka = static_cast<uint64_t>(j * (C::KBLOCK >> 4) + 2 * kk);
+              const uint64_t kb = static_cast<uint64_t>(j * (C::NP * (D / C::KB) >> 4) + 2 * kk);
+              mma_f8f6f4(d_tmem, a_desc + ka, b_desc + kb, idesc, j + kk > 0 ? 1u : 0u);
+            }
           mma_commit(&done[stage]);
           if (r.x & kLastFlag) mma_commit(&q_empty[qb]);
           if (++stage == C::STAGES) {

@@ -361,3 +361,36 @@ def test_few_heads_long_runs_and_float16(heads):
     idx.logits_fp8(t["q"], t["kv"], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len, out=out)
     torch.cuda.synchronize()
     _check_float16(w, out, ref, tol)
+
+
+@pytest.mark.parametrize("heads", [32, 64])
+@pytest.mark.parametrize("next_n", [1, 2, 3, 4])
+def test_head_dim_192(heads, next_n):
+    """head_dim 192 ("flashinfer.attn_scores", fp8_paged_mqa_logits: head_dim % 32 == 0; the
+    shared-memory note that 192 fits at 64 heads): each row three 64-byte K blocks, six MMAs per
+    tile (scores may reach 192 * 448^2, above 2^25: the saturating ReLU rescale is 2^-26).  Every
+    page size, ragged lengths, 2% of keys scaled x60 before the e4m3 cast."""
+    for block_size in (32, 64, 128):
+        w = _small(400 + heads + next_n + block_size, next_n, [0, 1, 129, 64, 300, 2049],
+                   max_seq_len=2049, num_heads=heads, head_dim=192, block_size=block_size,
+                   scale_range=(0.25, 4.0), outlier_frac=0.02, outlier_mult=60.0)
+        ref, tol = _oracle(w)
+        got, row_ends = gpu_logits(w)
+        check_logits(w, got, ref, tol)
+        assert (row_ends.cpu().numpy() == expected_row_ends(w)).all()
+
+
+def test_head_dim_192_long_runs_and_float16():
+    g = torch.Generator().manual_seed(192)
+    lens = torch.randint(0, 900, (120,), generator=g).tolist()
+    w = _small(420, 2, lens, max_seq_len=900, head_dim=192)
+    ref, tol = _oracle(w)
+    for num_sms in (1, 3, 0):
+        got, _ = gpu_logits(w, num_sms=num_sms)
+        check_logits(w, got, ref, tol)
+    t = to_device(w)
+    out = torch.full((w.rows, idx.idx_padded_seq_len(w.max_seq_len)), float("nan"),
+                     dtype=torch.float16, device="cuda")
+    idx.logits_fp8(t["q"], t["kv"], t["weights"], t["bt"], t["seq_lens"], w.max_seq_len, out=out)
+    torch.cuda.synchronize()
+    _check_float16(w, out, ref, tol)
