@@ -9,9 +9,9 @@
 // its one to four pages (of 128, 64 or 32 tokens; the kernel is instantiated per page size)},
 // issuing the block-table reads of the whole list in parallel.  The producer and the MMA issuer
 // then walk the whole list, each epilogue team only its own tiles:
-// The kernel is instantiated per head count H (32, 64), head_dim D (128, 64), output and page
-// size; H = 64, D = 128 below.  A row of D e4m3 bytes is one swizzle atom wide (128- or 64-byte
-// swizzle).
+// The kernel is instantiated per head count H (8, 16, 32, 64), head_dim D (64, 128, 192), output
+// type and page size; H = 64, D = 128 below.  A row of 64 or 128 e4m3 bytes is one swizzle atom
+// wide (64- or 128-byte swizzle); a row of 192 is three 64-byte atoms.
 //   warp 0     producer (one thread): per tile, TMA-loads the pages' e4m3 values (128-byte
 //              swizzled, 16 KiB per tile) into a KV stage and bulk-copies their float32 scales
 //              (512 B per tile) into a scale slot; per request, TMA-loads q and bulk-copies w
@@ -82,9 +82,9 @@ constexpr int kMaskShift = 18;                    // bit 18 + p: the tile's page
 constexpr int kOrdShift = 22;                     // bits 22-29: the request's ordinal mod 256
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
 
-// next_n = NN draft slots of H heads each (H = 32 or 64), head_dim D (128 or 64): one e4m3 row
-// of q or K is one swizzle atom wide (128- or 64-byte swizzle).  MX: the KV pool holds MXFP4
-// pages, which converter warps turn into the e4m3 tile in shared memory (D = 128 only).
+// next_n = NN draft slots of H heads each (H = 8, 16, 32 or 64), head_dim D (64, 128 or 192).
+// MX: the KV pool holds MXFP4 pages, which converter warps turn into the e4m3 tile in shared
+// memory (D = 128 only).
 template <int NN, int H, int D, bool MX_ = false>
 struct Cfg {
   static constexpr bool MX = MX_;
