@@ -741,21 +741,30 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
       __syncwarp();
     } else if (warp == 1) {
       // ============================== MMA issuer ==============================================
-      // This thread is the pipeline's serial point, so its loop is kept short: the next record
-      // is read one tile ahead, and the shared-memory descriptors are built once and advanced by
-      // adding the stage / buffer offset to their start-address field (addresses stay below
-      // 256 KiB, so the 14-bit field never carries).
+      // This thread is the pipeline's serial point: the tensor core idles whenever it falls
+      // behind, and it shares its scheduler with busy epilogue warps (each instruction of its
+      // serial chain waits for an issue slot), so its loop is kept to a few instructions per
+      // tile: the next record's flags are loaded a tile ahead, and the shared-memory descriptors
+      // are kept as (start-address word, constant word) pairs of which only the start address is
+      // advanced (addresses stay below 256 KiB, so the 14-bit field never carries).
       if (lane == 0 && ok) {
         constexpr uint32_t idesc = idesc_e4m3_f32(kTileTokens, C::NP);
-        const uint64_t a_desc0 = smem_desc_rows<D / C::KB>(smem_addr(s_kv));
-        const uint64_t b_desc0 = smem_desc_rows<D / C::KB>(smem_addr(s_q));
+        constexpr int kSteps = D / C::KB / 32;  // K steps of 32 bytes per K block
+        constexpr uint32_t kStageStep = C::STAGE_BYTES >> 4, kQStep = C::Q_BYTES >> 4;
+        const uint64_t a0 = smem_desc_rows<D / C::KB>(smem_addr(s_kv));
+        const uint64_t b0 = smem_desc_rows<D / C::KB>(smem_addr(s_q));
+        const uint32_t a_hi = static_cast<uint32_t>(a0 >> 32), b_hi = static_cast<uint32_t>(b0 >> 32);
+        const uint32_t a_lo0 = static_cast<uint32_t>(a0), b_lo0 = static_cast<uint32_t>(b0);
         int acc = kbase % C::ACC;
-        int4 r_next = s_list[0];
+        uint32_t a_lo = a_lo0 + static_cast<uint32_t>(stage) * kStageStep;
+        uint32_t b_lo = b_lo0 + static_cast<uint32_t>(qb) * kQStep;
+        uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::NP);
+        int rx = s_list[0].x;
         for (int i = 0; i < n; ++i) {
-          const int4 r = r_next;
-          if (i + 1 < n) r_next = s_list[i + 1];
-          if (r.x & kFirstFlag) {
+          const int rx_next = i + 1 < n ? s_list[i + 1].x : 0;
+          if (rx & kFirstFlag) {
             qb = qcount & 1;
+            b_lo = b_lo0 + static_cast<uint32_t>(qb) * kQStep;
             if (!mbar_wait(&q_full[qb], (qcount >> 1) & 1, kWaitLimitNs)) {
               ok = false;
               break;
@@ -767,24 +776,25 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(stage * (C::STAGE_BYTES >> 4));
-          const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(qb * (C::Q_BYTES >> 4));
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::NP);
 #pragma unroll
           for (int j = 0; j < C::KB; ++j)
 #pragma unroll
-            for (int kk = 0; kk < D / C::KB / 32; ++kk) {  // K step of 32 bytes = 2 in the field
-              const uint64_t ka = static_cast<uint64_t>(j * (C::KBLOCK >> 4) + 2 * kk);
-              const uint64_t kb = static_cast<uint64_t>(j * (C::NP * (D / C::KB) >> 4) + 2 * kk);
-              mma_f8f6f4(d_tmem, a_desc + ka, b_desc + kb, idesc, j + kk > 0 ? 1u : 0u);
-            }
+            for (int kk = 0; kk < kSteps; ++kk)  // K step of 32 bytes = 2 in the address field
+              mma_f8f6f4(d_tmem, a_lo + static_cast<uint32_t>(j * (C::KBLOCK >> 4) + 2 * kk), a_hi,
+                         b_lo + static_cast<uint32_t>(j * (C::NP * (D / C::KB) >> 4) + 2 * kk),
+                         b_hi, idesc, j + kk > 0 ? 1u : 0u);
           mma_commit(&done[stage]);
-          if (r.x & kLastFlag) mma_commit(&q_empty[qb]);
+          if (rx & kLastFlag) mma_commit(&q_empty[qb]);
+          rx = rx_next;
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
+            a_lo = a_lo0;
+          } else {
+            a_lo += kStageStep;
           }
           if (++acc == C::ACC) acc = 0;
+          d_tmem = tmem_base + static_cast<uint32_t>(acc * C::NP);
         }
         // A short list is the run's last: commit the drain behind its MMAs now, so that it has
         // completed by the teardown.
