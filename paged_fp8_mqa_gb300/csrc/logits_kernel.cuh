@@ -112,6 +112,11 @@ struct Cfg {
   // groups); eight warps take one unit per thread, or two warps four each where the epilogue's
   // 16 warps leave registers for only two more.
   static constexpr int CONV_WARPS = MX ? (N >= 192 ? 2 : 8) : 0;
+  // (MX) The converter warps form groups taking tiles in turn (four groups of two warps, or two
+  // of one), so that one tile's waits (for its raw pages and for its stage's previous MMAs)
+  // overlap the others' conversions.
+  static constexpr int CONV_GROUPS = MX ? (N >= 192 ? 2 : 4) : 1;
+  static constexpr int GROUP_WARPS = MX ? CONV_WARPS / CONV_GROUPS : 1;
   static constexpr int CONV_BASE = kEpiWarpBase + EPI_WARPS;  // first converter warp
   static constexpr int THREADS = (kEpiWarpBase + EPI_WARPS + CONV_WARPS) * 32;
   static constexpr int SLOTS = (NN + SPLIT - 1) / SPLIT;  // draft slots per epilogue warp (max)
@@ -122,7 +127,7 @@ struct Cfg {
          : D == 192 ? (N <= 64 ? 7 : (N <= 128 ? 6 : (N == 192 ? 5 : 4)))
                     : (N <= 128 ? 10 : (N == 192 ? 9 : 8));
   static constexpr uint32_t RAW_BYTES = MX ? kTileTokens * (D / 2 + D / 32) : 0;
-  static constexpr int RAW_STAGES = MX ? (N <= 128 ? 10 : (N == 192 ? 8 : 6)) : 0;
+  static constexpr int RAW_STAGES = MX ? (N <= 192 ? 8 : 6) : 0;
   static constexpr int ACC = N <= 128 ? 4 : 2;  // even: tile k's accumulator belongs to team k&1
   static constexpr int TMEM_COLS = (ACC * NP <= 256) ? 256 : 512;
   static constexpr uint32_t Q_BYTES = NP * D;
@@ -150,6 +155,8 @@ struct Cfg {
                     OFF_RAW % 16 == 0 && RAW_BYTES % 16 == 0,
                 "copy destinations 16-byte aligned");
   static_assert(!MX || D == 128, "MXFP4 tiles: head_dim 128");
+  static_assert(!MX || (STAGES % CONV_GROUPS == 0 && RAW_STAGES % CONV_GROUPS == 0),
+                "(MX) a converter group's tiles keep to its own stages");
   static_assert(smem_bytes(kMaxBatch) <= 232448, "fits the 227 KiB per-CTA limit");
   static_assert(ACC * NP <= TMEM_COLS && ACC % 2 == 0 && ACC <= STAGES, "accumulators");
   static_assert(H == 8 || H == 16 || H == 32 || H == 64, "8, 16, 32 or 64 heads");
@@ -560,12 +567,12 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
       prefetch_tensor_map(&q_map);
       for (int s = 0; s < C::STAGES; ++s) {
         // The producer (MX: the converter warps) + the accumulator's last readers.
-        mbar_init(&full[s], (C::MX ? C::CONV_WARPS : 1) + C::TEAM_WARPS);
+        mbar_init(&full[s], (C::MX ? C::GROUP_WARPS : 1) + C::TEAM_WARPS);
         mbar_init(&done[s], 1);  // the MMA's commit
       }
       for (int s = 0; s < C::RAW_STAGES; ++s) {
         mbar_init(&raw_full[s], 1);
-        mbar_init(&raw_empty[s], C::CONV_WARPS);
+        mbar_init(&raw_empty[s], C::GROUP_WARPS);
       }
       for (int c = 0; c < 2; ++c) {
         mbar_init(&q_full[c], 1);
@@ -818,8 +825,14 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
       if (ok) {
         constexpr int BS = 1 << BS_SHIFT;
         constexpr uint32_t kRawPage = BS * (D / 2 + D / 32);
-        constexpr int kConvThreads = C::CONV_WARPS * 32;
-        for (int i = 0; i < n; ++i) {
+        constexpr int kGroupThreads = C::GROUP_WARPS * 32;
+        const int grp = (warp - C::CONV_BASE) / C::GROUP_WARPS;
+        const int gtid = tid - (C::CONV_BASE + grp * C::GROUP_WARPS) * 32;
+        for (int i = (grp - kbase % C::CONV_GROUPS + C::CONV_GROUPS) % C::CONV_GROUPS; i < n;
+             i += C::CONV_GROUPS) {
+          const int k = kbase + i;
+          const int stage = k % C::STAGES, rstage = k % C::RAW_STAGES;
+          const uint32_t phase = (k / C::STAGES) & 1, rphase = (k / C::RAW_STAGES) & 1;
           const int4 r = s_list[i];
           if (!mbar_wait(&raw_full[rstage], rphase, kWaitLimitNs) ||
               !mbar_wait(&done[stage], phase ^ 1, kWaitLimitNs)) {
@@ -827,7 +840,8 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
             break;
           }
           bool inexact = false;
-          for (int u = tid - C::CONV_BASE * 32; u < 2 * kTileTokens; u += kConvThreads) {
+          const int live = s_len[r.x & 0xFFFF] - r.y * kTileTokens;  // tokens below seq_len
+          for (int u = gtid; u < 2 * kTileTokens; u += kGroupThreads) {
             const int ct = u >> 1, hf = u & 1;
             const int pg = ct >> BS_SHIFT, tt = ct & (BS - 1);
             uint8_t *row = s_kv + stage * C::STAGE_BYTES + ct * 128;
@@ -840,7 +854,7 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
               for (int g = 0; g < 4; ++g) emax = max(emax, static_cast<int>((sf >> (8 * g)) & 0xFFu));
               if (((sf & 0xFFu) == 0xFFu || ((sf >> 8) & 0xFFu) == 0xFFu ||
                    ((sf >> 16) & 0xFFu) == 0xFFu || (sf >> 24) == 0xFFu) &&
-                  r.y * kTileTokens + ct < s_len[r.x & 0xFFFF])
+                  ct < live)
                 inexact = true;
 #pragma unroll
               for (int j = 0; j < 2; ++j) {
@@ -850,20 +864,19 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
                 bool lost = false;
                 mx_group_to_e4m3(*reinterpret_cast<const uint4 *>(raw + tt * (D / 2) + 16 * g), rel,
                                  s_tab[rel >= -8 ? -rel : 0], out, &lost);
-                if (lost && r.y * kTileTokens + ct < s_len[r.x & 0xFFFF]) inexact = true;
+                if (lost && ct < live) inexact = true;
                 *reinterpret_cast<uint4 *>(row + (((2 * g) ^ (ct & 7)) << 4)) =
                     make_uint4(out[0], out[1], out[2], out[3]);
                 *reinterpret_cast<uint4 *>(row + (((2 * g + 1) ^ (ct & 7)) << 4)) =
                     make_uint4(out[4], out[5], out[6], out[7]);
               }
-              if (hf == 0)
-                s_scale[((kbase + i) % C::SCALE_SLOTS) * kTileTokens + ct] = pow2f(emax - 127);
+              if (hf == 0) s_scale[(k % C::SCALE_SLOTS) * kTileTokens + ct] = pow2f(emax - 127);
             } else {
 #pragma unroll
               for (int j = 0; j < 4; ++j)
                 *reinterpret_cast<uint4 *>(row + (((4 * hf + j) ^ (ct & 7)) << 4)) =
                     make_uint4(0u, 0u, 0u, 0u);
-              if (hf == 0) s_scale[((kbase + i) % C::SCALE_SLOTS) * kTileTokens + ct] = 0.0f;
+              if (hf == 0) s_scale[(k % C::SCALE_SLOTS) * kTileTokens + ct] = 0.0f;
             }
           }
           if (inexact) flag_error(IDX_DEV_INEXACT_SCALE);
@@ -873,16 +886,7 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
             mbar_arrive(&raw_empty[rstage]);
             mbar_arrive(&full[stage]);
             // The first ACC tiles' accumulators were never read: stand in for their readers.
-            if (warp == C::CONV_BASE && kbase + i < C::ACC)
-              mbar_arrive_count(&full[stage], C::TEAM_WARPS);
-          }
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-          if (++rstage == C::RAW_STAGES) {
-            rstage = 0;
-            rphase ^= 1;
+            if (gtid == 0 && k < C::ACC) mbar_arrive_count(&full[stage], C::TEAM_WARPS);
           }
         }
       }
