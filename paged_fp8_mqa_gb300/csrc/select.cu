@@ -559,6 +559,56 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
   }
 }
 
+// Repair of a row of K' = row_end keys (at most top_k): every key is selected, so v is the row's
+// smallest key (one reduction) and one pass writes the keys above it as candidates and the keys
+// equal to it as ties, with no radix passes.
+__device__ void repair_all_keys(const float *row, int row_end, int top_k, int2 *slots, int *c_out,
+                                int *m_out, float *v_out) {
+  __shared__ unsigned s_min;
+  __shared__ int s_nc, s_nt;
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid == 0) {
+    s_min = 0xFFFFFFFFu;
+    s_nc = 0;
+    s_nt = 0;
+  }
+  __syncthreads();
+  unsigned mn = 0xFFFFFFFFu;
+  for (int i = tid; i < row_end; i += kThreads) mn = min(mn, order_key(__ldg(row + i)));
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  if (lane == 0) atomicMin(&s_min, mn);
+  __syncthreads();
+  const uint32_t v = s_min;
+  for (int i0 = 0; i0 < row_end; i0 += kThreads) {  // slots reserved with one atomic per warp
+    const int i = i0 + tid;
+    const uint32_t key = i < row_end ? order_key(__ldg(row + i)) : 0u;
+    const bool is_c = i < row_end && key > v;
+    const bool is_t = i < row_end && key == v;
+    const unsigned mc = __ballot_sync(0xffffffffu, is_c);
+    if (mc) {
+      const int leader = __ffs(mc) - 1;
+      int n = 0;
+      if (lane == leader) n = atomicAdd(&s_nc, __popc(mc));
+      n = __shfl_sync(0xffffffffu, n, leader) + __popc(mc & lanemask_lt());
+      if (is_c) slots[top_k + n] = make_int2(i, __float_as_int(key_value(key)));
+    }
+    const unsigned mt = __ballot_sync(0xffffffffu, is_t);
+    if (mt) {
+      const int leader = __ffs(mt) - 1;
+      int n = 0;
+      if (lane == leader) n = atomicAdd(&s_nt, __popc(mt));
+      n = __shfl_sync(0xffffffffu, n, leader) + __popc(mt & lanemask_lt());
+      if (is_t) slots[top_k - 1 - n] = make_int2(i, __float_as_int(key_value(v)));
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    *c_out = s_nc;
+    *m_out = s_nt;
+    *v_out = key_value(v);
+  }
+}
+
 // Repairs a row that does not fit (every thread of the CTA calls it): its slots get exactly its
 // top-K', and *c_out / *m_out / *v_out (shared) the keys above v, the keys equal to v kept, and v.
 // thr, nc, nt: the row's threshold and classification counts.
@@ -567,6 +617,11 @@ __device__ __forceinline__ void repair_any(const float *row, int row_end, int K,
                                            float *v_out, uint8_t *dyn) {
   // The threshold bounds the K'-th key from below when at least K' and at most a buffer's worth
   // of keys were counted at or above it (NaN thresholds excepted).
+  if (K == row_end) {  // a row of at most top_k keys: all of them
+    repair_all_keys(row, row_end, top_k, slots, c_out, m_out, v_out);
+    __syncthreads();
+    return;
+  }
   const bool hint = thr == thr && nc + nt >= K && nc + nt <= kBufKeys;
   if (!repair_row_gather(row, row_end, K, top_k, slots, hint, order_key(thr), c_out, m_out, v_out,
                          dyn)) {
@@ -671,8 +726,13 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
   __threadfence();
   const int K = row_end < a.top_k ? row_end : a.top_k;
   if (tid == 0) {
-    const int nc = atomicAdd(counter, 0);
-    const int nt = atomicAdd(counter + 1, 0);
+    // Both counts read at L2 (where the other CTAs' additions landed), the two reads in flight
+    // together.
+    int nc, nt;
+    asm volatile("ld.global.cg.s32 %0, [%2];\n\tld.global.cg.s32 %1, [%3];"
+                 : "=r"(nc), "=r"(nt)
+                 : "l"(counter), "l"(counter + 1)
+                 : "memory");
     s_nc = nc;
     s_nt = nt;
     s_fits = row_fits(nc, nt, K, a.top_k, a.capacity);

@@ -49,6 +49,7 @@ CASES = [
     (3, 32, 128, 128, [2500, 3, 2, 0, 127, 129]),
     (4, 64, 64, 64, [4000, 4, 3, 100, 0, 8193]),
     (2, 32, 64, 32, [3000, 1, 0, 200, 7000]),
+    (3, 64, 128, 64, [2900, 2, 0, 131, 6001]),
 ]
 
 
@@ -58,6 +59,20 @@ def test_mxfp4_parity(next_n, heads, head_dim, block_size, lens):
     w, m = _case(600 + next_n + heads + head_dim, next_n, lens, heads, head_dim, block_size)
     ref, tol = _oracle(w, m)
     got, row_ends = _gpu(w, m)
+    stats = check_logits(w, got, ref, tol)
+    assert stats["checked"] == expected_scores(w)
+    assert (row_ends.cpu().numpy() == expected_row_ends(w)).all()
+
+
+@pytest.mark.parametrize("next_n", [1, 3, 4])
+def test_mxfp4_one_cta_many_lists(next_n):
+    """One CTA walks several tile lists of many short requests: the converter groups take the
+    run's tiles in turn across list boundaries."""
+    g = torch.Generator().manual_seed(45 + next_n)
+    lens = torch.randint(1, 700, (120,), generator=g).tolist()
+    w, m = _case(650 + next_n, next_n, lens)
+    ref, tol = _oracle(w, m)
+    got, row_ends = _gpu(w, m, num_sms=1)
     stats = check_logits(w, got, ref, tol)
     assert stats["checked"] == expected_scores(w)
     assert (row_ends.cpu().numpy() == expected_row_ends(w)).all()
