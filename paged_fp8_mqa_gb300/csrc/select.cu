@@ -87,27 +87,58 @@ __device__ __forceinline__ int block_scan(int v, int *s_warp, int *total) {
   return before + incl - v;
 }
 
-// The bin of the need-th largest key of a histogram of nbins (2048 or 1024) bins, scanning
-// from the top: *s_bin and *s_above (the count of keys in higher bins).  All threads call it.
+// The bin of the need-th largest key of a histogram of nbins (2048 or 1024) bins, counting from
+// the top: *s_bin and *s_above (the count of keys in higher bins); both are left unchanged if
+// the histogram holds fewer than `need` keys.  All threads call it.  Warp w sums the w-th range
+// of nbins / 32 bins from the top; warp 0 scans the 32 sums, then the bins of the range that
+// holds the need-th key, and publishes the bin (two block barriers in all).
 __device__ __forceinline__ void find_bin(const unsigned *h, int nbins, unsigned need,
                                          int *s_bin, unsigned *s_above, int *s_warp) {
-  const int tid = threadIdx.x;
-  const int per = nbins / kThreads;
-  const int hi = nbins - 1 - per * tid;
-  unsigned local = 0;
-  for (int j = 0; j < per; ++j) local += h[hi - j];
-  int total;
-  const unsigned before = static_cast<unsigned>(block_scan(static_cast<int>(local), s_warp, &total));
-  if (before < need && need <= before + local) {
-    unsigned cum = before;
-    for (int j = 0; j < per; ++j) {
-      const unsigned c = h[hi - j];
-      if (cum + c >= need) {
-        *s_bin = hi - j;
-        *s_above = cum;
-        break;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per_warp = nbins / kWarps;  // 64 or 32
+  const int per_lane = per_warp / 32;   // 2 or 1
+  unsigned *s_wsum = reinterpret_cast<unsigned *>(s_warp);
+  {
+    const int top = nbins - 1 - warp * per_warp - lane * per_lane;
+    unsigned x = 0;
+    for (int j = 0; j < per_lane; ++j) x += h[top - j];
+    x = __reduce_add_sync(0xffffffffu, x);
+    if (lane == 0) s_wsum[warp] = x;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const auto scan = [&](unsigned v) {  // inclusive scan over the lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
       }
-      cum += c;
+      return v;
+    };
+    const unsigned ws = s_wsum[lane];  // range `lane`, counted from the top
+    const unsigned incl = scan(ws), excl = incl - ws;
+    const unsigned hit = __ballot_sync(0xffffffffu, excl < need && need <= incl);
+    if (hit) {
+      const int w = __ffs(hit) - 1;
+      const unsigned above = __shfl_sync(0xffffffffu, excl, w);
+      const int top = nbins - 1 - w * per_warp - lane * per_lane;
+      unsigned v = 0;
+      for (int j = 0; j < per_lane; ++j) v += h[top - j];
+      const unsigned incl2 = scan(v), excl2 = incl2 - v;
+      const unsigned need2 = need - above;
+      const unsigned hit2 = __ballot_sync(0xffffffffu, excl2 < need2 && need2 <= incl2);
+      if (hit2 && lane == __ffs(hit2) - 1) {
+        unsigned cum = above + excl2;
+        for (int j = 0; j < per_lane; ++j) {
+          const unsigned c = h[top - j];
+          if (cum + c >= need) {
+            *s_bin = top - j;
+            *s_above = cum;
+            break;
+          }
+          cum += c;
+        }
+      }
     }
   }
   __syncthreads();
