@@ -334,7 +334,18 @@ __device__ bool repair_row_gather(const float *row, int row_end, int K, int top_
     // This thread's keys >= lo as a bit mask; then one warp scan and one shared atomic per warp
     // place them in the buffer, each lane storing only its own (few) keys, re-read from L1.
     uint32_t take = 0;
-    if (base + kThreads * 4 * kPassLoads <= row_end) {
+    if (base + kThreads * 4 * kPassLoads <= row_end && lo >= 0x80000000u) {
+      // lo is a non-negative float's key: key(x) >= lo exactly when x's bits, read as a signed
+      // integer, are >= lo's float bits (negative x and -NaN read negative; +NaN above +inf).
+      const int lo_bits = static_cast<int>(lo & 0x7FFFFFFFu);
+#pragma unroll
+      for (int u = 0; u < kPassLoads; ++u) {
+        take |= (__float_as_int(v[u].x) >= lo_bits ? 1u : 0u) << (4 * u);
+        take |= (__float_as_int(v[u].y) >= lo_bits ? 1u : 0u) << (4 * u + 1);
+        take |= (__float_as_int(v[u].z) >= lo_bits ? 1u : 0u) << (4 * u + 2);
+        take |= (__float_as_int(v[u].w) >= lo_bits ? 1u : 0u) << (4 * u + 3);
+      }
+    } else if (base + kThreads * 4 * kPassLoads <= row_end) {
 #pragma unroll
       for (int u = 0; u < kPassLoads; ++u) {
         take |= (order_key(v[u].x) >= lo ? 1u : 0u) << (4 * u);
