@@ -448,49 +448,81 @@ def time_launch_events(w, t, steps, stream):
 def time_e2e(w, dev, steps, stream, sel=None):
     """Same metric through the public calls with host buffers: every step copies its inputs
     from pinned host memory, runs the step and copies its result back (the logits, or for a
-    selecting workload the selection: candidates, counters, ranges and thresholds)."""
+    selecting workload the selection: candidates, counters, ranges and thresholds).  The steps
+    are pipelined as a serving loop would run them: step i + 1's inputs are copied (into the
+    second of two device input sets, on a copy stream) while step i computes, and step i's
+    result is copied back on another copy stream."""
     host = dict(q=w.q.pin_memory(), kv=w.kv_fused.pin_memory(),
                 weights=w.weights.pin_memory(), bt=w.block_tables.pin_memory(),
                 seq_lens=w.seq_lens.pin_memory())
     if sel is not None:
         host["thr"] = sel["thr0"].cpu().pin_memory()
-    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    devb = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
     pad = idx.idx_padded_seq_len(w.max_seq_len)
     out = torch.empty(w.rows, pad, device=dev)
     row_ends = torch.empty(w.rows, dtype=torch.int32, device=dev)
-    if sel is None:
-        results = {"out": out}
-    else:
-        results = {"cand": sel["cand"], "counters": sel["counters"], "ranges": sel["ranges"],
-                   "thr": devb["thr"]}
-    back = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in results.items()}
+
+    def results(j):
+        if sel is None:
+            return {"out": out}
+        return {"cand": sel["cand"], "counters": sel["counters"], "ranges": sel["ranges"],
+                "thr": devb[j]["thr"]}
+    back = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in results(0).items()}
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(v.numel() * v.element_size() for v in back.values())
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # set j's inputs landed
+    ev_used = [torch.cuda.Event() for _ in range(2)]  # the step computing on set j finished
+    ev_back = torch.cuda.Event()                      # the last result copy finished
+    ev_used[0].record(stream)
+    ev_used[1].record(stream)
+    ev_back.record(stream)
 
-    def step():
-        for k in host:
-            devb[k].copy_(host[k], non_blocking=True)
-        idx.logits_fp8(devb["q"], devb["kv"], devb["weights"], devb["bt"], devb["seq_lens"],
-                       w.max_seq_len, out=out, row_ends_out=row_ends, stream=stream)
+    def copy_in(i):
+        j = i % 2
+        s_in.wait_event(ev_used[j])
+        with torch.cuda.stream(s_in):
+            for k in host:
+                devb[j][k].copy_(host[k], non_blocking=True)
+        ev_in[j].record(s_in)
+
+    def compute(i):
+        j = i % 2
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_back)  # the result buffers are free again
+        d = devb[j]
+        idx.logits_fp8(d["q"], d["kv"], d["weights"], d["bt"], d["seq_lens"], w.max_seq_len,
+                       out=out, row_ends_out=row_ends, stream=stream)
         if sel is not None:
-            sel["counters"].zero_()
-            idx.threshold_select(out, row_ends, devb["thr"], sel["counters"], sel["cand"],
+            with torch.cuda.stream(stream):
+                sel["counters"].zero_()
+            idx.threshold_select(out, row_ends, d["thr"], sel["counters"], sel["cand"],
                                  w.top_k, w.capacity, w.max_seq_len, arrivals=sel["arrivals"],
                                  ranges=sel["ranges"], stream=stream)
-        for k, v in results.items():
-            back[k].copy_(v, non_blocking=True)
+        ev_used[j].record(stream)
+        s_out.wait_event(ev_used[j])
+        with torch.cuda.stream(s_out):
+            for k, v in results(j).items():
+                back[k].copy_(v, non_blocking=True)
+        ev_back.record(s_out)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
+    def run(n):
+        copy_in(0)
+        for i in range(n):
+            if i + 1 < n:
+                copy_in(i + 1)
+            compute(i)
+        stream.wait_event(ev_back)
+
+    run(3)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(steps):
-            step()
-        e1.record(stream)
+    e0.record(stream)
+    ev_used[0].record(stream)  # the copies start after e0
+    ev_used[1].record(stream)
+    run(steps)
+    e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     return ms, h2d, d2h
@@ -736,7 +768,10 @@ def main() -> None:
             "data": "synthetic", "config": workload_config(w),
             "launch_event_ms": event_ms, "host_enqueue_ms": host_ms,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "note": "every step copies its inputs from pinned host memory and its result "
+                            "back; the next step's input copy overlaps the current step's "
+                            "compute and result copy (two device input sets, two copy streams)"},
             "gpu_launches": args.steps * (2 if select_diag else 1), "device_status": status,
             "clocks": clocks, "roofline": roof, "cpu_baseline": cpu,
         }
