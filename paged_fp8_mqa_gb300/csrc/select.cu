@@ -50,18 +50,24 @@ constexpr int kSweepLoads = kChunk / (kThreads * 4);  // float4 per thread, all 
 constexpr int kBufKeys = 6144;                  // keys of the bin holding v, kept in shared memory
 constexpr int kTieRank = 2048;                  // ties ranked in shared memory (ordered case)
 constexpr uint32_t kSelectSmem = 2048 * 4 + kBufKeys * 8;  // dynamic: histogram + (key, index)
-constexpr int kPassLoads = 8;                   // float4 loads in flight per thread, histogram
+constexpr int kPassLoads = 8;                   // 16-byte loads in flight per thread, histogram
 constexpr int kSamples = 2048;                  // keys sampled to bound the K'-th from below
 constexpr int kSweepKeys = 16;                  // contiguous keys per thread, final sweep
 constexpr int kRepairSpan = kThreads * kSweepKeys;
 
-// Order-preserving map float -> uint32: a < b in IEEE totalOrder iff key(a) < key(b).
-__device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(f);
+// Scores are handled as their bit patterns from the load on: a float-typed NaN may not keep its
+// bits (a NaN read as a float and turned into its order key gave the key of -0 on this GPU), and
+// the repair must order +NaN above +inf and -NaN below -inf, and store every score's own bits.
+__device__ __forceinline__ uint32_t ldg_bits(const float *p) {
+  return __ldg(reinterpret_cast<const unsigned *>(p));
+}
+// Order-preserving map of a binary32's bits -> uint32: a < b in IEEE totalOrder iff
+// key(a) < key(b); key_bits is its inverse.
+__device__ __forceinline__ uint32_t order_key(uint32_t u) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-__device__ __forceinline__ float key_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+__device__ __forceinline__ uint32_t key_bits(uint32_t k) {
+  return (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
 }
 
 // Block-wide exclusive scan of one int per thread; returns the prefix, *total the sum.
@@ -153,7 +159,7 @@ __device__ __forceinline__ void find_bin(const unsigned *h, int nbins, unsigned 
 // Returns false, having written nothing, if more than kTieRank tied keys would need ranking.
 __device__ bool finish_from_buffer(const uint32_t *s_bkey, const int *s_bidx, int nb, int b1_in,
                                    unsigned need, int K, int top_k, int2 *slots, int *s_cand,
-                                   unsigned *s_h, int *cand_out, int *tie_out, float *thr_out) {
+                                   unsigned *s_h, int *cand_out, int *tie_out, uint32_t *thr_out) {
   __shared__ int s_bin, s_ntie;
   __shared__ unsigned s_above;
   __shared__ int s_warp[kWarps];
@@ -210,7 +216,7 @@ __device__ bool finish_from_buffer(const uint32_t *s_bkey, const int *s_bidx, in
       int n = 0;
       if (lane == leader) n = atomicAdd(s_cand, __popc(mc));
       n = __shfl_sync(0xffffffffu, n, leader) + __popc(mc & lanemask_lt());
-      if (is_c) slots[top_k + n] = make_int2(s_bidx[j], __float_as_int(key_value(key)));
+      if (is_c) slots[top_k + n] = make_int2(s_bidx[j], static_cast<int>(key_bits(key)));
     }
     const unsigned mt = __ballot_sync(0xffffffffu, is_t);
     if (mt) {
@@ -220,7 +226,7 @@ __device__ bool finish_from_buffer(const uint32_t *s_bkey, const int *s_bidx, in
       n = __shfl_sync(0xffffffffu, n, leader) + __popc(mt & lanemask_lt());
       if (is_t) {
         if (ties == m)
-          slots[top_k - 1 - n] = make_int2(s_bidx[j], __float_as_int(key_value(vkey)));
+          slots[top_k - 1 - n] = make_int2(s_bidx[j], static_cast<int>(key_bits(vkey)));
         else
           s_tidx[n] = s_bidx[j];
       }
@@ -233,33 +239,33 @@ __device__ bool finish_from_buffer(const uint32_t *s_bkey, const int *s_bidx, in
       const int mine = s_tidx[j];
       int rank = 0;
       for (int q = 0; q < ties; ++q) rank += s_tidx[q] < mine ? 1 : 0;
-      if (rank < m) slots[top_k - 1 - rank] = make_int2(mine, __float_as_int(key_value(vkey)));
+      if (rank < m) slots[top_k - 1 - rank] = make_int2(mine, static_cast<int>(key_bits(vkey)));
     }
   }
   if (tid == 0) {
     *cand_out = c;
     *tie_out = m;
-    *thr_out = key_value(vkey);
+    *thr_out = key_bits(vkey);
   }
   return true;
 }
 
-// kPassLoads float4 loads of the row per thread, all in flight before any is used (the row is
-// L2-resident; one load at a time would leave a sweep bound by the L2 latency).  Keys past
-// row_end read as 0.0f and must be masked by the caller.
+// kPassLoads 16-byte loads of the row per thread, all in flight before any is used (the row is
+// L2-resident; one load at a time would leave a sweep bound by the L2 latency), as bits.  Keys
+// past row_end read as 0 and must be masked by the caller.
 __device__ __forceinline__ void load_pass(const float *row, int row_end, int base,
-                                          float4 (&v)[kPassLoads]) {
+                                          uint4 (&v)[kPassLoads]) {
   const int tid = threadIdx.x;
 #pragma unroll
   for (int u = 0; u < kPassLoads; ++u) {
     const int i = base + (u * kThreads + tid) * 4;
     if (i + 3 < row_end) {
-      v[u] = __ldg(reinterpret_cast<const float4 *>(row + i));
+      v[u] = __ldg(reinterpret_cast<const uint4 *>(row + i));
     } else {
-      v[u].x = i < row_end ? __ldg(row + i) : 0.0f;
-      v[u].y = i + 1 < row_end ? __ldg(row + i + 1) : 0.0f;
-      v[u].z = i + 2 < row_end ? __ldg(row + i + 2) : 0.0f;
-      v[u].w = 0.0f;
+      v[u].x = i < row_end ? ldg_bits(row + i) : 0u;
+      v[u].y = i + 1 < row_end ? ldg_bits(row + i + 1) : 0u;
+      v[u].z = i + 2 < row_end ? ldg_bits(row + i + 2) : 0u;
+      v[u].w = 0u;
     }
   }
 }
@@ -273,7 +279,7 @@ __device__ __forceinline__ void load_pass(const float *row, int row_end, int bas
 // ties can be ranked).
 __device__ bool repair_row_gather(const float *row, int row_end, int K, int top_k, int2 *slots,
                                   bool have_hint, uint32_t lo_hint, int *cand_out, int *tie_out,
-                                  float *thr_out, uint8_t *dyn) {
+                                  uint32_t *thr_out, uint8_t *dyn) {
   unsigned *s_h = reinterpret_cast<unsigned *>(dyn);                // [2048]: samples, histogram
   uint32_t *s_bkey = reinterpret_cast<uint32_t *>(dyn + 2048 * 4);  // [kBufKeys]
   int *s_bidx = reinterpret_cast<int *>(s_bkey + kBufKeys);         // [kBufKeys]
@@ -294,7 +300,7 @@ __device__ bool repair_row_gather(const float *row, int row_end, int K, int top_
 #pragma unroll
       for (int q = 0; q < kSamples / kThreads; ++q)
         smp[q] = order_key(
-            __ldg(row + static_cast<int64_t>(q * kThreads + tid) * row_end / kSamples));
+            ldg_bits(row + static_cast<int64_t>(q * kThreads + tid) * row_end / kSamples));
       const int64_t want =
           static_cast<int64_t>(K) * kSamples * 3 / (2 * static_cast<int64_t>(row_end));
       const unsigned rank = static_cast<unsigned>(min(static_cast<int64_t>(kSamples), want + 17));
@@ -329,7 +335,7 @@ __device__ bool repair_row_gather(const float *row, int row_end, int K, int top_
   __syncthreads();
   const int lane = tid & 31;
   for (int base = 0; base < row_end; base += kThreads * 4 * kPassLoads) {
-    float4 v[kPassLoads];
+    uint4 v[kPassLoads];
     load_pass(row, row_end, base, v);
     // This thread's keys >= lo as a bit mask; then one warp scan and one shared atomic per warp
     // place them in the buffer, each lane storing only its own (few) keys, re-read from L1.
@@ -340,10 +346,10 @@ __device__ bool repair_row_gather(const float *row, int row_end, int K, int top_
       const int lo_bits = static_cast<int>(lo & 0x7FFFFFFFu);
 #pragma unroll
       for (int u = 0; u < kPassLoads; ++u) {
-        take |= (__float_as_int(v[u].x) >= lo_bits ? 1u : 0u) << (4 * u);
-        take |= (__float_as_int(v[u].y) >= lo_bits ? 1u : 0u) << (4 * u + 1);
-        take |= (__float_as_int(v[u].z) >= lo_bits ? 1u : 0u) << (4 * u + 2);
-        take |= (__float_as_int(v[u].w) >= lo_bits ? 1u : 0u) << (4 * u + 3);
+        take |= (static_cast<int>(v[u].x) >= lo_bits ? 1u : 0u) << (4 * u);
+        take |= (static_cast<int>(v[u].y) >= lo_bits ? 1u : 0u) << (4 * u + 1);
+        take |= (static_cast<int>(v[u].z) >= lo_bits ? 1u : 0u) << (4 * u + 2);
+        take |= (static_cast<int>(v[u].w) >= lo_bits ? 1u : 0u) << (4 * u + 3);
       }
     } else if (base + kThreads * 4 * kPassLoads <= row_end) {
 #pragma unroll
@@ -357,7 +363,7 @@ __device__ bool repair_row_gather(const float *row, int row_end, int K, int top_
 #pragma unroll
       for (int u = 0; u < kPassLoads; ++u) {
         const int i = base + (u * kThreads + tid) * 4;
-        const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        const uint32_t e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           if (i + k < row_end && order_key(e[k]) >= lo) take |= 1u << (4 * u + k);
@@ -377,7 +383,7 @@ __device__ bool repair_row_gather(const float *row, int row_end, int K, int top_
       const int bit = __ffs(take) - 1;
       take &= take - 1;
       const int i = base + ((bit >> 2) * kThreads + tid) * 4 + (bit & 3);
-      const uint32_t key = order_key(__ldg(row + i));
+      const uint32_t key = order_key(ldg_bits(row + i));
       atomicAdd(&s_h[key >> 21], 1u);
       if (n < kBufKeys) {
         s_bkey[n] = key;
@@ -397,7 +403,7 @@ __device__ bool repair_row_gather(const float *row, int row_end, int K, int top_
 // the buffer, or more tied keys than can be ranked, in which case nothing it wrote is counted and
 // the caller falls back to repair_row.
 __device__ bool repair_row_fast(const float *row, int row_end, int K, int top_k, int2 *slots,
-                                int *cand_out, int *tie_out, float *thr_out, uint8_t *dyn) {
+                                int *cand_out, int *tie_out, uint32_t *thr_out, uint8_t *dyn) {
   unsigned *s_h = reinterpret_cast<unsigned *>(dyn);                // [2048]
   uint32_t *s_bkey = reinterpret_cast<uint32_t *>(dyn + 2048 * 4);  // [kBufKeys]
   int *s_bidx = reinterpret_cast<int *>(s_bkey + kBufKeys);         // [kBufKeys]
@@ -415,12 +421,12 @@ __device__ bool repair_row_fast(const float *row, int row_end, int K, int top_k,
   __syncthreads();
   // ---- sweep 1: histogram of the leading 11 key bits
   for (int base = 0; base < row_end; base += kThreads * 4 * kPassLoads) {
-    float4 v[kPassLoads];
+    uint4 v[kPassLoads];
     load_pass(row, row_end, base, v);
 #pragma unroll
     for (int u = 0; u < kPassLoads; ++u) {
       const int i = base + (u * kThreads + tid) * 4;
-      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      const uint32_t e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         if (i + k < row_end) atomicAdd(&s_h[order_key(e[k]) >> 21], 1u);
@@ -434,12 +440,12 @@ __device__ bool repair_row_fast(const float *row, int row_end, int K, int top_k,
   if (nb > kBufKeys) return false;
   // ---- sweep 2: keys of higher bins are candidates; the bin's own keys go to the buffer
   for (int base = 0; base < row_end; base += kThreads * 4 * kPassLoads) {
-    float4 v[kPassLoads];
+    uint4 v[kPassLoads];
     load_pass(row, row_end, base, v);
 #pragma unroll
     for (int u = 0; u < kPassLoads; ++u) {
       const int i = base + (u * kThreads + tid) * 4;
-      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      const uint32_t e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         if (i + k >= row_end) continue;
@@ -447,7 +453,7 @@ __device__ bool repair_row_fast(const float *row, int row_end, int K, int top_k,
         const uint32_t bin = key >> 21;
         if (bin > b1) {
           const int n = atomicAdd(&s_cand, 1);
-          slots[top_k + n] = make_int2(i + k, __float_as_int(e[k]));
+          slots[top_k + n] = make_int2(i + k, static_cast<int>(e[k]));
         } else if (bin == b1) {
           const int n = atomicAdd(&s_nbuf, 1);
           s_bkey[n] = key;
@@ -464,7 +470,7 @@ __device__ bool repair_row_fast(const float *row, int row_end, int K, int top_k,
 
 // Repairs row `r` (called by every thread of the row's last CTA): see the file comment.
 __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2 *slots,
-                           int *cand_out, int *tie_out, float *thr_out) {
+                           int *cand_out, int *tie_out, uint32_t *thr_out) {
   __shared__ unsigned s_hist[256];
   __shared__ uint32_t s_prefix, s_mask;
   __shared__ int s_need, s_cand, s_tie_base;
@@ -481,26 +487,15 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
     for (int i = tid; i < 256; i += kThreads) s_hist[i] = 0;
     __syncthreads();
     const uint32_t prefix = s_prefix, mask = s_mask;
-    // kPassLoads float4 per thread in flight before any is used (the row is L2-resident; one
+    // kPassLoads 16-byte loads per thread in flight before any is used (the row is L2-resident; one
     // load at a time would leave each pass bound by the L2 latency).
     for (int base = 0; base < row_end; base += kThreads * 4 * kPassLoads) {
-      float4 v[kPassLoads];
+      uint4 v[kPassLoads];
+      load_pass(row, row_end, base, v);
 #pragma unroll
       for (int u = 0; u < kPassLoads; ++u) {
         const int i = base + (u * kThreads + tid) * 4;
-        if (i + 3 < row_end) {
-          v[u] = __ldg(reinterpret_cast<const float4 *>(row + i));
-        } else {
-          v[u].x = i < row_end ? __ldg(row + i) : 0.0f;
-          v[u].y = i + 1 < row_end ? __ldg(row + i + 1) : 0.0f;
-          v[u].z = i + 2 < row_end ? __ldg(row + i + 2) : 0.0f;
-          v[u].w = 0.0f;  // i + 3 >= row_end here
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kPassLoads; ++u) {
-        const int i = base + (u * kThreads + tid) * 4;
-        const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        const uint32_t e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t key = order_key(e[k]);
@@ -550,15 +545,15 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
   }
   __syncthreads();
   for (int i0 = 0; i0 < row_end; i0 += kRepairSpan) {
-    // Each thread takes kSweepKeys consecutive keys (four float4 loads in flight), so that one
+    // Each thread takes kSweepKeys consecutive keys (four 16-byte loads in flight), so that one
     // block scan per span ranks the ties in index order.
     const int first = i0 + tid * kSweepKeys;
     uint32_t keys[kSweepKeys];
     if (first + kSweepKeys - 1 < row_end) {
-      float4 v[kSweepKeys / 4];
+      uint4 v[kSweepKeys / 4];
 #pragma unroll
       for (int u = 0; u < kSweepKeys / 4; ++u)
-        v[u] = __ldg(reinterpret_cast<const float4 *>(row + first) + u);
+        v[u] = __ldg(reinterpret_cast<const uint4 *>(row + first) + u);
 #pragma unroll
       for (int u = 0; u < kSweepKeys / 4; ++u) {
         keys[4 * u] = order_key(v[u].x);
@@ -569,7 +564,7 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
     } else {
 #pragma unroll
       for (int k = 0; k < kSweepKeys; ++k)  // key 0 is below every real key's tie/candidate
-        keys[k] = first + k < row_end ? order_key(__ldg(row + first + k)) : 0u;
+        keys[k] = first + k < row_end ? order_key(ldg_bits(row + first + k)) : 0u;
     }
     int mine = 0;
 #pragma unroll
@@ -577,7 +572,7 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
       const bool valid = first + k < row_end;
       if (valid && keys[k] > vkey) {
         const int n = atomicAdd(&s_cand, 1);
-        if (n < c) slots[top_k + n] = make_int2(first + k, __float_as_int(key_value(keys[k])));
+        if (n < c) slots[top_k + n] = make_int2(first + k, static_cast<int>(key_bits(keys[k])));
       }
       mine += (valid && keys[k] == vkey) ? 1 : 0;
     }
@@ -586,7 +581,8 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
 #pragma unroll
     for (int k = 0; k < kSweepKeys; ++k) {
       if (first + k < row_end && keys[k] == vkey) {
-        if (rank < m) slots[top_k - 1 - rank] = make_int2(first + k, __float_as_int(key_value(vkey)));
+        if (rank < m)
+          slots[top_k - 1 - rank] = make_int2(first + k, static_cast<int>(key_bits(vkey)));
         ++rank;
       }
     }
@@ -597,7 +593,7 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
   if (tid == 0) {
     *cand_out = c;
     *tie_out = m;
-    *thr_out = key_value(vkey);
+    *thr_out = key_bits(vkey);
   }
 }
 
@@ -605,7 +601,7 @@ __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2
 // smallest key (one reduction) and one pass writes the keys above it as candidates and the keys
 // equal to it as ties, with no radix passes.
 __device__ void repair_all_keys(const float *row, int row_end, int top_k, int2 *slots, int *c_out,
-                                int *m_out, float *v_out) {
+                                int *m_out, uint32_t *v_out) {
   __shared__ unsigned s_min;
   __shared__ int s_nc, s_nt;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -616,14 +612,14 @@ __device__ void repair_all_keys(const float *row, int row_end, int top_k, int2 *
   }
   __syncthreads();
   unsigned mn = 0xFFFFFFFFu;
-  for (int i = tid; i < row_end; i += kThreads) mn = min(mn, order_key(__ldg(row + i)));
+  for (int i = tid; i < row_end; i += kThreads) mn = min(mn, order_key(ldg_bits(row + i)));
   mn = __reduce_min_sync(0xffffffffu, mn);
   if (lane == 0) atomicMin(&s_min, mn);
   __syncthreads();
   const uint32_t v = s_min;
   for (int i0 = 0; i0 < row_end; i0 += kThreads) {  // slots reserved with one atomic per warp
     const int i = i0 + tid;
-    const uint32_t key = i < row_end ? order_key(__ldg(row + i)) : 0u;
+    const uint32_t key = i < row_end ? order_key(ldg_bits(row + i)) : 0u;
     const bool is_c = i < row_end && key > v;
     const bool is_t = i < row_end && key == v;
     const unsigned mc = __ballot_sync(0xffffffffu, is_c);
@@ -632,7 +628,7 @@ __device__ void repair_all_keys(const float *row, int row_end, int top_k, int2 *
       int n = 0;
       if (lane == leader) n = atomicAdd(&s_nc, __popc(mc));
       n = __shfl_sync(0xffffffffu, n, leader) + __popc(mc & lanemask_lt());
-      if (is_c) slots[top_k + n] = make_int2(i, __float_as_int(key_value(key)));
+      if (is_c) slots[top_k + n] = make_int2(i, static_cast<int>(key_bits(key)));
     }
     const unsigned mt = __ballot_sync(0xffffffffu, is_t);
     if (mt) {
@@ -640,14 +636,14 @@ __device__ void repair_all_keys(const float *row, int row_end, int top_k, int2 *
       int n = 0;
       if (lane == leader) n = atomicAdd(&s_nt, __popc(mt));
       n = __shfl_sync(0xffffffffu, n, leader) + __popc(mt & lanemask_lt());
-      if (is_t) slots[top_k - 1 - n] = make_int2(i, __float_as_int(key_value(v)));
+      if (is_t) slots[top_k - 1 - n] = make_int2(i, static_cast<int>(key_bits(v)));
     }
   }
   __syncthreads();
   if (tid == 0) {
     *c_out = s_nc;
     *m_out = s_nt;
-    *v_out = key_value(v);
+    *v_out = key_bits(v);
   }
 }
 
@@ -656,7 +652,7 @@ __device__ void repair_all_keys(const float *row, int row_end, int top_k, int2 *
 // thr, nc, nt: the row's threshold and classification counts.
 __device__ __forceinline__ void repair_any(const float *row, int row_end, int K, float thr, int nc,
                                            int nt, int top_k, int2 *slots, int *c_out, int *m_out,
-                                           float *v_out, uint8_t *dyn) {
+                                           uint32_t *v_out, uint8_t *dyn) {
   // The threshold bounds the K'-th key from below when at least K' and at most a buffer's worth
   // of keys were counted at or above it (NaN thresholds excepted).
   if (K == row_end) {  // a row of at most top_k keys: all of them
@@ -665,8 +661,8 @@ __device__ __forceinline__ void repair_any(const float *row, int row_end, int K,
     return;
   }
   const bool hint = thr == thr && nc + nt >= K && nc + nt <= kBufKeys;
-  if (!repair_row_gather(row, row_end, K, top_k, slots, hint, order_key(thr), c_out, m_out, v_out,
-                         dyn)) {
+  const uint32_t thr_key = order_key(__float_as_uint(thr));
+  if (!repair_row_gather(row, row_end, K, top_k, slots, hint, thr_key, c_out, m_out, v_out, dyn)) {
     __syncthreads();
     if (!repair_row_fast(row, row_end, K, top_k, slots, c_out, m_out, v_out, dyn)) {
       __syncthreads();
@@ -746,7 +742,7 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
     for (uint32_t m = cm | tm; m != 0u; m &= m - 1u) {
       const int bit = __ffs(m) - 1;
       const int i = begin + ((bit >> 2) * kThreads + tid) * 4 + (bit & 3);
-      const int2 item = make_int2(i, __float_as_int(__ldg(row + i)));
+      const int2 item = make_int2(i, static_cast<int>(ldg_bits(row + i)));
       if ((cm >> bit) & 1u) {
         if (nc < a.capacity) slots[a.top_k + nc] = item;
         ++nc;
@@ -787,12 +783,12 @@ __global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs 
     }
   } else {
     __shared__ int s_c, s_m;
-    __shared__ float s_v;
+    __shared__ uint32_t s_v;
     repair_any(row, row_end, K, thr, s_nc, s_nt, a.top_k, slots, &s_c, &s_m, &s_v, select_smem);
     if (tid == 0) {
       counter[0] = s_c;
       counter[1] = s_m;
-      a.thresholds[r] = s_v;
+      reinterpret_cast<uint32_t *>(a.thresholds)[r] = s_v;  // v's own bits
       a.ranges[r] = a.top_k - s_m;
       a.ranges[a.rows + r] = a.top_k + s_c;
     }
@@ -824,7 +820,7 @@ __global__ void __launch_bounds__(kThreads) k_fused_repair(const FusedRepairArgs
     return;
   }
   __shared__ int s_c, s_m;
-  __shared__ float s_v;
+  __shared__ uint32_t s_v;
   int2 *slots = reinterpret_cast<int2 *>(a.candidates) +
                 static_cast<int64_t>(r) * (a.top_k + a.capacity);
   repair_any(a.scratch + static_cast<int64_t>(r) * a.scratch_stride, row_end, K, a.thresholds[r],
@@ -832,7 +828,7 @@ __global__ void __launch_bounds__(kThreads) k_fused_repair(const FusedRepairArgs
   if (threadIdx.x == 0) {
     counter[0] = s_c;
     counter[1] = s_m;
-    a.thresholds[r] = s_v;
+    reinterpret_cast<uint32_t *>(a.thresholds)[r] = s_v;
     a.ranges[r] = a.top_k - s_m;
     a.ranges[rows + r] = a.top_k + s_c;
   }

@@ -196,3 +196,30 @@ def test_row_lengths_around_chunks(max_context):
         for t in (thr, torch.full_like(thr, math.inf), thr - 0.5):
             res = gpu_select(x.cuda(), row_ends.cuda(), t.cuda(), top_k, capacity, max_context)
             check_selection(lc, row_ends.numpy(), top_k, capacity, res, t.numpy())
+
+
+@pytest.mark.parametrize("top_k,capacity", [(300, 299), (2048, 4096)])
+def test_repair_with_nan_inf_and_signed_zeros(top_k, capacity):
+    """Repairs (rows longer than the repair's buffer, and rows of at most top_k keys) over keys
+    that include +NaN and -NaN (above +inf and below -inf in totalOrder), +-inf and +-0.  The
+    thresholds +inf and -inf make every long row need a repair (no candidates, or all of them);
+    a threshold that lets such a row fit would count its NaNs as ties, which the fit rule treats
+    as the threshold's value rather than by totalOrder, so only repaired rows are compared."""
+    g = torch.Generator().manual_seed(77 + top_k)
+    rows, n = 6, 20000
+    x = torch.randn(rows, n, generator=g).abs()  # non-negative: the gathering bound is >= +0
+    x[1] = 0.0
+    x[1, ::2] = -0.0
+    nan_pos = np.frombuffer(np.array([0x7FC00001], dtype=np.uint32).tobytes(), dtype=np.float32)[0]
+    nan_neg = np.frombuffer(np.array([0xFFC00002], dtype=np.uint32).tobytes(), dtype=np.float32)[0]
+    for r in range(rows):
+        idx_ = torch.randperm(n, generator=g)[:40]
+        x[r, idx_[:10]] = float(nan_pos)
+        x[r, idx_[10:20]] = float(nan_neg)
+        x[r, idx_[20:30]] = math.inf
+        x[r, idx_[30:40]] = -math.inf
+    lc = x.numpy()
+    row_ends = torch.tensor([n, n, 15000, top_k, max(top_k - 7, 1), 9000], dtype=torch.int32)
+    for t in (torch.full((rows,), math.inf), torch.full((rows,), -math.inf)):
+        res = gpu_select(x.cuda(), row_ends.cuda(), t.cuda(), top_k, capacity, n)
+        check_selection(lc, row_ends.numpy(), top_k, capacity, res, t.numpy())
