@@ -852,10 +852,9 @@ __global__ void __launch_bounds__(Cfg<NN, H, D, MX>::THREADS, 1)
               int emax = 0;
 #pragma unroll
               for (int g = 0; g < 4; ++g) emax = max(emax, static_cast<int>((sf >> (8 * g)) & 0xFFu));
-              if (((sf & 0xFFu) == 0xFFu || ((sf >> 8) & 0xFFu) == 0xFFu ||
-                   ((sf >> 16) & 0xFFu) == 0xFFu || (sf >> 24) == 0xFFu) &&
-                  ct < live)
-                inexact = true;
+              // A 0xFF (NaN) scale byte: a zero byte of ~sf.
+              const uint32_t nsf = ~sf;
+              if (((nsf - 0x01010101u) & ~nsf & 0x80808080u) != 0u && ct < live) inexact = true;
 #pragma unroll
               for (int j = 0; j < 2; ++j) {
                 const int g = 2 * hf + ((j + (ct >> 1)) & 1);

@@ -58,8 +58,9 @@ __device__ __forceinline__ uint32_t prmt(uint32_t lo, uint32_t hi, uint32_t sel)
 // nibble's bit 3.
 __device__ __forceinline__ void e2m1x8_to_e4m3(uint32_t w, uint2 tab, uint32_t &a, uint32_t &b) {
   const uint32_t w4 = w << 4;
-  const uint32_t ma = prmt(tab.x, tab.y, w & 0x7777u);
-  const uint32_t mb = prmt(tab.x, tab.y, (w >> 16) & 0x7777u);
+  const uint32_t m = w & 0x77777777u;        // the eight codes' magnitudes; prmt reads a
+  const uint32_t ma = prmt(tab.x, tab.y, m);  // selector's low 16 bits only
+  const uint32_t mb = prmt(tab.x, tab.y, m >> 16);
   const uint32_t sa = prmt(w, w4, 0x9D8Cu);  // elements 0..3: bytes 4, 0, 5, 1 (sign mode)
   const uint32_t sb = prmt(w, w4, 0xBFAEu);  // elements 4..7: bytes 6, 2, 7, 3 (sign mode)
   a = ma | (sa & 0x80808080u);
