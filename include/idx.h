@@ -203,7 +203,8 @@ int idx_logits_mxfp4(const uint8_t *q, const uint8_t *q_sf, const uint8_t *kv_fu
 /*
  * idx_threshold_select ("flashinfer.sdsa.indexer_threshold_select": description; Parameters
  * row_ends, thresholds, counters, candidates, max_context, top_k, arrivals, ranges), over
- * logits already written by idx_logits_fp8.  One launch, no host synchronisation.
+ * logits already written by idx_logits_fp8.  One launch (two with arrivals), no host
+ * synchronisation.
  *
  * For row r, key i < row_ends[r] with score s = logits[r*logits_row_stride + i] and
  * thr = thresholds[r]: s > thr makes a candidate, "neither above nor below" (s == thr or NaN)
@@ -215,12 +216,14 @@ int idx_logits_mxfp4(const uint8_t *q, const uint8_t *q_sf, const uint8_t *kv_fu
  * candidates >= K' or (ties <= top_k and candidates + ties >= K'): then every item of its
  * exact top-K' (descending value, ties to the lowest index) is in its slots.
  *
- * With arrivals (and ranges), the last CTA of each row to finish repairs a row that does not
- * fit: it finds the row's K'-th largest score v by radix select over totalOrder keys, stores
- * the keys above v as candidates and the lowest-index keys equal to v as ties (exactly K'
- * items), sets counters[r] to those counts, thresholds[r] = v, and resets arrivals[r] to 0.
+ * With arrivals (and ranges), a second launch, which starts once every row's counts are final,
+ * repairs each row that does not fit: it finds the row's K'-th largest score v by radix select
+ * over totalOrder keys, stores the keys above v as candidates and the lowest-index keys equal
+ * to v as ties (exactly K' items), and sets counters[r] to those counts and thresholds[r] = v.
  * Every row then holds its exact top-K' and ranges[0*rows + r] .. ranges[1*rows + r] (half
- * open) is the slot range holding its candidates and ties.
+ * open) is the slot range holding its candidates and ties.  arrivals (as on the pages) asks for
+ * the repair; no CTA counts arrivals, so its contents are never read, and the second launch sets
+ * arrivals[r] = 0 for every row.
  *
  *   logits            device float32, 16-byte aligned, row stride a multiple of 4
  *   row_ends          device int32 [rows], 0 .. max_context
@@ -230,8 +233,8 @@ int idx_logits_mxfp4(const uint8_t *q, const uint8_t *q_sf, const uint8_t *kv_fu
  *   candidates        device int32 [rows][top_k + capacity][2]
  *   top_k             >= 1 (the number of tie slots)
  *   capacity          >= 0 candidate slots; >= top_k - 1 when arrivals is given
- *   max_context       the most keys a row sees; sizes the grid (one CTA per 16384 keys)
- *   arrivals          NULL (no repair), or device int32 [rows], zeroed once; every call
+ *   max_context       the most keys a row sees; sizes the grid (one CTA per 8192 keys)
+ *   arrivals          NULL (no repair), or device int32 [rows] (any contents); every call
  *                     leaves it zeroed
  *   ranges            device int32 [2][rows]; required when arrivals is given, else ignored
  */
@@ -244,7 +247,7 @@ int idx_threshold_select(const float *logits, int64_t logits_row_stride, const i
  * idx_threshold_select_static -- the pages have no counterpart to this entry point; it exists
  * for callers that cannot allocate device memory.
  *
- * idx_threshold_select with repair needs an `arrivals` workspace of one int32 per row.  Some
+ * idx_threshold_select with repair takes an `arrivals` array of one int32 per row.  Some
  * callers cannot provide one: a serving runtime that plans all of its device memory up front
  * and forbids allocation inside a step, or a plugin that has no handle on its host
  * framework's allocator and may not call cudaMalloc itself.  This entry point takes the same

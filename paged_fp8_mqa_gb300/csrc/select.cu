@@ -2,19 +2,21 @@
 // indexer_threshold_select": description; Parameters row_ends, thresholds, counters,
 // candidates, max_context, top_k, arrivals, ranges).
 //
-// Grid: (ceil(max_context / kChunk), rows).  CTA (c, r) sweeps keys [c*kChunk, (c+1)*kChunk)
-// of row r below row_ends[r]: s > thr is a candidate, "neither above nor below" (== or NaN) a
-// tie.  Slots are reserved with one atomicAdd per warp and per kind for all the warp's 512 keys
-// (a warp scan of the counts), the n-th candidate going to slot top_k + n (n < capacity), the
-// n-th tie to top_k - 1 - n (n < top_k), each as (key index, raw float32 bits).
+// Launch 1, grid (ceil(max_context / kChunk), rows) of 512-thread CTAs (two per SM): CTA (c, r)
+// sweeps keys [c*kChunk, (c+1)*kChunk) of row r below row_ends[r]: s > thr is a candidate,
+// "neither above nor below" (== or NaN) a tie.  Slots are reserved with one atomicAdd per warp
+// and per kind for all the warp's 512 keys (a warp scan of the counts), the n-th candidate going
+// to slot top_k + n (n < capacity), the n-th tie to top_k - 1 - n (n < top_k), each as (key
+// index, raw float32 bits).
 //
-// With `arrivals`, the last CTA of a row to finish (an atomicAdd ticket, no waiting) decides
-// whether the row fits; if not, it repairs it alone: an MSB-first radix select over
-// order-preserving uint32 keys (i.e. IEEE totalOrder) finds the row's K'-th largest key v,
-// K' = min(row_end, top_k), and the row's keys above v become candidates and its lowest-index
-// keys equal to v ties, K' items in all.  It then rewrites counters, the threshold (v) and
-// ranges, and returns arrivals[r] to zero.  The repair first needs a key lo <= v: 0 if the whole
-// row fits a 6144-key shared-memory buffer, else the row's threshold if the classification
+// With `arrivals`, a second launch (a programmatic dependent: it proceeds only once launch 1 has
+// finished, so every count is final) decides for each row whether it fits and, if not, repairs
+// it with one 1024-thread CTA: an MSB-first radix select over order-preserving uint32 keys (i.e.
+// IEEE totalOrder) finds the row's K'-th largest key v, K' = min(row_end, top_k), and the row's
+// keys above v become candidates and its lowest-index keys equal to v ties, K' items in all.  It
+// then rewrites counters, the threshold (v) and ranges, and zeroes arrivals[r] (which nothing
+// reads: no CTA waits for or counts the others).  The repair first needs a key lo <= v: 0 if the
+// whole row fits a 6144-key shared-memory buffer, else the row's threshold if the classification
 // counted between K' and 6144 keys at or above it, else a bound read off a sample of 2048 of
 // the row's keys with a safety margin.  One sweep gathers every key >= lo into the buffer (one
 // shared atomic per warp and 32 keys), where three histogram passes (11, 11, 10 bits) find v
@@ -45,8 +47,9 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 16384;      // keys per sweeping CTA
-constexpr int kSweepLoads = kChunk / (kThreads * 4);  // float4 per thread, all in flight
+constexpr int kClsThreads = 512;  // threads of a classifying CTA (two per SM)
+constexpr int kChunk = 8192;       // keys per classifying CTA
+constexpr int kSweepLoads = kChunk / (kClsThreads * 4);  // float4 per thread, all in flight
 constexpr int kBufKeys = 6144;                  // keys of the bin holding v, kept in shared memory
 constexpr int kTieRank = 2048;                  // ties ranked in shared memory (ordered case)
 constexpr uint32_t kSelectSmem = 2048 * 4 + kBufKeys * 8;  // dynamic: histogram + (key, index)
@@ -672,128 +675,143 @@ __device__ __forceinline__ void repair_any(const float *row, int row_end, int K,
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads) k_threshold_select(const SelectArgs a) {
+// Launch 1: CTA (c, r) classifies keys [c*kChunk, (c+1)*kChunk) of row r below row_ends[r].
+// A CTA past the row's keys leaves at once.
+__global__ void __launch_bounds__(kClsThreads) k_select_classify(const SelectArgs a) {
   // The previous kernel in the stream may still be running: no global memory before this.
   griddep_wait();
   griddep_launch_dependents();
-  extern __shared__ __align__(16) uint8_t select_smem[];
   const int r = blockIdx.y;
   const int tid = threadIdx.x;
   int row_end = a.row_ends[r];
   row_end = row_end < 0 ? 0 : (row_end > a.max_context ? a.max_context : row_end);
+  const int begin = blockIdx.x * kChunk;
+  const int end = min(begin + kChunk, row_end);
+  if (begin >= end) return;
   const float thr = a.thresholds[r];
   const float *row = a.logits + static_cast<int64_t>(r) * a.row_stride;
   int2 *slots = reinterpret_cast<int2 *>(a.candidates) +
                 static_cast<int64_t>(r) * (a.top_k + a.capacity);
   int *counter = a.counters + 2 * r;
+  float4 v[kSweepLoads];  // all of this thread's loads in flight before any is classified
+#pragma unroll
+  for (int u = 0; u < kSweepLoads; ++u) {
+    const int i = begin + (u * kClsThreads + tid) * 4;
+    if (i + 3 < end) {
+      v[u] = __ldg(reinterpret_cast<const float4 *>(row + i));
+    } else {
+      v[u].x = i < end ? row[i] : 0.0f;
+      v[u].y = i + 1 < end ? row[i + 1] : 0.0f;
+      v[u].z = i + 2 < end ? row[i + 2] : 0.0f;
+      v[u].w = 0.0f;
+    }
+  }
+  // The thread's candidates and ties as bit masks; one warp scan of both counts and one
+  // atomicAdd per warp and kind reserve all the warp's slots at once (a reservation per
+  // 32 keys would put a round trip to L2 on the path for each of them).
+  static_assert(kSweepLoads * 4 <= 16, "16 keys per thread fit the 16-bit counts");
+  uint32_t cm = 0, tm = 0;
+#pragma unroll
+  for (int u = 0; u < kSweepLoads; ++u) {
+    const int i = begin + (u * kClsThreads + tid) * 4;
+    const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const bool valid = i + k < end;
+      const float s = e[k];
+      cm |= (valid && s > thr ? 1u : 0u) << (4 * u + k);
+      tm |= (valid && !(s > thr) && !(s < thr) ? 1u : 0u) << (4 * u + k);
+    }
+  }
+  const int lane = tid & 31;
+  const int mine = __popc(cm) | (__popc(tm) << 16);  // a warp's sums stay below 2^16
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int excl = incl - mine;
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  int bc = 0, bt = 0;
+  if (lane == 0) {
+    if (total & 0xFFFF) bc = atomicAdd(counter, total & 0xFFFF);
+    if (total >> 16) bt = atomicAdd(counter + 1, total >> 16);
+  }
+  int nc = __shfl_sync(0xffffffffu, bc, 0) + (excl & 0xFFFF);
+  int nt = __shfl_sync(0xffffffffu, bt, 0) + (excl >> 16);
+  // The few keys taken are re-read (L1 hits) rather than kept in registers.
+  for (uint32_t m = cm | tm; m != 0u; m &= m - 1u) {
+    const int bit = __ffs(m) - 1;
+    const int i = begin + ((bit >> 2) * kClsThreads + tid) * 4 + (bit & 3);
+    const int2 item = make_int2(i, static_cast<int>(ldg_bits(row + i)));
+    if ((cm >> bit) & 1u) {
+      if (nc < a.capacity) slots[a.top_k + nc] = item;
+      ++nc;
+    } else {
+      if (nt < a.top_k) slots[a.top_k - 1 - nt] = item;
+      ++nt;
+    }
+  }
+}
 
-  // ---- sweep: classify this CTA's keys ------------------------------------------------------
-  const int begin = blockIdx.x * kChunk;
-  const int end = min(begin + kChunk, row_end);
-  if (begin < end) {
-    float4 v[kSweepLoads];  // all of this thread's loads in flight before any is classified
-#pragma unroll
-    for (int u = 0; u < kSweepLoads; ++u) {
-      const int i = begin + (u * kThreads + tid) * 4;
-      if (i + 3 < end) {
-        v[u] = __ldg(reinterpret_cast<const float4 *>(row + i));
+// Launch 2 (with arrivals): starts once launch 1 has finished and its writes are visible
+// (programmatic dependent launch: griddepcontrol.wait returns only then), so every row's counts
+// are final.  CTA j takes rows j, j + gridDim.x, ...: one thread per row applies the fit rule and
+// writes the slot range of a row that fits (and zeroes its arrivals entry); the rows that do not
+// fit are then repaired one after another by the whole CTA.
+__global__ void __launch_bounds__(kThreads) k_select_finish(const SelectArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
+  extern __shared__ __align__(16) uint8_t select_smem[];
+  __shared__ int s_list[kThreads];  // this round's rows that do not fit
+  __shared__ int s_n;
+  __shared__ int s_c, s_m;
+  __shared__ uint32_t s_v;
+  const int tid = threadIdx.x;
+  const int stride = gridDim.x;
+  const auto clamp_end = [&](int r) {
+    const int e = a.row_ends[r];
+    return e < 0 ? 0 : (e > a.max_context ? a.max_context : e);
+  };
+  for (int first = blockIdx.x; first < a.rows; first += stride * kThreads) {
+    if (tid == 0) s_n = 0;
+    __syncthreads();
+    const int r = first + tid * stride;
+    if (r < a.rows) {
+      const int row_end = clamp_end(r);
+      const int K = row_end < a.top_k ? row_end : a.top_k;
+      const int nc = a.counters[2 * r], nt = a.counters[2 * r + 1];
+      if (row_fits(nc, nt, K, a.top_k, a.capacity)) {
+        a.ranges[r] = a.top_k - min(nt, a.top_k);
+        a.ranges[a.rows + r] = a.top_k + min(nc, a.capacity);
       } else {
-        v[u].x = i < end ? row[i] : 0.0f;
-        v[u].y = i + 1 < end ? row[i + 1] : 0.0f;
-        v[u].z = i + 2 < end ? row[i + 2] : 0.0f;
-        v[u].w = 0.0f;
+        s_list[atomicAdd(&s_n, 1)] = r;
       }
+      a.arrivals[r] = 0;
     }
-    // The thread's candidates and ties as bit masks; one warp scan of both counts and one
-    // atomicAdd per warp and kind reserve all the warp's slots at once (a reservation per
-    // 32 keys would put a round trip to L2 on the path for each of them).
-    static_assert(kSweepLoads * 4 <= 16, "16 keys per thread fit the 16-bit counts");
-    uint32_t cm = 0, tm = 0;
-#pragma unroll
-    for (int u = 0; u < kSweepLoads; ++u) {
-      const int i = begin + (u * kThreads + tid) * 4;
-      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const bool valid = i + k < end;
-        const float s = e[k];
-        cm |= (valid && s > thr ? 1u : 0u) << (4 * u + k);
-        tm |= (valid && !(s > thr) && !(s < thr) ? 1u : 0u) << (4 * u + k);
+    __syncthreads();
+    const int n = s_n;
+    for (int j = 0; j < n; ++j) {
+      const int rr = s_list[j];
+      const int row_end = clamp_end(rr);
+      const int K = row_end < a.top_k ? row_end : a.top_k;
+      int *counter = a.counters + 2 * rr;
+      int2 *slots = reinterpret_cast<int2 *>(a.candidates) +
+                    static_cast<int64_t>(rr) * (a.top_k + a.capacity);
+      repair_any(a.logits + static_cast<int64_t>(rr) * a.row_stride, row_end, K,
+                 a.thresholds[rr], counter[0], counter[1], a.top_k, slots, &s_c, &s_m, &s_v,
+                 select_smem);
+      if (tid == 0) {
+        counter[0] = s_c;
+        counter[1] = s_m;
+        reinterpret_cast<uint32_t *>(a.thresholds)[rr] = s_v;  // v's own bits
+        a.ranges[rr] = a.top_k - s_m;
+        a.ranges[a.rows + rr] = a.top_k + s_c;
       }
-    }
-    const int lane = tid & 31;
-    const int mine = __popc(cm) | (__popc(tm) << 16);  // a warp's sums stay below 2^16
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const int excl = incl - mine;
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    int bc = 0, bt = 0;
-    if (lane == 0) {
-      if (total & 0xFFFF) bc = atomicAdd(counter, total & 0xFFFF);
-      if (total >> 16) bt = atomicAdd(counter + 1, total >> 16);
-    }
-    int nc = __shfl_sync(0xffffffffu, bc, 0) + (excl & 0xFFFF);
-    int nt = __shfl_sync(0xffffffffu, bt, 0) + (excl >> 16);
-    // The few keys taken are re-read (L1 hits) rather than kept in registers.
-    for (uint32_t m = cm | tm; m != 0u; m &= m - 1u) {
-      const int bit = __ffs(m) - 1;
-      const int i = begin + ((bit >> 2) * kThreads + tid) * 4 + (bit & 3);
-      const int2 item = make_int2(i, static_cast<int>(ldg_bits(row + i)));
-      if ((cm >> bit) & 1u) {
-        if (nc < a.capacity) slots[a.top_k + nc] = item;
-        ++nc;
-      } else {
-        if (nt < a.top_k) slots[a.top_k - 1 - nt] = item;
-        ++nt;
-      }
+      __syncthreads();
     }
   }
-  if (a.arrivals == nullptr) return;
-
-  // ---- last CTA of the row: fit test, repair, reset -----------------------------------------
-  __shared__ int s_last, s_fits, s_nc, s_nt;
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.arrivals + r, 1) == static_cast<int>(gridDim.x) - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const int K = row_end < a.top_k ? row_end : a.top_k;
-  if (tid == 0) {
-    // Both counts read at L2 (where the other CTAs' additions landed), the two reads in flight
-    // together.
-    int nc, nt;
-    asm volatile("ld.global.cg.s32 %0, [%2];\n\tld.global.cg.s32 %1, [%3];"
-                 : "=r"(nc), "=r"(nt)
-                 : "l"(counter), "l"(counter + 1)
-                 : "memory");
-    s_nc = nc;
-    s_nt = nt;
-    s_fits = row_fits(nc, nt, K, a.top_k, a.capacity);
-  }
-  __syncthreads();
-  if (s_fits) {
-    if (tid == 0) {
-      a.ranges[r] = a.top_k - min(s_nt, a.top_k);
-      a.ranges[a.rows + r] = a.top_k + min(s_nc, a.capacity);
-    }
-  } else {
-    __shared__ int s_c, s_m;
-    __shared__ uint32_t s_v;
-    repair_any(row, row_end, K, thr, s_nc, s_nt, a.top_k, slots, &s_c, &s_m, &s_v, select_smem);
-    if (tid == 0) {
-      counter[0] = s_c;
-      counter[1] = s_m;
-      reinterpret_cast<uint32_t *>(a.thresholds)[r] = s_v;  // v's own bits
-      a.ranges[r] = a.top_k - s_m;
-      a.ranges[a.rows + r] = a.top_k + s_c;
-    }
-  }
-  if (tid == 0) a.arrivals[r] = 0;
 }
 
 // The last stage of the fused score + select: CTA (b, t) for row r = b * next_n + t, after the
@@ -838,14 +856,23 @@ __global__ void __launch_bounds__(kThreads) k_fused_repair(const FusedRepairArgs
 
 cudaError_t launch_threshold_select(const SelectArgs &args, cudaStream_t stream) {
   const int per_row = args.max_context > 0 ? (args.max_context + kChunk - 1) / kChunk : 1;
-  const dim3 grid(per_row, args.rows);
+  cudaError_t e = launch_dependent(k_select_classify, dim3(per_row, args.rows), dim3(kClsThreads),
+                                   0, stream, args);
+  if (e != cudaSuccess || args.arrivals == nullptr) return e;
   static PerDeviceOnce configured;
-  const cudaError_t e = configured.run([] {
-    return cudaFuncSetAttribute(k_threshold_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = configured.run([] {
+    return cudaFuncSetAttribute(k_select_finish, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kSelectSmem);
   });
   if (e != cudaSuccess) return e;
-  return launch_dependent(k_threshold_select, grid, dim3(kThreads), kSelectSmem, stream, args);
+  // One CTA per row up to one per SM.
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int ctas = args.rows < sms ? args.rows : sms;
+  return launch_dependent(k_select_finish, dim3(ctas), dim3(kThreads), kSelectSmem, stream, args);
 }
 
 cudaError_t launch_fused_repair(const FusedRepairArgs &args, cudaStream_t stream) {
