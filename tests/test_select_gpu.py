@@ -164,7 +164,8 @@ def test_arrivals_stay_zero_across_calls():
 
 @pytest.mark.parametrize("kind", ["normal", "ties"])
 def test_very_long_rows(kind):
-    """Rows of up to 270000 keys (17 sweeping CTAs each), repaired by each row's last CTA."""
+    """Rows of up to 270000 keys (33 classifying CTAs each), each repaired by one CTA of the
+    finishing launch."""
     rows, n = 3, 270000
     x = _synthetic(rows, n, kind, seed=9)
     row_ends = torch.tensor([n, 262145, 70000], dtype=torch.int32)
@@ -179,7 +180,7 @@ def test_very_long_rows(kind):
 
 @pytest.mark.parametrize("max_context", [32768, 100000, 262144])
 def test_row_lengths_around_chunks(max_context):
-    """Rows spread over 2 to 16 sweeping CTAs, with ragged ends around the chunks' borders,
+    """Rows spread over 4 to 32 classifying CTAs, with ragged ends around the chunks' borders,
     thresholds that fit and that force the repair, and a row of many equal keys (the bin of the
     K'-th value too full for the repair's shared-memory buffer)."""
     g = torch.Generator().manual_seed(max_context)
@@ -223,3 +224,38 @@ def test_repair_with_nan_inf_and_signed_zeros(top_k, capacity):
     for t in (torch.full((rows,), math.inf), torch.full((rows,), -math.inf)):
         res = gpu_select(x.cuda(), row_ends.cuda(), t.cuda(), top_k, capacity, n)
         check_selection(lc, row_ends.numpy(), top_k, capacity, res, t.numpy())
+
+
+def test_many_rows_per_finishing_cta():
+    """More rows than SMs: each CTA of the finishing launch applies the fit rule to several rows
+    and repairs several rows one after another.  Lengths from 0 to 20000, thresholds that fit,
+    that force a repair (+inf) and that are a little low (too many candidates for capacity =
+    top_k - 1); arrivals holds garbage on entry (it is only the switch) and is zero after."""
+    g = torch.Generator().manual_seed(404)
+    rows, n = 400, 20000
+    x = torch.randn(rows, n, generator=g)
+    x[7] = torch.randint(-2, 3, (n,), generator=g).to(torch.float32)  # many ties
+    ends = torch.randint(0, n + 1, (rows,), generator=g)
+    ends[:4] = torch.tensor([0, 1, n, 64])
+    row_ends = ends.to(torch.int32)
+    lc = x.numpy()
+    top_k, capacity = 64, 63
+    kth = kth_values(lc.astype(np.float64), row_ends.numpy(), top_k)
+    kth = torch.from_numpy(np.nan_to_num(kth, nan=0.0)).to(torch.float32)
+    kind = torch.arange(rows) % 3
+    thr = torch.where(kind == 0, kth, torch.where(kind == 1, torch.full_like(kth, math.inf),
+                                                   kth - 0.25))
+    d = torch.device("cuda")
+    t = thr.clone().to(d)
+    counters = torch.zeros(rows, 2, dtype=torch.int32, device=d)
+    cand = torch.full((rows, top_k + capacity, 2), -1, dtype=torch.int32, device=d)
+    arrivals = torch.full((rows,), 7, dtype=torch.int32, device=d)
+    ranges = torch.full((2, rows), -1, dtype=torch.int32, device=d)
+    idx.threshold_select(x.to(d), row_ends.to(d), t, counters, cand, top_k, capacity, n,
+                         arrivals=arrivals, ranges=ranges)
+    torch.cuda.synchronize()
+    res = dict(thresholds=t.cpu().numpy(), counters=counters.cpu().numpy(),
+               candidates=cand.cpu().numpy(), arrivals=arrivals.cpu().numpy(),
+               ranges=ranges.cpu().numpy())
+    repaired = check_selection(lc, row_ends.numpy(), top_k, capacity, res, thr.numpy())
+    assert repaired >= rows // 3 - 10  # the +inf rows with at least one key, and more
