@@ -273,8 +273,9 @@ def time_select(w, t, stream, launches: int = 200) -> dict:
     keys = int(w.row_ends().to(torch.int64).sum())
     return {"ms_per_launch": ms, "keys": keys, "keys_per_s": keys / (ms * 1e-3),
             "logits_gbs": 4 * keys / (ms * 1e-3) / 1e9,
-            "note": "reads each row's logits (L2-resident after the logits kernel) once; "
-                    "rows that do not fit are re-read by the last CTA's radix repair"}
+            "note": "two launches (classification; fit rule and repair); reads each row's "
+                    "logits (L2-resident after the logits kernel) once, and rows that do not "
+                    "fit again in their radix repair"}
 
 
 def time_device(w, t, steps, warmup, stream, sampler=None):
@@ -373,7 +374,7 @@ def time_selecting(name: str, dev, steps: int, warmup: int, stream, peaks: dict)
             "all_rows_fit": {"ms_per_step": two_fit, "fused_ms_per_step": fused_fit["ms_per_step"],
                              "thresholds": "each row's K'-th largest score"},
             "kv_roofline_time_ms": t_roof, "kv_roofline_frac": t_roof / two,
-            "note": "step = counter/threshold reset + logits + select (2 kernels, plus 2 small "
+            "note": "step = counter/threshold reset + logits + select (3 kernels, plus 2 small "
                     "torch fills); fused = the same outputs through idx_indexer_threshold_select "
                     "(3 kernels)"}
 
