@@ -259,8 +259,8 @@ int idx_threshold_select(const float *logits, int64_t logits_row_stride, const i
  *   rows   1 .. IDX_STATIC_SELECT_MAX_ROWS; more returns IDX_INVALID_ARG with nothing launched
  *
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
- * that device current) and caches it; make that first call before any stream capture.  Each
- * call clears the counters it uses (an asynchronous memset on `stream`) before its launch.
+ * that device current) and caches it.  Each call clears the counters it uses (an asynchronous
+ * memset on `stream`) before its launches.
  * Every call, on every stream, shares the one array: calls whose work overlaps on the GPU race
  * on it and must be serialised by the caller (one stream, or events).
  */
