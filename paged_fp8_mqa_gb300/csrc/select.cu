@@ -11,7 +11,8 @@
 //
 // With `arrivals`, a second launch (a programmatic dependent: it proceeds only once launch 1 has
 // finished, so every count is final) decides for each row whether it fits and, if not, repairs
-// it with one 1024-thread CTA: an MSB-first radix select over order-preserving uint32 keys (i.e.
+// it with one 1024-thread CTA (one CTA per row, or per SM taking rows in turn when there are
+// more rows than SMs): an MSB-first radix select over order-preserving uint32 keys (i.e.
 // IEEE totalOrder) finds the row's K'-th largest key v, K' = min(row_end, top_k), and the row's
 // keys above v become candidates and its lowest-index keys equal to v ties, K' items in all.  It
 // then rewrites counters, the threshold (v) and ranges, and zeroes arrivals[r] (which nothing
@@ -675,19 +676,10 @@ __device__ __forceinline__ void repair_any(const float *row, int row_end, int K,
   __syncthreads();
 }
 
-// Launch 1: CTA (c, r) classifies keys [c*kChunk, (c+1)*kChunk) of row r below row_ends[r].
-// A CTA past the row's keys leaves at once.
-__global__ void __launch_bounds__(kClsThreads) k_select_classify(const SelectArgs a) {
-  // The previous kernel in the stream may still be running: no global memory before this.
-  griddep_wait();
-  griddep_launch_dependents();
-  const int r = blockIdx.y;
+// Classifies keys [begin, end) of row r (a chunk of at most kChunk keys); every thread of the
+// CTA calls it.
+__device__ __forceinline__ void classify_chunk(const SelectArgs &a, int r, int begin, int end) {
   const int tid = threadIdx.x;
-  int row_end = a.row_ends[r];
-  row_end = row_end < 0 ? 0 : (row_end > a.max_context ? a.max_context : row_end);
-  const int begin = blockIdx.x * kChunk;
-  const int end = min(begin + kChunk, row_end);
-  if (begin >= end) return;
   const float thr = a.thresholds[r];
   const float *row = a.logits + static_cast<int64_t>(r) * a.row_stride;
   int2 *slots = reinterpret_cast<int2 *>(a.candidates) +
@@ -755,11 +747,64 @@ __global__ void __launch_bounds__(kClsThreads) k_select_classify(const SelectArg
   }
 }
 
-// Launch 2 (with arrivals): starts once launch 1 has finished and its writes are visible
-// (programmatic dependent launch: griddepcontrol.wait returns only then), so every row's counts
-// are final.  CTA j takes rows j, j + gridDim.x, ...: one thread per row applies the fit rule and
-// writes the slot range of a row that fits (and zeroes its arrivals entry); the rows that do not
-// fit are then repaired one after another by the whole CTA.
+// Launch 1, one CTA per chunk: CTA (c, r) classifies keys [c*kChunk, (c+1)*kChunk) of row r
+// below row_ends[r]; a CTA past the row's keys leaves at once.
+__global__ void __launch_bounds__(kClsThreads) k_select_classify(const SelectArgs a) {
+  // The previous kernel in the stream may still be running: no global memory before this.
+  griddep_wait();
+  griddep_launch_dependents();
+  const int r = blockIdx.y;
+  int row_end = a.row_ends[r];
+  row_end = row_end < 0 ? 0 : (row_end > a.max_context ? a.max_context : row_end);
+  const int begin = blockIdx.x * kChunk;
+  const int end = min(begin + kChunk, row_end);
+  if (begin >= end) return;
+  classify_chunk(a, r, begin, end);
+}
+
+// Launch 2 (with arrivals), at most one row per SM: CTA r applies the fit rule to row r and
+// repairs it if it does not fit.  It starts once launch 1 has finished and its writes are visible
+// (programmatic dependent launch: griddepcontrol.wait returns only then), so the counts are
+// final.
+__global__ void __launch_bounds__(kThreads) k_select_finish_row(const SelectArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
+  extern __shared__ __align__(16) uint8_t select_smem[];
+  __shared__ int s_c, s_m;
+  __shared__ uint32_t s_v;
+  const int tid = threadIdx.x;
+  const int r = blockIdx.x;
+  int row_end = a.row_ends[r];
+  row_end = row_end < 0 ? 0 : (row_end > a.max_context ? a.max_context : row_end);
+  const int K = row_end < a.top_k ? row_end : a.top_k;
+  int *counter = a.counters + 2 * r;
+  const int nc = counter[0], nt = counter[1];
+  if (row_fits(nc, nt, K, a.top_k, a.capacity)) {
+    if (tid == 0) {
+      a.ranges[r] = a.top_k - min(nt, a.top_k);
+      a.ranges[a.rows + r] = a.top_k + min(nc, a.capacity);
+      a.arrivals[r] = 0;
+    }
+    return;
+  }
+  int2 *slots = reinterpret_cast<int2 *>(a.candidates) +
+                static_cast<int64_t>(r) * (a.top_k + a.capacity);
+  repair_any(a.logits + static_cast<int64_t>(r) * a.row_stride, row_end, K, a.thresholds[r], nc,
+             nt, a.top_k, slots, &s_c, &s_m, &s_v, select_smem);
+  if (tid == 0) {
+    counter[0] = s_c;
+    counter[1] = s_m;
+    reinterpret_cast<uint32_t *>(a.thresholds)[r] = s_v;  // v's own bits
+    a.ranges[r] = a.top_k - s_m;
+    a.ranges[a.rows + r] = a.top_k + s_c;
+    a.arrivals[r] = 0;
+  }
+}
+
+// Launch 2 (with arrivals), more rows than SMs: CTA j takes rows j, j + gridDim.x, ...: one
+// thread per row applies the fit rule and writes the slot range of a row that fits (and zeroes
+// its arrivals entry); the rows that do not fit are then repaired one after another by the
+// whole CTA.
 __global__ void __launch_bounds__(kThreads) k_select_finish(const SelectArgs a) {
   griddep_wait();
   griddep_launch_dependents();
@@ -769,11 +814,11 @@ __global__ void __launch_bounds__(kThreads) k_select_finish(const SelectArgs a) 
   __shared__ int s_c, s_m;
   __shared__ uint32_t s_v;
   const int tid = threadIdx.x;
-  const int stride = gridDim.x;
   const auto clamp_end = [&](int r) {
     const int e = a.row_ends[r];
     return e < 0 ? 0 : (e > a.max_context ? a.max_context : e);
   };
+  const int stride = gridDim.x;
   for (int first = blockIdx.x; first < a.rows; first += stride * kThreads) {
     if (tid == 0) s_n = 0;
     __syncthreads();
@@ -855,24 +900,28 @@ __global__ void __launch_bounds__(kThreads) k_fused_repair(const FusedRepairArgs
 }  // namespace
 
 cudaError_t launch_threshold_select(const SelectArgs &args, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
   const int per_row = args.max_context > 0 ? (args.max_context + kChunk - 1) / kChunk : 1;
-  cudaError_t e = launch_dependent(k_select_classify, dim3(per_row, args.rows), dim3(kClsThreads),
-                                   0, stream, args);
+  e = launch_dependent(k_select_classify, dim3(per_row, args.rows), dim3(kClsThreads), 0, stream,
+                       args);
   if (e != cudaSuccess || args.arrivals == nullptr) return e;
   static PerDeviceOnce configured;
   e = configured.run([] {
+    cudaError_t e2 = cudaFuncSetAttribute(
+        k_select_finish_row, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelectSmem);
+    if (e2 != cudaSuccess) return e2;
     return cudaFuncSetAttribute(k_select_finish, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kSelectSmem);
   });
   if (e != cudaSuccess) return e;
-  // One CTA per row up to one per SM.
-  int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  const int ctas = args.rows < sms ? args.rows : sms;
-  return launch_dependent(k_select_finish, dim3(ctas), dim3(kThreads), kSelectSmem, stream, args);
+  if (args.rows <= sms)
+    return launch_dependent(k_select_finish_row, dim3(args.rows), dim3(kThreads), kSelectSmem,
+                            stream, args);
+  return launch_dependent(k_select_finish, dim3(sms), dim3(kThreads), kSelectSmem, stream, args);
 }
 
 cudaError_t launch_fused_repair(const FusedRepairArgs &args, cudaStream_t stream) {

@@ -259,3 +259,24 @@ def test_many_rows_per_finishing_cta():
                ranges=ranges.cpu().numpy())
     repaired = check_selection(lc, row_ends.numpy(), top_k, capacity, res, thr.numpy())
     assert repaired >= rows // 3 - 10  # the +inf rows with at least one key, and more
+
+
+def test_thousands_of_short_rows():
+    """2500 short rows of 0..3000 keys (16 rows per finishing CTA); thresholds that fit and +inf
+    (a repair for every non-empty row)."""
+    g = torch.Generator().manual_seed(2500)
+    rows, n = 2500, 3000
+    x = torch.randn(rows, n, generator=g)
+    row_ends = torch.randint(0, n + 1, (rows,), generator=g).to(torch.int32)
+    row_ends[:3] = torch.tensor([0, n, 1], dtype=torch.int32)
+    stride = 3072
+    logits = torch.zeros(rows, stride)
+    logits[:, :n] = x
+    lc = logits.numpy()
+    top_k, capacity = 32, 31
+    kth = kth_values(lc.astype(np.float64), row_ends.numpy(), top_k)
+    kth = torch.from_numpy(np.nan_to_num(kth, nan=0.0)).to(torch.float32)
+    thr = torch.where(torch.arange(rows) % 2 == 0, kth, torch.full_like(kth, math.inf))
+    res = gpu_select(logits.cuda(), row_ends.cuda(), thr.cuda(), top_k, capacity, n)
+    repaired = check_selection(lc, row_ends.numpy(), top_k, capacity, res, thr.numpy())
+    assert repaired >= rows // 2 - 10
