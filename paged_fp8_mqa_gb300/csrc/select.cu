@@ -2,7 +2,7 @@
 // indexer_threshold_select": description; Parameters row_ends, thresholds, counters,
 // candidates, max_context, top_k, arrivals, ranges).
 //
-// Launch 1, grid (ceil(max_context / kChunk), rows) of 512-thread CTAs (two per SM): CTA (c, r)
+// Launch 1, grid (rows, ceil(max_context / kChunk)) of 512-thread CTAs (two per SM): CTA (r, c)
 // sweeps keys [c*kChunk, (c+1)*kChunk) of row r below row_ends[r]: s > thr is a candidate,
 // "neither above nor below" (== or NaN) a tie.  Slots are reserved with one atomicAdd per warp
 // and per kind for all the warp's 512 keys (a warp scan of the counts), the n-th candidate going
@@ -747,16 +747,18 @@ __device__ __forceinline__ void classify_chunk(const SelectArgs &a, int r, int b
   }
 }
 
-// Launch 1, one CTA per chunk: CTA (c, r) classifies keys [c*kChunk, (c+1)*kChunk) of row r
-// below row_ends[r]; a CTA past the row's keys leaves at once.
+// Launch 1, one CTA per chunk: CTA (r, c) classifies keys [c*kChunk, (c+1)*kChunk) of row r
+// below row_ends[r]; a CTA past the row's keys leaves at once.  The rows are the grid's fast
+// dimension, so every row's first chunk is dispatched before any row's second: with rows of
+// mixed lengths, the CTAs with keys start in the first wave and those past the ends come last.
 __global__ void __launch_bounds__(kClsThreads) k_select_classify(const SelectArgs a) {
   // The previous kernel in the stream may still be running: no global memory before this.
   griddep_wait();
   griddep_launch_dependents();
-  const int r = blockIdx.y;
+  const int r = blockIdx.x;
   int row_end = a.row_ends[r];
   row_end = row_end < 0 ? 0 : (row_end > a.max_context ? a.max_context : row_end);
-  const int begin = blockIdx.x * kChunk;
+  const int begin = blockIdx.y * kChunk;
   const int end = min(begin + kChunk, row_end);
   if (begin >= end) return;
   classify_chunk(a, r, begin, end);
@@ -906,7 +908,7 @@ cudaError_t launch_threshold_select(const SelectArgs &args, cudaStream_t stream)
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int per_row = args.max_context > 0 ? (args.max_context + kChunk - 1) / kChunk : 1;
-  e = launch_dependent(k_select_classify, dim3(per_row, args.rows), dim3(kClsThreads), 0, stream,
+  e = launch_dependent(k_select_classify, dim3(args.rows, per_row), dim3(kClsThreads), 0, stream,
                        args);
   if (e != cudaSuccess || args.arrivals == nullptr) return e;
   static PerDeviceOnce configured;
