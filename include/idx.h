@@ -233,11 +233,13 @@ int idx_logits_mxfp4(const uint8_t *q, const uint8_t *q_sf, const uint8_t *kv_fu
  *   candidates        device int32 [rows][top_k + capacity][2]
  *   top_k             >= 1 (the number of tie slots)
  *   capacity          >= 0 candidate slots; >= top_k - 1 when arrivals is given
- *   max_context       the most keys a row sees; sizes the grid (one CTA per 8192 keys)
+ *   max_context       the most keys a row sees, at most IDX_SELECT_MAX_CONTEXT; sizes the grid
+ *                     (one CTA per 8192 keys)
  *   arrivals          NULL (no repair), or device int32 [rows] (any contents); every call
  *                     leaves it zeroed
  *   ranges            device int32 [2][rows]; required when arrivals is given, else ignored
  */
+#define IDX_SELECT_MAX_CONTEXT (65535 * 8192)
 int idx_threshold_select(const float *logits, int64_t logits_row_stride, const int32_t *row_ends,
                          int32_t rows, float *thresholds, int32_t *counters, int32_t *candidates,
                          int32_t top_k, int32_t capacity, int32_t max_context, int32_t *arrivals,

@@ -158,6 +158,7 @@ def idx_threshold_select_static(logits, logits_row_stride, row_ends, rows, thres
 
 
 IDX_STATIC_SELECT_MAX_ROWS = 16384
+IDX_SELECT_MAX_CONTEXT = 65535 * 8192
 
 
 def idx_indexer_threshold_select(q, kv_fused, num_blocks, block_size, weights, block_tables,

@@ -576,6 +576,8 @@ IDX_EXPORT int idx_threshold_select(const float *logits, int64_t logits_row_stri
     return fail(IDX_INVALID_ARG, "top_k >= 1, capacity >= 0, max_context >= 0 required");
   if (logits_row_stride < max_context || logits_row_stride % 4 != 0)
     return fail(IDX_INVALID_ARG, "logits_row_stride must be >= max_context and a multiple of 4");
+  if (max_context > IDX_SELECT_MAX_CONTEXT)
+    return fail(IDX_INVALID_ARG, "max_context must be <= IDX_SELECT_MAX_CONTEXT (65535 * 8192)");
   if (!aligned(logits, 16)) return fail(IDX_INVALID_ARG, "logits must be 16-byte aligned");
   if (!aligned(candidates, 8) || !aligned(counters, 4) || !aligned(thresholds, 4) ||
       !aligned(row_ends, 4))
@@ -624,6 +626,8 @@ IDX_EXPORT int idx_threshold_select_static(const float *logits, int64_t logits_r
   if (capacity < top_k - 1) return fail(IDX_INVALID_ARG, "capacity must be >= top_k - 1");
   if (logits_row_stride < max_context || logits_row_stride % 4 != 0)
     return fail(IDX_INVALID_ARG, "logits_row_stride must be >= max_context and a multiple of 4");
+  if (max_context > IDX_SELECT_MAX_CONTEXT)
+    return fail(IDX_INVALID_ARG, "max_context must be <= IDX_SELECT_MAX_CONTEXT (65535 * 8192)");
   if (!aligned(logits, 16)) return fail(IDX_INVALID_ARG, "logits must be 16-byte aligned");
   if (!aligned(candidates, 8) || !aligned(counters, 4) || !aligned(thresholds, 4) ||
       !aligned(row_ends, 4) || !aligned(ranges, 4))

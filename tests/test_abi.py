@@ -98,6 +98,7 @@ def test_logits_rejects_bad_arguments(lib, over, code):
     (dict(ranges=None), idx.IDX_INVALID_ARG),
     (dict(capacity=10), idx.IDX_INVALID_ARG),
     (dict(candidates=P((1 << 20) + 4)), idx.IDX_INVALID_ARG),
+    (dict(max_context=65535 * 8192 + 1, logits_row_stride=65536 * 8192), idx.IDX_INVALID_ARG),
 ])
 def test_select_rejects_bad_arguments(lib, over, code):
     a = dict(logits=FAKE, logits_row_stride=1024, row_ends=FAKE, rows=4, thresholds=FAKE,
