@@ -472,7 +472,7 @@ __device__ bool repair_row_fast(const float *row, int row_end, int K, int top_k,
                             cand_out, tie_out, thr_out);
 }
 
-// Repairs row `r` (called by every thread of the row's last CTA): see the file comment.
+// Repairs a row (called by every thread of the repairing CTA): see the file comment.
 __device__ void repair_row(const float *row, int row_end, int K, int top_k, int2 *slots,
                            int *cand_out, int *tie_out, uint32_t *thr_out) {
   __shared__ unsigned s_hist[256];
